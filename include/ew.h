@@ -1,0 +1,187 @@
+/*
+ * ew.h -- C ABI of libew.so, memory-bound elementwise operators for GB300
+ * (sm_103a).
+ *
+ * Operations (each output element depends only on the same index of the
+ * inputs, "逐元素操作算子" §一.1, except the gather):
+ *
+ *   ew_add            C[i] = A[i] + B[i]
+ *                     "HyperAI elementwise add on RTX 5090" (hyper.ai), Versions
+ *                     1-6; "逐元素操作算子" §二 template kernel.
+ *   ew_saxpy          y[i] = alpha * x[i] + y[i], in place, one fused multiply-add
+ *                     "Puzzle 31: occupancy optimisation" (puzzles.modular.com),
+ *                     overview and minimal kernel.
+ *   ew_relu           y[i] = max(x[i], 0)
+ *                     CUDA-MODE lecture notes (cyqw.cn/news/898472), §5.2 example 1.
+ *   ew_copy           out[i] = in[i]
+ *                     CUDA-MODE lecture notes, §3.2 coalesced version.
+ *   ew_gather_stride  out[i] = in[(stride * i) mod n]
+ *                     CUDA-MODE lecture notes, §3.2 non-coalesced version (stride 2).
+ *
+ * Arithmetic (bit-exact, no tolerance):
+ *   f32 add      IEEE binary32 addition, round to nearest even; subnormals kept.
+ *   f16/bf16 add the exact sum rounded once to the format, nearest even.  This
+ *                equals "binary32 add, then one rounding" (binary32 carries more
+ *                than 2p+1 significand bits for both formats).
+ *   saxpy        f32: fmaf(alpha, x, y), one rounding.  f16/bf16: x and y widened
+ *                exactly to binary32, fmaf there, then one rounding to the format.
+ *                alpha is binary32 and is never rounded to the 16-bit format.
+ *   relu         x > 0 -> x;  x <= 0 (including -0) -> +0;  NaN -> x unchanged.
+ *   copy/gather  raw element bits.
+ *
+ * Common conventions
+ *   Pointers   device pointers (cudaMalloc, cudaMallocAsync, or any memory the
+ *              current device can address), owned by the caller.  The library
+ *              allocates no memory and keeps no reference after a call returns.
+ *              Each pointer must be aligned to the element size (4 bytes for
+ *              EW_F32, 2 for EW_F16/EW_BF16), else EW_ERR_INVALID_VALUE.  Any
+ *              such alignment is accepted; the widest vector width that all the
+ *              pointers of a call share is used (see ew_plan_query).
+ *   Layout     n contiguous elements, index 0 first.
+ *   n          element count.  n == 0 returns EW_OK and launches nothing;
+ *              n < 0 is EW_ERR_INVALID_VALUE.
+ *   Aliasing   an output may be *identical* to an input (in-place add, saxpy
+ *              with x == y, relu, copy).  Any other overlap of an output's byte
+ *              range with an input's is EW_ERR_OVERLAP.  ew_gather_stride
+ *              accepts no overlap at all.
+ *   Streams    every call enqueues at most one kernel on `stream` (NULL = the
+ *              legacy default stream) on the calling thread's current device and
+ *              returns without synchronising.  Device faults surface at the
+ *              caller's next synchronisation.
+ *   Errors     every call returns an ew_status and never prints or aborts.
+ *              Argument errors are detected on the host before any CUDA call.
+ *              EW_ERR_CUDA: a CUDA runtime call or the launch failed; the
+ *              cudaError_t value is kept per thread (ew_last_cuda_error).
+ *   Threads    all entry points are thread-safe.  The variant selection
+ *              (ew_set_path) is process-wide.
+ */
+#ifndef EW_H
+#define EW_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define EW_API __attribute__((visibility("default")))
+#else
+#define EW_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t (struct CUstream_st *), so no CUDA header is needed. */
+typedef struct CUstream_st *ew_stream_t;
+
+typedef enum {
+    EW_F32 = 0,  /* IEEE binary32 */
+    EW_F16 = 1,  /* IEEE binary16 */
+    EW_BF16 = 2  /* bfloat16 (upper half of binary32) */
+} ew_dtype;
+
+typedef enum {
+    EW_OK = 0,
+    EW_ERR_INVALID_VALUE = 1,     /* n < 0, stride <= 0, misaligned pointer, bad enum */
+    EW_ERR_NULL_POINTER = 2,      /* a NULL pointer with n > 0 */
+    EW_ERR_UNSUPPORTED_DTYPE = 3, /* dtype outside ew_dtype */
+    EW_ERR_OVERLAP = 4,           /* partial overlap between an input and the output */
+    EW_ERR_NOT_DEVICE_POINTER = 5,/* pointer check enabled and a pointer is not device-accessible */
+    EW_ERR_CUDA = 6,              /* CUDA runtime error; see ew_last_cuda_error */
+    EW_ERR_TIMEOUT = 7            /* a bounded device-side wait gave up (see ew_device_error) */
+} ew_status;
+
+/* Kernel variant for the body of a call.  EW_PATH_AUTO picks the fastest
+ * measured variant that the pointers' alignment allows. */
+typedef enum {
+    EW_PATH_AUTO = 0,
+    EW_PATH_SCALAR = 1, /* one element per access, grid-stride */
+    EW_PATH_V128 = 2,   /* 16-byte vector accesses */
+    EW_PATH_V256 = 3,   /* 32-byte vector accesses (sm_100 family) */
+    EW_PATH_TMA = 4     /* bulk async copies (cp.async.bulk) through shared memory */
+} ew_path;
+
+/* ---- operators ------------------------------------------------------- */
+
+/* C = A + B.  a, b: n input elements; c: n output elements (c may be a or b). */
+EW_API ew_status ew_add(ew_dtype dtype, const void *a, const void *b, void *c, int64_t n,
+                 ew_stream_t stream);
+
+/* y = alpha * x + y in place.  x: n inputs; y: n inputs overwritten with the
+ * result (x == y is allowed). */
+EW_API ew_status ew_saxpy(ew_dtype dtype, float alpha, const void *x, void *y, int64_t n,
+                   ew_stream_t stream);
+
+/* y = max(x, 0).  x: n inputs; y: n outputs (y == x computes in place). */
+EW_API ew_status ew_relu(ew_dtype dtype, const void *x, void *y, int64_t n, ew_stream_t stream);
+
+/* out = in.  in == out is a no-op that launches nothing. */
+EW_API ew_status ew_copy(ew_dtype dtype, const void *in, void *out, int64_t n, ew_stream_t stream);
+
+/* out[i] = in[(stride * i) mod n] for i in [0, n); the product is formed
+ * without overflow.  stride >= 1 (else EW_ERR_INVALID_VALUE).  in and out must
+ * not overlap.  As in the page's non-coalesced copy, each thread reads one
+ * element per access, so a warp's load touches every stride-th element of a
+ * span while its store covers consecutive elements. */
+EW_API ew_status ew_gather_stride(ew_dtype dtype, const void *in, void *out, int64_t n,
+                           int64_t stride, ew_stream_t stream);
+
+/* ---- variant selection and introspection ------------------------------ */
+
+/* Select the kernel variant for later calls in this process (EW_PATH_AUTO
+ * restores the default).  A forced variant that the alignment of a call does
+ * not allow falls back to the widest one it does.  EW_ERR_INVALID_VALUE for a
+ * value outside ew_path. */
+EW_API ew_status ew_set_path(ew_path path);
+EW_API ew_path ew_get_path(void);
+
+/* Enable (1) or disable (0, the default) a cudaPointerGetAttributes check of
+ * every pointer before launch; a pointer the device cannot access then gives
+ * EW_ERR_NOT_DEVICE_POINTER.  Process-wide. */
+EW_API ew_status ew_set_pointer_check(int enable);
+
+/* How an ew_add / ew_saxpy / ew_relu / ew_copy call with these pointers is
+ * split under the current ew_set_path selection (host arithmetic only; needs no
+ * GPU).  ptrs: the call's input and output pointers; nptrs in [1, 4]. */
+typedef struct {
+    int32_t path;      /* ew_path that will run */
+    int32_t vec_bytes; /* bytes per access in the body (element size for SCALAR) */
+    int64_t head;      /* leading elements done one by one, to reach vector alignment */
+    int64_t nvec;      /* whole vectors in the body */
+    int64_t tail;      /* trailing elements done one by one */
+} ew_plan;
+EW_API ew_status ew_plan_query(ew_dtype dtype, const void *const *ptrs, int32_t nptrs, int64_t n,
+                        ew_plan *out);
+
+/* What the most recent operator call on this thread launched. */
+typedef struct {
+    int32_t launches;  /* kernels enqueued by the call (0 or 1) */
+    int32_t path;      /* ew_path that ran */
+    int32_t vec_bytes;
+    int32_t grid;      /* blocks */
+    int32_t block;     /* threads per block */
+    int32_t smem;      /* dynamic shared memory bytes per block */
+    int64_t head, nvec, tail;
+} ew_launch_record;
+EW_API ew_status ew_last_launch(ew_launch_record *out);
+
+/* ---- errors ----------------------------------------------------------- */
+
+EW_API const char *ew_status_string(ew_status status);
+
+/* cudaError_t value behind the last EW_ERR_CUDA returned on this thread (0 if none). */
+EW_API int ew_last_cuda_error(void);
+
+/* Read and clear the device-side error word of the current device after
+ * synchronising `stream`.  *code = 0 when no bounded wait has given up since the
+ * last read; otherwise the wait site that gave up.  Returns EW_ERR_TIMEOUT when
+ * *code != 0, EW_ERR_CUDA when the synchronisation itself fails. */
+EW_API ew_status ew_device_error(ew_stream_t stream, int32_t *code);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+EW_API int ew_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EW_H */

@@ -1,0 +1,357 @@
+// ew_api.cu -- the C ABI declared in include/ew.h: argument validation,
+// alignment planning, launch geometry and dispatch to the kernel tables.
+//
+// Validation happens entirely on the host, before any CUDA runtime call, so
+// argument errors never reach the GPU.
+//
+// Launch geometry ("逐元素操作算子" §二: a grid sized by the SM count rather
+// than by N; CUDA-MODE lecture notes §4.2 wave quantization and §4.4 the
+// occupancy calculator): grid = min(SMs x resident blocks per SM from the
+// occupancy API, blocks needed to give every thread one unrolled iteration).
+// The grid is thus at most one full wave and each thread strides through the
+// body, so there is no partial last wave of blocks.
+#include <algorithm>
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include <cuda_runtime.h>
+
+#include "ew.h"
+#include "ew_internal.h"
+
+using namespace ew;
+
+namespace {
+
+std::atomic<int> g_path{EW_PATH_AUTO};
+std::atomic<int> g_pointer_check{-1};  // -1: not yet read from the environment
+
+thread_local int t_last_cuda_error = 0;
+thread_local ew_launch_record t_last{};
+
+int elem_size(ew_dtype dt) { return dt == EW_F32 ? 4 : 2; }
+bool dtype_ok(int dt) { return dt == EW_F32 || dt == EW_F16 || dt == EW_BF16; }
+
+ew_status cuda_fail(cudaError_t e) {
+    t_last_cuda_error = static_cast<int>(e);
+    return EW_ERR_CUDA;
+}
+
+// byte ranges [p, p+len) and [q, q+len) share a byte
+bool overlaps(const void *p, const void *q, int64_t len) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(q);
+    return a < b + static_cast<uintptr_t>(len) && b < a + static_cast<uintptr_t>(len);
+}
+
+// ---------------------------------------------------------------- planning
+
+int path_cap_bytes(int path, int e) {
+    switch (path) {
+        case EW_PATH_SCALAR: return e;
+        case EW_PATH_V128: return 16;
+        default: return 32;  // AUTO, V256, TMA
+    }
+}
+
+// Widest vector width (<= cap) at which all pointers sit at the same offset;
+// the head brings that common offset to zero.
+ew_plan make_plan(int path, int e, const uintptr_t *p, int np, int64_t n) {
+    int vb = e;
+    for (int w = path_cap_bytes(path, e); w > e; w >>= 1) {
+        bool same = true;
+        for (int k = 1; k < np; ++k) same = same && (p[k] % w == p[0] % w);
+        if (same) { vb = w; break; }
+    }
+    ew_plan pl{};
+    pl.vec_bytes = vb;
+    int64_t head = (vb == e) ? 0 : static_cast<int64_t>((vb - p[0] % vb) % vb) / e;
+    head = std::min<int64_t>(head, n);
+    const int64_t per = vb / e;
+    pl.head = head;
+    pl.nvec = (n - head) / per;
+    pl.tail = n - head - pl.nvec * per;
+    pl.path = (vb == 32) ? EW_PATH_V256 : (vb == 16) ? EW_PATH_V128 : EW_PATH_SCALAR;
+    if (path == EW_PATH_TMA && vb >= 16) pl.path = EW_PATH_TMA;
+    return pl;
+}
+
+int resolved_path() {
+    const int p = g_path.load(std::memory_order_relaxed);
+    return p == EW_PATH_AUTO ? EW_PATH_V256 : p;
+}
+
+// ---------------------------------------------------------------- devices
+
+struct DevInfo { int sms = 0; };
+std::mutex g_mu;
+std::map<int, DevInfo> g_dev;
+std::map<std::pair<int, const void *>, int> g_occ;
+
+cudaError_t device_info(int *dev, int *sms) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_dev.find(*dev);
+    if (it == g_dev.end()) {
+        DevInfo d;
+        e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, *dev);
+        if (e != cudaSuccess) return e;
+        it = g_dev.emplace(*dev, d).first;
+    }
+    *sms = it->second.sms;
+    return cudaSuccess;
+}
+
+cudaError_t blocks_per_sm(int dev, const void *kernel, int block, int smem, int *out) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto key = std::make_pair(dev, kernel);
+    auto it = g_occ.find(key);
+    if (it == g_occ.end()) {
+        int b = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, block, smem);
+        if (e != cudaSuccess) return e;
+        it = g_occ.emplace(key, std::max(b, 1)).first;
+    }
+    *out = it->second;
+    return cudaSuccess;
+}
+
+bool pointer_check_enabled() {
+    int v = g_pointer_check.load(std::memory_order_relaxed);
+    if (v < 0) {
+        const char *s = std::getenv("EW_CHECK_POINTERS");
+        v = (s && s[0] == '1') ? 1 : 0;
+        g_pointer_check.store(v, std::memory_order_relaxed);
+    }
+    return v == 1;
+}
+
+ew_status check_device_pointers(const void *const *p, int np) {
+    for (int k = 0; k < np; ++k) {
+        cudaPointerAttributes at{};
+        cudaError_t e = cudaPointerGetAttributes(&at, p[k]);
+        if (e != cudaSuccess) { cudaGetLastError(); return EW_ERR_NOT_DEVICE_POINTER; }
+        if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged)
+            return EW_ERR_NOT_DEVICE_POINTER;
+    }
+    return EW_OK;
+}
+
+// ---------------------------------------------------------------- dispatch
+
+const StreamEntry *table_for(int dt) {
+    return dt == EW_F32 ? stream_table_f32() : dt == EW_F16 ? stream_table_f16() : stream_table_bf16();
+}
+
+// Common path of add / saxpy / relu / copy once arguments are valid.
+ew_status run_stream(int op, ew_dtype dt, const void *in0, const void *in1, void *out,
+                     int64_t n, float alpha, cudaStream_t s) {
+    t_last = ew_launch_record{};
+    const int e = elem_size(dt);
+    const void *ptrs[3] = {in0, out, in1};
+    const int np = (in1 != nullptr) ? 3 : 2;
+    uintptr_t up[3];
+    for (int k = 0; k < np; ++k) up[k] = reinterpret_cast<uintptr_t>(ptrs[k]);
+    const ew_plan pl = make_plan(resolved_path(), e, up, np, n);
+
+    if (pointer_check_enabled()) {
+        ew_status st = check_device_pointers(ptrs, np);
+        if (st != EW_OK) return st;
+    }
+    int dev = 0, sms = 0;
+    cudaError_t ce = device_info(&dev, &sms);
+    if (ce != cudaSuccess) return cuda_fail(ce);
+
+    StreamArgs a{in0, in1, out, n, pl.head, pl.nvec, pl.head + pl.nvec * (pl.vec_bytes / e), alpha};
+
+    // copy of 16-bit elements is one kernel for both 16-bit formats
+    const int tdt = (op == OP_COPY && dt == EW_BF16) ? EW_F16 : dt;
+    const StreamEntry &ent = table_for(tdt)[op * 5 + vec_index(pl.vec_bytes)];
+    if (ent.launch == nullptr) return EW_ERR_INVALID_VALUE;
+
+    int occ = 1;
+    ce = blocks_per_sm(dev, ent.kernel, kBlock, 0, &occ);
+    if (ce != cudaSuccess) return cuda_fail(ce);
+    const int64_t per_block = static_cast<int64_t>(kBlock) * ent.unroll;
+    const int64_t want = std::max<int64_t>((pl.nvec + per_block - 1) / per_block,
+                                           (pl.head + pl.tail + kBlock - 1) / kBlock);
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(sms) * occ)));
+
+    ce = ent.launch(a, grid, s);
+    if (ce != cudaSuccess) return cuda_fail(ce);
+    t_last.launches = 1;
+    t_last.path = pl.path == EW_PATH_TMA ? EW_PATH_V256 : pl.path;
+    t_last.vec_bytes = pl.vec_bytes;
+    t_last.grid = grid;
+    t_last.block = kBlock;
+    t_last.smem = 0;
+    t_last.head = pl.head;
+    t_last.nvec = pl.nvec;
+    t_last.tail = pl.tail;
+    return EW_OK;
+}
+
+// Shared argument checks: dtype, n, null pointers, element alignment.
+ew_status check_common(ew_dtype dt, int64_t n, const void *const *p, int np) {
+    if (!dtype_ok(static_cast<int>(dt))) return EW_ERR_UNSUPPORTED_DTYPE;
+    if (n < 0) return EW_ERR_INVALID_VALUE;
+    if (n == 0) return EW_OK;
+    for (int k = 0; k < np; ++k)
+        if (p[k] == nullptr) return EW_ERR_NULL_POINTER;
+    const uintptr_t e = static_cast<uintptr_t>(elem_size(dt));
+    for (int k = 0; k < np; ++k)
+        if (reinterpret_cast<uintptr_t>(p[k]) % e != 0) return EW_ERR_INVALID_VALUE;
+    if (n > INT64_MAX / 8) return EW_ERR_INVALID_VALUE;
+    return EW_OK;
+}
+
+// An output may equal an input exactly; any other shared byte is an error.
+ew_status check_alias(const void *in, const void *out, int64_t bytes) {
+    if (in == out) return EW_OK;
+    return overlaps(in, out, bytes) ? EW_ERR_OVERLAP : EW_OK;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- C ABI
+
+extern "C" {
+
+ew_status ew_add(ew_dtype dt, const void *a, const void *b, void *c, int64_t n, ew_stream_t s) {
+    t_last = ew_launch_record{};
+    const void *p[3] = {a, b, c};
+    ew_status st = check_common(dt, n, p, 3);
+    if (st != EW_OK || n == 0) return st;
+    const int64_t bytes = n * elem_size(dt);
+    if ((st = check_alias(a, c, bytes)) != EW_OK) return st;
+    if ((st = check_alias(b, c, bytes)) != EW_OK) return st;
+    return run_stream(OP_ADD, dt, a, b, c, n, 0.0f, reinterpret_cast<cudaStream_t>(s));
+}
+
+ew_status ew_saxpy(ew_dtype dt, float alpha, const void *x, void *y, int64_t n, ew_stream_t s) {
+    t_last = ew_launch_record{};
+    const void *p[2] = {x, y};
+    ew_status st = check_common(dt, n, p, 2);
+    if (st != EW_OK || n == 0) return st;
+    if ((st = check_alias(x, y, n * elem_size(dt))) != EW_OK) return st;
+    return run_stream(OP_SAXPY, dt, x, y, y, n, alpha, reinterpret_cast<cudaStream_t>(s));
+}
+
+ew_status ew_relu(ew_dtype dt, const void *x, void *y, int64_t n, ew_stream_t s) {
+    t_last = ew_launch_record{};
+    const void *p[2] = {x, y};
+    ew_status st = check_common(dt, n, p, 2);
+    if (st != EW_OK || n == 0) return st;
+    if ((st = check_alias(x, y, n * elem_size(dt))) != EW_OK) return st;
+    return run_stream(OP_RELU, dt, x, nullptr, y, n, 0.0f, reinterpret_cast<cudaStream_t>(s));
+}
+
+ew_status ew_copy(ew_dtype dt, const void *in, void *out, int64_t n, ew_stream_t s) {
+    t_last = ew_launch_record{};
+    const void *p[2] = {in, out};
+    ew_status st = check_common(dt, n, p, 2);
+    if (st != EW_OK || n == 0) return st;
+    if ((st = check_alias(in, out, n * elem_size(dt))) != EW_OK) return st;
+    if (in == out) return EW_OK;  // nothing to move
+    return run_stream(OP_COPY, dt, in, nullptr, out, n, 0.0f, reinterpret_cast<cudaStream_t>(s));
+}
+
+ew_status ew_gather_stride(ew_dtype dt, const void *in, void *out, int64_t n, int64_t stride,
+                           ew_stream_t s) {
+    t_last = ew_launch_record{};
+    const void *p[2] = {in, out};
+    ew_status st = check_common(dt, n, p, 2);
+    if (st != EW_OK) return st;
+    if (stride <= 0) return EW_ERR_INVALID_VALUE;
+    if (n == 0) return EW_OK;
+    if (overlaps(in, out, n * elem_size(dt))) return EW_ERR_OVERLAP;
+    if (pointer_check_enabled()) {
+        if ((st = check_device_pointers(p, 2)) != EW_OK) return st;
+    }
+    int dev = 0, sms = 0;
+    cudaError_t ce = device_info(&dev, &sms);
+    if (ce != cudaSuccess) return cuda_fail(ce);
+    const GatherEntry *g = (dt == EW_F32) ? gather_entry_4() : gather_entry_2();
+    int occ = 1;
+    ce = blocks_per_sm(dev, g->kernel, kBlock, 0, &occ);
+    if (ce != cudaSuccess) return cuda_fail(ce);
+    const int64_t per_block = static_cast<int64_t>(kBlock) * g->unroll;
+    const int64_t want = (n + per_block - 1) / per_block;
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(sms) * occ)));
+    const uint64_t un = static_cast<uint64_t>(n);
+    const uint64_t nthr = static_cast<uint64_t>(grid) * kBlock;
+    GatherArgs ga{in, out, un, static_cast<uint64_t>(stride) % un,
+                  static_cast<uint64_t>((static_cast<unsigned __int128>(static_cast<uint64_t>(stride)) * nthr) % un)};
+    ce = g->launch(ga, grid, reinterpret_cast<cudaStream_t>(s));
+    if (ce != cudaSuccess) return cuda_fail(ce);
+    t_last.launches = 1;
+    t_last.path = EW_PATH_SCALAR;
+    t_last.vec_bytes = elem_size(dt);
+    t_last.grid = grid;
+    t_last.block = kBlock;
+    t_last.nvec = n;
+    return EW_OK;
+}
+
+ew_status ew_set_path(ew_path path) {
+    const int p = static_cast<int>(path);
+    if (p < EW_PATH_AUTO || p > EW_PATH_TMA) return EW_ERR_INVALID_VALUE;
+    g_path.store(p, std::memory_order_relaxed);
+    return EW_OK;
+}
+
+ew_path ew_get_path(void) { return static_cast<ew_path>(g_path.load(std::memory_order_relaxed)); }
+
+ew_status ew_set_pointer_check(int enable) {
+    if (enable != 0 && enable != 1) return EW_ERR_INVALID_VALUE;
+    g_pointer_check.store(enable, std::memory_order_relaxed);
+    return EW_OK;
+}
+
+ew_status ew_plan_query(ew_dtype dt, const void *const *ptrs, int32_t nptrs, int64_t n, ew_plan *out) {
+    if (out == nullptr || ptrs == nullptr) return EW_ERR_NULL_POINTER;
+    if (nptrs < 1 || nptrs > 4) return EW_ERR_INVALID_VALUE;
+    ew_status st = check_common(dt, n, ptrs, nptrs);
+    if (st != EW_OK) return st;
+    uintptr_t up[4];
+    for (int k = 0; k < nptrs; ++k) up[k] = reinterpret_cast<uintptr_t>(ptrs[k]);
+    *out = make_plan(resolved_path(), elem_size(dt), up, nptrs, n);
+    return EW_OK;
+}
+
+ew_status ew_last_launch(ew_launch_record *out) {
+    if (out == nullptr) return EW_ERR_NULL_POINTER;
+    *out = t_last;
+    return EW_OK;
+}
+
+const char *ew_status_string(ew_status st) {
+    switch (st) {
+        case EW_OK: return "EW_OK";
+        case EW_ERR_INVALID_VALUE: return "EW_ERR_INVALID_VALUE: bad size, stride, alignment or enum";
+        case EW_ERR_NULL_POINTER: return "EW_ERR_NULL_POINTER: null pointer with n > 0";
+        case EW_ERR_UNSUPPORTED_DTYPE: return "EW_ERR_UNSUPPORTED_DTYPE: dtype is not f32, f16 or bf16";
+        case EW_ERR_OVERLAP: return "EW_ERR_OVERLAP: output partially overlaps an input";
+        case EW_ERR_NOT_DEVICE_POINTER: return "EW_ERR_NOT_DEVICE_POINTER: pointer not accessible by the device";
+        case EW_ERR_CUDA: return "EW_ERR_CUDA: CUDA runtime error (see ew_last_cuda_error)";
+        case EW_ERR_TIMEOUT: return "EW_ERR_TIMEOUT: a bounded device wait gave up";
+    }
+    return "unknown ew_status";
+}
+
+int ew_last_cuda_error(void) { return t_last_cuda_error; }
+
+ew_status ew_device_error(ew_stream_t s, int32_t *code) {
+    if (code == nullptr) return EW_ERR_NULL_POINTER;
+    cudaError_t e = read_and_clear_device_error(reinterpret_cast<cudaStream_t>(s), code);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return *code != 0 ? EW_ERR_TIMEOUT : EW_OK;
+}
+
+int ew_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,78 @@
+// ew_internal.h -- interface between the host dispatcher (ew_api.cu) and the
+// kernel translation units (ew_kernels_*.cu, ew_tma.cu).  Not installed.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace ew {
+
+constexpr int kBlock = 256;  // threads per block for the LSU kernels
+
+// Operator ids of the streaming (contiguous) kernels.
+enum OpId : int { OP_ADD = 0, OP_SAXPY = 1, OP_RELU = 2, OP_COPY = 3, OP_COUNT = 4 };
+// dtype ids match ew_dtype.
+enum DtId : int { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2, DT_COUNT = 3 };
+
+// Vector widths in bytes, indexed 0..4 -> 32, 16, 8, 4, 2.
+constexpr int kVecBytes[5] = {32, 16, 8, 4, 2};
+inline int vec_index(int vb) {
+    return vb == 32 ? 0 : vb == 16 ? 1 : vb == 8 ? 2 : vb == 4 ? 3 : 4;
+}
+
+// Arguments of one streaming launch.  Elements [0, head) and [tail0, n) are
+// done one by one; the body is nvec vectors starting at element head.
+struct StreamArgs {
+    const void *in0;  // A (add), x (saxpy), x (relu), in (copy)
+    const void *in1;  // B (add), y (saxpy); unused otherwise
+    void *out;        // C (add), y (saxpy), y (relu), out (copy)
+    int64_t n;
+    int64_t head;
+    int64_t nvec;
+    int64_t tail0;
+    float alpha;
+};
+
+using StreamLaunchFn = cudaError_t (*)(const StreamArgs &, int grid, cudaStream_t);
+
+struct StreamEntry {
+    const void *kernel;     // for occupancy queries
+    StreamLaunchFn launch;  // nullptr where the width does not apply
+    int unroll;             // vectors in flight per thread per input
+};
+
+// Tables filled by the kernel translation units: [op][vec_index].
+const StreamEntry *stream_table_f32();   // OP_COUNT x 5
+const StreamEntry *stream_table_f16();
+const StreamEntry *stream_table_bf16();
+
+// Strided gather: out[i] = in[(s*i) mod n].
+struct GatherArgs {
+    const void *in;
+    void *out;
+    uint64_t n;
+    uint64_t s_mod;      // stride mod n
+    uint64_t step_mod;   // (stride * grid_threads) mod n
+};
+using GatherLaunchFn = cudaError_t (*)(const GatherArgs &, int grid, cudaStream_t);
+struct GatherEntry {
+    const void *kernel;
+    GatherLaunchFn launch;
+    int unroll;
+};
+const GatherEntry *gather_entry_4();  // binary32
+const GatherEntry *gather_entry_2();  // 16-bit types
+
+// Bulk-copy (cp.async.bulk) staging variant of the streaming kernels.
+struct TmaEntry {
+    const void *kernel;
+    StreamLaunchFn launch;  // grid = persistent CTAs; smem fixed per kernel
+    int smem_bytes;
+    int block;
+};
+// Returns nullptr where no bulk-copy kernel exists for (op, dtype).
+const TmaEntry *tma_entry(int op, int dtype);
+// Device error word written by bounded waits (read and cleared by the host).
+cudaError_t read_and_clear_device_error(cudaStream_t s, int32_t *code);
+
+}  // namespace ew

@@ -1,0 +1,144 @@
+// ew_kernels.cuh -- the streaming (load, operate, store) kernel and the
+// strided-gather kernel, as templates instantiated per operator and width by
+// ew_kernels_{f32,f16,bf16}.cu.
+//
+// Streaming kernel ("逐元素操作算子" §二: template kernel, grid-stride loop,
+// float4 body with scalar tail; "HyperAI elementwise add", Versions 5-6:
+// several wide loads in flight per thread):
+//   * persistent grid: at most (SM count x resident blocks per SM) blocks, each
+//     thread walks the body with a grid stride;
+//   * each iteration issues U independent VB-byte loads per input before any
+//     arithmetic, then U VB-byte stores;
+//   * the few elements before the first VB-aligned address (head) and after
+//     the last whole vector (tail) are done one by one by the first threads of
+//     the grid, in the same launch.
+#pragma once
+
+#include "ew_device.cuh"
+#include "ew_internal.h"
+
+namespace ew {
+
+template <class Op> __device__ __forceinline__ Op make_op(float) { return Op{}; }
+template <> __device__ __forceinline__ OpSaxpyF32 make_op<OpSaxpyF32>(float a) { return OpSaxpyF32{a}; }
+template <> __device__ __forceinline__ OpSaxpyF16 make_op<OpSaxpyF16>(float a) { return OpSaxpyF16{a}; }
+template <> __device__ __forceinline__ OpSaxpyBF16 make_op<OpSaxpyBF16>(float a) { return OpSaxpyBF16{a}; }
+
+template <class Op, int VB, int U>
+__global__ void __launch_bounds__(kBlock) stream_kernel(const StreamArgs a) {
+    const Op op = make_op<Op>(a.alpha);
+    constexpr int E = Op::kElem;
+    const char *in0 = static_cast<const char *>(a.in0);
+    const char *in1 = static_cast<const char *>(a.in1);
+    char *out = static_cast<char *>(a.out);
+    const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+
+    // scalar head [0, head) and tail [tail0, n)
+    if (t < a.head) apply_one(op, in0, in1, out, t * E);
+    if (t < a.n - a.tail0) apply_one(op, in0, in1, out, (a.tail0 + t) * E);
+
+    // vector body
+    const int64_t base = a.head * E;
+    const char *b0 = in0 + base;
+    const char *b1 = (Op::kIn == 2) ? in1 + base : nullptr;
+    char *bo = out + base;
+    const int64_t nvec = a.nvec;
+    int64_t v = t;
+    for (; v + (U - 1) * nthr < nvec; v += U * nthr) {
+        Vec<VB> x[U], y[U];
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+            x[j] = ld<VB>(b0 + (v + j * nthr) * VB);
+            if constexpr (Op::kIn == 2) y[j] = ld<VB>(b1 + (v + j * nthr) * VB);
+            else y[j] = x[j];
+        }
+#pragma unroll
+        for (int j = 0; j < U; ++j) st<VB>(bo + (v + j * nthr) * VB, apply<Op, VB>(op, x[j], y[j]));
+    }
+    for (; v < nvec; v += nthr) {
+        const Vec<VB> x = ld<VB>(b0 + v * VB);
+        Vec<VB> y = x;
+        if constexpr (Op::kIn == 2) y = ld<VB>(b1 + v * VB);
+        st<VB>(bo + v * VB, apply<Op, VB>(op, x, y));
+    }
+}
+
+template <class Op, int VB, int U>
+cudaError_t launch_stream(const StreamArgs &a, int grid, cudaStream_t s) {
+    stream_kernel<Op, VB, U><<<grid, kBlock, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+// Loads in flight per thread per input, by width: about 64 bytes each.
+template <int VB> struct UnrollFor { static constexpr int value = VB >= 32 ? 2 : VB == 16 ? 4 : 8; };
+
+template <class Op, int VB>
+constexpr StreamEntry stream_entry() {
+    return StreamEntry{reinterpret_cast<const void *>(&stream_kernel<Op, VB, UnrollFor<VB>::value>),
+                       &launch_stream<Op, VB, UnrollFor<VB>::value>, UnrollFor<VB>::value};
+}
+constexpr StreamEntry kNoEntry{nullptr, nullptr, 0};
+
+// ---------------------------------------------------------------- gather
+//
+// out[i] = in[(s*i) mod n] ("CUDA-MODE lecture notes" §3.2, non-coalesced copy,
+// s = 2 on the page).  One output element per access, as on the page, so a
+// warp's load touches every s-th element of a span of 32*s elements while its
+// store covers 32 consecutive elements.  With i = v + j*T (T = grid threads),
+// (s*i) mod n advances by (s*T) mod n per unrolled slot: the index needs one
+// modular product per thread and conditional subtractions afterwards.
+
+__device__ __forceinline__ uint64_t mulmod_u64(uint64_t a, uint64_t b, uint64_t n) {
+    // a, b < n <= 2^63: doubling and adding stay below 2^64
+    uint64_t r = 0;
+    while (b != 0) {
+        if (b & 1u) {
+            r += a;
+            if (r >= n) r -= n;
+        }
+        a += a;
+        if (a >= n) a -= n;
+        b >>= 1;
+    }
+    return r;
+}
+__device__ __forceinline__ uint64_t addmod_u64(uint64_t a, uint64_t b, uint64_t n) {
+    const uint64_t r = a + b;  // a, b < n <= 2^63
+    return r >= n ? r - n : r;
+}
+
+template <int E, int U>
+__global__ void __launch_bounds__(kBlock) gather_kernel(const GatherArgs g) {
+    const char *in = static_cast<const char *>(g.in);
+    char *out = static_cast<char *>(g.out);
+    const uint64_t n = g.n;
+    const uint64_t nthr = static_cast<uint64_t>(gridDim.x) * blockDim.x;
+    uint64_t v = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (v >= n) return;
+    uint64_t jv = mulmod_u64(g.s_mod, v, n);  // (s*v) mod n, v < n
+    for (; v + (U - 1) * nthr < n; v += U * nthr) {
+        Vec<E> x[U];
+        uint64_t j = jv;
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            x[k] = ld<E>(in + j * E);
+            j = addmod_u64(j, g.step_mod, n);
+        }
+#pragma unroll
+        for (int k = 0; k < U; ++k) st<E>(out + (v + k * nthr) * E, x[k]);
+        jv = j;  // U slots further on: (s*(v + U*T)) mod n
+    }
+    for (; v < n; v += nthr) {
+        st<E>(out + v * E, ld<E>(in + jv * E));
+        jv = addmod_u64(jv, g.step_mod, n);
+    }
+}
+
+template <int E, int U>
+cudaError_t launch_gather(const GatherArgs &g, int grid, cudaStream_t s) {
+    gather_kernel<E, U><<<grid, kBlock, 0, s>>>(g);
+    return cudaGetLastError();
+}
+
+}  // namespace ew

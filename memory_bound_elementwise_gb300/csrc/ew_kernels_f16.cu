@@ -1,0 +1,31 @@
+// ew_kernels_f16.cu -- binary16 instantiations of the streaming kernels, the
+// 2-byte copy (shared by binary16 and bfloat16) and the 2-byte strided gather.
+#include "ew_kernels.cuh"
+
+namespace ew {
+
+namespace {
+template <class Op>
+constexpr StreamEntry e16(int vi) {
+    return vi == 0 ? stream_entry<Op, 32>() : vi == 1 ? stream_entry<Op, 16>()
+         : vi == 2 ? stream_entry<Op, 8>() : vi == 3 ? stream_entry<Op, 4>()
+         : stream_entry<Op, 2>();
+}
+
+const StreamEntry kTable[OP_COUNT][5] = {
+    {e16<OpAddF16>(0), e16<OpAddF16>(1), e16<OpAddF16>(2), e16<OpAddF16>(3), e16<OpAddF16>(4)},
+    {e16<OpSaxpyF16>(0), e16<OpSaxpyF16>(1), e16<OpSaxpyF16>(2), e16<OpSaxpyF16>(3), e16<OpSaxpyF16>(4)},
+    {e16<OpReluF16>(0), e16<OpReluF16>(1), e16<OpReluF16>(2), e16<OpReluF16>(3), e16<OpReluF16>(4)},
+    {e16<OpCopy<2>>(0), e16<OpCopy<2>>(1), e16<OpCopy<2>>(2), e16<OpCopy<2>>(3), e16<OpCopy<2>>(4)},
+};
+
+constexpr int kGatherUnroll = 8;
+const GatherEntry kGather2{reinterpret_cast<const void *>(&gather_kernel<2, kGatherUnroll>),
+                           &launch_gather<2, kGatherUnroll>, kGatherUnroll};
+}  // namespace
+
+const StreamEntry *stream_table_f16() { return &kTable[0][0]; }
+
+const GatherEntry *gather_entry_2() { return &kGather2; }
+
+}  // namespace ew

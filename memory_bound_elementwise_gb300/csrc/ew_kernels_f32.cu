@@ -1,0 +1,29 @@
+// ew_kernels_f32.cu -- binary32 instantiations of the streaming kernels and
+// the 4-byte strided gather.
+#include "ew_kernels.cuh"
+
+namespace ew {
+
+namespace {
+template <class Op>
+constexpr StreamEntry e32(int vi) {
+    return vi == 0 ? stream_entry<Op, 32>() : vi == 1 ? stream_entry<Op, 16>()
+         : vi == 2 ? stream_entry<Op, 8>() : vi == 3 ? stream_entry<Op, 4>() : kNoEntry;
+}
+const StreamEntry kTable[OP_COUNT][5] = {
+    {e32<OpAddF32>(0), e32<OpAddF32>(1), e32<OpAddF32>(2), e32<OpAddF32>(3), kNoEntry},
+    {e32<OpSaxpyF32>(0), e32<OpSaxpyF32>(1), e32<OpSaxpyF32>(2), e32<OpSaxpyF32>(3), kNoEntry},
+    {e32<OpReluF32>(0), e32<OpReluF32>(1), e32<OpReluF32>(2), e32<OpReluF32>(3), kNoEntry},
+    {e32<OpCopy<4>>(0), e32<OpCopy<4>>(1), e32<OpCopy<4>>(2), e32<OpCopy<4>>(3), kNoEntry},
+};
+
+constexpr int kGatherUnroll = 8;
+const GatherEntry kGather4{reinterpret_cast<const void *>(&gather_kernel<4, kGatherUnroll>),
+                           &launch_gather<4, kGatherUnroll>, kGatherUnroll};
+}  // namespace
+
+const StreamEntry *stream_table_f32() { return &kTable[0][0]; }
+
+const GatherEntry *gather_entry_4() { return &kGather4; }
+
+}  // namespace ew

@@ -1,18 +1,9 @@
 """Worked examples printed on the pages (fixtures under tests/golden/)."""
-import json
-import os
-
 import pytest
 
 import oracle
 from memory_bound_elementwise_gb300 import metrics
-
-GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
-
-
-def load(name):
-    with open(os.path.join(GOLDEN, name), encoding="utf-8") as f:
-        return json.load(f)
+from tests.golden_util import load_golden as load
 
 
 def test_ceil_div_worked_example():

@@ -1,0 +1,348 @@
+"""GPU parity: every operator, dtype and kernel variant against the oracle,
+element by element, through the C ABI.
+
+Small cases span several vectors, grid strides and ragged heads/tails at every
+alignment offset; output buffers carry guard zones that must stay untouched.
+The full-size cases are the measured workloads: fp32 add at 2^20+3 and 2^28,
+fp32 SAXPY at 32M in place, bf16/fp16 add at 2^28 (aligned and offset by one
+element), fp32 ReLU at 2^28 (out of place and in place), fp32 copy and
+stride-2 gather at 2^26.
+The bar is bit-exact; NaN results of arithmetic compare as "both NaN".
+"""
+import numpy as np
+import pytest
+import torch
+
+import memory_bound_elementwise_gb300 as ew
+import oracle
+from memory_bound_elementwise_gb300 import inputs
+from tests.gpu_util import GuardedBuffer, assert_bits_equal, ESIZE
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = ["f32", "f16", "bf16"]
+PATHS = ["auto", "scalar", "v128", "v256"]
+SMALL_N = [1, 2, 3, 5, 7, 8, 9, 15, 16, 17, 31, 32, 33, 64, 255, 257, 1000, 4099, 70001]
+DT_CODE = {"f32": 0, "f16": 1, "bf16": 2}
+
+
+@pytest.fixture(autouse=True)
+def _reset_path():
+    ew.set_path("auto")
+    yield
+    ew.set_path("auto")
+
+
+def _stream():
+    return torch.cuda.current_stream().cuda_stream
+
+
+def run_op(op, dtype, bufs, n, alpha=2.5):
+    """Call the C ABI directly with raw pointers."""
+    L = ew.lib()
+    dt = DT_CODE[dtype]
+    p = [b.view.data_ptr() for b in bufs]
+    if op == "add":
+        st = L.ew_add(dt, p[0], p[1], p[2], n, _stream())
+    elif op == "saxpy":
+        st = L.ew_saxpy(dt, alpha, p[0], p[1], n, _stream())
+    elif op == "relu":
+        st = L.ew_relu(dt, p[0], p[1], n, _stream())
+    elif op == "copy":
+        st = L.ew_copy(dt, p[0], p[1], n, _stream())
+    else:
+        raise ValueError(op)
+    assert st == 0, ew.status_string(st)
+
+
+def expected(op, dtype, x, y, alpha=2.5):
+    if op == "add":
+        return oracle.add(dtype, x, y)
+    if op == "saxpy":
+        return oracle.saxpy(dtype, alpha, x, y)
+    if op == "relu":
+        return oracle.relu(dtype, x)
+    return oracle.copy(x)
+
+
+def make_inputs(dtype, n, seed, specials=True):
+    x = inputs.as_dtype(inputs.normal(n, seed) * np.float32(3.0), dtype)
+    y = inputs.as_dtype(inputs.uniform(n, seed + 1), dtype)
+    if specials:
+        x = inputs.with_specials(x, dtype, seed)
+        y = inputs.with_specials(y, dtype, seed + 7)
+    return x, y
+
+
+def check_case(op, dtype, n, offs, seed, path="auto"):
+    x, y = make_inputs(dtype, n, seed)
+    nin = {"add": 2, "saxpy": 2, "relu": 1, "copy": 1}[op]
+    if op == "saxpy":
+        bx = GuardedBuffer(n, dtype, offs[0]).fill(x)
+        by = GuardedBuffer(n, dtype, offs[1]).fill(y)
+        bufs, outb = [bx, by], by
+    elif nin == 2:
+        bx = GuardedBuffer(n, dtype, offs[0]).fill(x)
+        by = GuardedBuffer(n, dtype, offs[1]).fill(y)
+        bo = GuardedBuffer(n, dtype, offs[2])
+        bufs, outb = [bx, by, bo], bo
+    else:
+        bx = GuardedBuffer(n, dtype, offs[0]).fill(x)
+        bo = GuardedBuffer(n, dtype, offs[1])
+        bufs, outb = [bx, bo], bo
+    ew.set_path(path)
+    run_op(op, dtype, bufs, n)
+    rec = ew.last_launch()
+    torch.cuda.synchronize()
+    want = expected(op, dtype, x, y)
+    assert_bits_equal(outb.host(), want, dtype, nan_as_class=op in ("add", "saxpy"),
+                      what="%s %s n=%d offs=%s path=%s" % (op, dtype, n, offs, path))
+    for b in bufs:
+        assert b.guards_intact(), "guard zone written: %s %s n=%d offs=%s" % (op, dtype, n, offs)
+    return rec
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("op", ["add", "saxpy", "relu", "copy"])
+def test_small_sizes_every_offset(op, dtype):
+    per = 32 // ESIZE[dtype]
+    for n in SMALL_N:
+        for off in range(per):
+            nin = 3 if op == "add" else 2
+            check_case(op, dtype, n, [off] * nin, seed=1000 + n * 37 + off)
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("op", ["add", "saxpy", "relu", "copy"])
+def test_forced_paths(op, dtype, path):
+    for n in (1, 33, 1000, 70001):
+        for off in (0, 1, 3):
+            nin = 3 if op == "add" else 2
+            rec = check_case(op, dtype, n, [off] * nin, seed=2000 + n + off, path=path)
+            if path == "scalar":
+                assert rec["vec_bytes"] == ESIZE[dtype]
+            elif path == "v128":
+                assert rec["vec_bytes"] <= 16
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_mixed_offsets_fall_back(dtype):
+    for offs in ([1, 0, 3], [0, 2, 4], [4, 0, 8], [2, 6, 10], [0, 0, 1], [5, 5, 13]):
+        for n in (17, 1000, 4099):
+            check_case("add", dtype, n, offs, seed=3000 + n + sum(offs))
+            check_case("saxpy", dtype, n, offs[:2], seed=3100 + n + sum(offs))
+            check_case("relu", dtype, n, offs[:2], seed=3200 + n + sum(offs))
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_in_place(dtype):
+    n = 70001
+    x, y = make_inputs(dtype, n, 4000)
+    L = ew.lib()
+    dt = DT_CODE[dtype]
+    # c == a
+    ba = GuardedBuffer(n, dtype, 1).fill(x)
+    bb = GuardedBuffer(n, dtype, 1).fill(y)
+    assert L.ew_add(dt, ba.view.data_ptr(), bb.view.data_ptr(), ba.view.data_ptr(), n, _stream()) == 0
+    torch.cuda.synchronize()
+    assert_bits_equal(ba.host(), oracle.add(dtype, x, y), dtype, True, "add in place")
+    # saxpy with x == y
+    bx = GuardedBuffer(n, dtype, 0).fill(x)
+    assert L.ew_saxpy(dt, -0.75, bx.view.data_ptr(), bx.view.data_ptr(), n, _stream()) == 0
+    torch.cuda.synchronize()
+    assert_bits_equal(bx.host(), oracle.saxpy(dtype, -0.75, x, x), dtype, True, "saxpy x==y")
+    # relu in place
+    br = GuardedBuffer(n, dtype, 3).fill(x)
+    assert L.ew_relu(dt, br.view.data_ptr(), br.view.data_ptr(), n, _stream()) == 0
+    torch.cuda.synchronize()
+    assert_bits_equal(br.host(), oracle.relu(dtype, x), dtype, False, "relu in place")
+    for b in (ba, bb, bx, br):
+        assert b.guards_intact()
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_every_bit_pattern_add_relu(dtype):
+    """All 16-bit patterns (or 2^20 random binary32 patterns) as inputs."""
+    if dtype == "f32":
+        x = inputs.random_bits(1 << 20, "f32", 5000)
+        y = inputs.random_bits(1 << 20, "f32", 5001)
+    else:
+        allp = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+        x = np.tile(allp, 64)
+        y = inputs.random_bits(x.size, dtype, 5002)
+    n = x.size
+    bx = GuardedBuffer(n, dtype).fill(x)
+    by = GuardedBuffer(n, dtype).fill(y)
+    bo = GuardedBuffer(n, dtype)
+    run_op("add", dtype, [bx, by, bo], n)
+    torch.cuda.synchronize()
+    assert_bits_equal(bo.host(), oracle.add(dtype, x, y), dtype, True, "add all patterns")
+    run_op("relu", dtype, [bx, bo], n)
+    torch.cuda.synchronize()
+    assert_bits_equal(bo.host(), oracle.relu(dtype, x), dtype, False, "relu all patterns")
+    by.fill(y)
+    run_op("saxpy", dtype, [bx, by], n, alpha=-1.5)
+    torch.cuda.synchronize()
+    assert_bits_equal(by.host(), oracle.saxpy(dtype, -1.5, x, y), dtype, True, "saxpy all patterns")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+def test_gather_small(dtype):
+    L = ew.lib()
+    for n in (1, 2, 3, 8, 33, 1000, 4097, 70001, 262144):
+        x = inputs.random_bits(n, dtype, 6000 + n)
+        for s in (1, 2, 3, 7, n + 2, (1 << 40) + 3):
+            bi = GuardedBuffer(n, dtype, 1).fill(x)
+            bo = GuardedBuffer(n, dtype, 0)
+            assert L.ew_gather_stride(DT_CODE[dtype], bi.view.data_ptr(), bo.view.data_ptr(),
+                                      n, s, _stream()) == 0
+            torch.cuda.synchronize()
+            assert_bits_equal(bo.host(), oracle.gather_stride(x, s), dtype, False,
+                              "gather n=%d s=%d" % (n, s))
+            assert bi.guards_intact() and bo.guards_intact()
+
+
+def test_launch_record_and_grid():
+    n = 1 << 22
+    a = torch.zeros(n, device="cuda")
+    b = torch.zeros(n, device="cuda")
+    ew.ew_add(a, b, torch.empty_like(a))
+    rec = ew.last_launch()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert rec["launches"] == 1 and rec["vec_bytes"] == 32 and rec["path"] == 3
+    assert 1 <= rec["grid"] <= sms * (2048 // rec["block"])
+    assert rec["nvec"] == n // 8 and rec["head"] == 0 and rec["tail"] == 0
+    torch.cuda.synchronize()
+
+
+def test_pointer_check_rejects_host_memory():
+    import ctypes
+    host = (ctypes.c_float * 64)()
+    d = torch.zeros(64, device="cuda")
+    ew.set_pointer_check(True)
+    try:
+        st = ew.lib().ew_add(0, ctypes.addressof(host), d.data_ptr(), d.data_ptr(), 64, _stream())
+        assert st == 5
+        st = ew.lib().ew_add(0, d.data_ptr(), d.data_ptr(), d.data_ptr(), 64, _stream())
+        assert st == 0
+    finally:
+        ew.set_pointer_check(False)
+    torch.cuda.synchronize()
+
+
+def test_device_error_word_starts_clear():
+    st, code = ew.device_error()
+    assert (st, code) == (0, 0)
+
+
+def test_binding_tensor_api_matches_oracle():
+    n = 4099
+    x, y = make_inputs("bf16", n, 7000, specials=False)
+    tx = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+    ty = torch.from_numpy(y.view(np.int16)).cuda().view(torch.bfloat16)
+    tc = ew.ew_add(tx, ty)
+    got = tc.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert_bits_equal(got, oracle.add("bf16", x, y), "bf16", True, "binding add")
+    with pytest.raises(ValueError):
+        ew.ew_add(tx, ty[:-1])
+    with pytest.raises(TypeError):
+        ew.ew_relu(tx.to(torch.float64))
+
+
+# ------------------------------------------------------------ full-size configs
+
+
+def _full(op, dtype, n, seed_x, seed_y, offset=0, dist="uniform", inplace=False, alpha=2.5):
+    if dist == "uniform":
+        x = inputs.as_dtype(inputs.uniform(n, seed_x), dtype)
+        y = inputs.as_dtype(inputs.uniform(n, seed_y), dtype)
+    else:
+        x = inputs.as_dtype(inputs.normal(n, seed_x), dtype)
+        y = inputs.as_dtype(inputs.normal(n, seed_y), dtype) if op in ("add", "saxpy") else None
+    if op == "relu":
+        x = inputs.normal(n, seed_x)
+        inputs.inject_signed_zeros(x)
+        x = inputs.as_dtype(x, dtype)
+    bx = GuardedBuffer(n, dtype, offset).fill(x)
+    if op == "add":
+        by = GuardedBuffer(n, dtype, offset).fill(y)
+        bo = GuardedBuffer(n, dtype, offset)
+        run_op("add", dtype, [bx, by, bo], n)
+        want = oracle.add(dtype, x, y)
+    elif op == "saxpy":
+        by = GuardedBuffer(n, dtype, offset).fill(y)
+        bo = by
+        run_op("saxpy", dtype, [bx, by], n, alpha=alpha)
+        want = oracle.saxpy(dtype, alpha, x, y)
+    elif op == "relu":
+        bo = bx if inplace else GuardedBuffer(n, dtype, offset)
+        run_op("relu", dtype, [bx, bo], n)
+        want = oracle.relu(dtype, x)
+    torch.cuda.synchronize()
+    assert_bits_equal(bo.host(), want, dtype, op != "relu", "%s %s n=%d" % (op, dtype, n))
+    assert bo.guards_intact()
+    return ew.last_launch()
+
+
+def test_config_add_f32_odd_tail():
+    rec = _full("add", "f32", (1 << 20) + 3, inputs.seed_for("add_f32_small"),
+                inputs.seed_for("add_f32_small", 1))
+    assert rec["tail"] == 3
+
+
+def test_config_saxpy_f32_32M_in_place():
+    _full("saxpy", "f32", 32 << 20, inputs.seed_for("saxpy_f32"), inputs.seed_for("saxpy_f32", 1),
+          dist="normal")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("offset", [0, 1])
+def test_config_add_16bit_2p28(dtype, offset):
+    rec = _full("add", dtype, 1 << 28, inputs.seed_for("add_16"), inputs.seed_for("add_16", 1),
+                offset=offset, dist="normal")
+    assert rec["head"] == (15 if offset else 0)
+
+
+@pytest.mark.parametrize("inplace", [False, True])
+def test_config_relu_f32_2p28(inplace):
+    _full("relu", "f32", 1 << 28, inputs.seed_for("relu_f32"), None, inplace=inplace)
+
+
+def test_config_copy_and_gather_f32_2p26():
+    n = 1 << 26
+    x = inputs.uniform(n, inputs.seed_for("copy_f32"), 0.0, 1.0)
+    bi = GuardedBuffer(n, "f32").fill(x)
+    bo = GuardedBuffer(n, "f32")
+    assert ew.lib().ew_copy(0, bi.view.data_ptr(), bo.view.data_ptr(), n, _stream()) == 0
+    torch.cuda.synchronize()
+    assert_bits_equal(bo.host(), x, "f32", False, "copy 2^26")
+    assert ew.lib().ew_gather_stride(0, bi.view.data_ptr(), bo.view.data_ptr(), n, 2, _stream()) == 0
+    torch.cuda.synchronize()
+    assert_bits_equal(bo.host(), oracle.gather_stride(x, 2), "f32", False, "gather 2^26")
+    assert bo.guards_intact() and bi.guards_intact()
+
+
+def test_config_add_f32_2p28():
+    _full("add", "f32", 1 << 28, inputs.seed_for("add_f32"), inputs.seed_for("add_f32", 1))
+
+
+def test_beyond_2p31_elements_f16():
+    """n > 2^31 (byte offsets past 2^32): a seeded 2^20-element tile repeated on
+    the device; every output tile and the ragged end compared with the oracle."""
+    tile = 1 << 20
+    n = (1 << 31) + 17
+    a = inputs.as_dtype(inputs.normal(tile, 8100), "f16")
+    b = inputs.as_dtype(inputs.normal(tile, 8101), "f16")
+    reps = -(-n // tile)
+    ta = torch.from_numpy(a.view(np.int16)).cuda().repeat(reps)[:n].contiguous()
+    tb = torch.from_numpy(b.view(np.int16)).cuda().repeat(reps)[:n].contiguous()
+    tc = torch.empty_like(ta)
+    assert ew.lib().ew_add(1, ta.data_ptr(), tb.data_ptr(), tc.data_ptr(), n, _stream()) == 0
+    torch.cuda.synchronize()
+    want = torch.from_numpy(oracle.add("f16", a, b).view(np.int16)).cuda()
+    full = (n // tile) * tile
+    assert torch.equal(tc[:full].view(-1, tile), want.expand(n // tile, tile))
+    assert torch.equal(tc[full:], want[:n - full])
+    del ta, tb, tc
+    torch.cuda.empty_cache()
