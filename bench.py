@@ -311,12 +311,35 @@ def aux_measurements(torch, ew, inputs, metrics, stream, peak, dev):
     rc, pc = dev_of(np.zeros_like(a), "f32")
     record("add_f32_2p20p3_l2_resident", "add", "f32", n1, lambda: L.ew_add(0, pa, pb, pc, n1, s),
            steps=500)
-    # device-to-device copy ceiling of this GPU (cudaMemcpyAsync, 2 GiB, read + write bytes)
+    del ra, rb, rc
+    # the headline workload through the other variants: persistent schedule, bulk-copy path
+    a = inputs.uniform(n28, inputs.seed_for("add_f32"))
+    b = inputs.uniform(n28, inputs.seed_for("add_f32", 1))
+    ra, pa = dev_of(a, "f32")
+    rb, pb = dev_of(b, "f32")
+    rc, pc = dev_of(np.zeros_like(a), "f32")
+    del a, b
+    for label, path, sched in (("persistent", "auto", "persistent"), ("tma", "tma", "auto")):
+        ew.set_path(path)
+        ew.set_schedule(sched)
+        record("add_f32_2p28_" + label, "add", "f32", n28, lambda: L.ew_add(0, pa, pb, pc, n28, s))
+    ew.set_path("tma")
+    ew.set_schedule("auto")
+    record("copy_f32_2p26_tma", "copy", "f32", n26, lambda: L.ew_copy(0, pa, pb, n26, s), steps=200)
+    ew.set_path("auto")
+    del ra, rb, rc
+    # device-to-device copy ceiling of this GPU (cudaMemcpyAsync via torch copy_, 2 GiB,
+    # read + write bytes), timed on the same stream
     big = torch.empty(1 << 31, dtype=torch.uint8, device=dev)
     big2 = torch.empty_like(big)
-    total, kern = time_launches(torch, stream, lambda: big2.copy_(big, non_blocking=True), 20, 3)
-    out["memcpy_d2d_2GiB"] = {"gbps": metrics.gbps(2 * big.numel(), kern), "frac": metrics.gbps(2 * big.numel(), kern) / peak,
-                              "kernel_ms": kern * 1e3, "note": "torch copy_ (library D2D copy), read+write bytes"}
+
+    def d2d():
+        with torch.cuda.stream(stream):
+            big2.copy_(big, non_blocking=True)
+    total, kern = time_launches(torch, stream, d2d, 20, 3)
+    g = metrics.gbps(2 * big.numel(), kern)
+    out["memcpy_d2d_2GiB"] = {"gbps": g, "frac": g / peak, "kernel_ms": kern * 1e3,
+                              "note": "library device-to-device copy (torch copy_), read+write bytes"}
     return out
 
 

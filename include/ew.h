@@ -97,8 +97,21 @@ typedef enum {
     EW_PATH_SCALAR = 1, /* one element per access, grid-stride */
     EW_PATH_V128 = 2,   /* 16-byte vector accesses */
     EW_PATH_V256 = 3,   /* 32-byte vector accesses (sm_100 family) */
-    EW_PATH_TMA = 4     /* bulk async copies (cp.async.bulk) through shared memory */
+    EW_PATH_TMA = 4     /* bulk async copies (cp.async.bulk) through shared memory;
+                           needs all pointers at one offset modulo 16 bytes */
 } ew_path;
+
+/* How the body's chunks are handed to thread blocks.
+ * EW_SCHED_ONESHOT    one block per chunk of 256 threads x 64 bytes per thread
+ *                     per input; the hardware block scheduler balances the SMs
+ *                     (the default: fastest measured on GB300).
+ * EW_SCHED_PERSISTENT at most SMs x resident blocks per SM, each striding over
+ *                     the chunks (the grid-stride design of the pages). */
+typedef enum {
+    EW_SCHED_AUTO = 0,
+    EW_SCHED_ONESHOT = 1,
+    EW_SCHED_PERSISTENT = 2
+} ew_schedule;
 
 /* ---- operators ------------------------------------------------------- */
 
@@ -134,6 +147,12 @@ EW_API ew_status ew_gather_stride(ew_dtype dtype, const void *in, void *out, int
 EW_API ew_status ew_set_path(ew_path path);
 EW_API ew_path ew_get_path(void);
 
+/* Select the block schedule for later calls in this process (process-wide).
+ * EW_ERR_INVALID_VALUE for a value outside ew_schedule.  The bulk-copy path
+ * always runs one-shot. */
+EW_API ew_status ew_set_schedule(ew_schedule schedule);
+EW_API ew_schedule ew_get_schedule(void);
+
 /* Enable (1) or disable (0, the default) a cudaPointerGetAttributes check of
  * every pointer before launch; a pointer the device cannot access then gives
  * EW_ERR_NOT_DEVICE_POINTER.  Process-wide. */
@@ -160,7 +179,8 @@ typedef struct {
     int32_t grid;      /* blocks */
     int32_t block;     /* threads per block */
     int32_t smem;      /* dynamic shared memory bytes per block */
-    int64_t head, nvec, tail;
+    int32_t schedule;  /* ew_schedule that ran */
+    int64_t head, nvec, tail; /* for EW_PATH_TMA: nvec counts tiles of 8 KiB per input */
 } ew_launch_record;
 EW_API ew_status ew_last_launch(ew_launch_record *out);
 
@@ -173,9 +193,16 @@ EW_API int ew_last_cuda_error(void);
 
 /* Read and clear the device-side error word of the current device after
  * synchronising `stream`.  *code = 0 when no bounded wait has given up since the
- * last read; otherwise the wait site that gave up.  Returns EW_ERR_TIMEOUT when
+ * last read; otherwise the wait site that gave up (1: a bulk-copy tile of
+ * EW_PATH_TMA, 99: ew_selftest_bounded_wait).  Returns EW_ERR_TIMEOUT when
  * *code != 0, EW_ERR_CUDA when the synchronisation itself fails. */
 EW_API ew_status ew_device_error(ew_stream_t stream, int32_t *code);
+
+/* Self-test of the bounded device waits: enqueues one block that arms an
+ * mbarrier no copy will complete; its wait must give up after limit_ns
+ * nanoseconds (1 <= limit_ns <= 10^10, else EW_ERR_INVALID_VALUE) and record
+ * code 99, which a following ew_device_error returns.  Nothing else is touched. */
+EW_API ew_status ew_selftest_bounded_wait(int64_t limit_ns, ew_stream_t stream);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 EW_API int ew_version(void);

@@ -30,6 +30,9 @@ EW_F32, EW_F16, EW_BF16 = 0, 1, 2
 PATH_AUTO, PATH_SCALAR, PATH_V128, PATH_V256, PATH_TMA = 0, 1, 2, 3, 4
 PATH_NAMES = {PATH_AUTO: "auto", PATH_SCALAR: "scalar", PATH_V128: "v128",
               PATH_V256: "v256", PATH_TMA: "tma"}
+# ew_schedule
+SCHED_AUTO, SCHED_ONESHOT, SCHED_PERSISTENT = 0, 1, 2
+SCHED_NAMES = {SCHED_AUTO: "auto", SCHED_ONESHOT: "oneshot", SCHED_PERSISTENT: "persistent"}
 # ew_status
 EW_OK = 0
 STATUS_NAMES = {0: "EW_OK", 1: "EW_ERR_INVALID_VALUE", 2: "EW_ERR_NULL_POINTER",
@@ -38,8 +41,9 @@ STATUS_NAMES = {0: "EW_OK", 1: "EW_ERR_INVALID_VALUE", 2: "EW_ERR_NULL_POINTER",
 
 # Every function declared in include/ew.h.
 EXPORTS = ("ew_add", "ew_saxpy", "ew_relu", "ew_copy", "ew_gather_stride", "ew_set_path",
-           "ew_get_path", "ew_set_pointer_check", "ew_plan_query", "ew_last_launch",
-           "ew_status_string", "ew_last_cuda_error", "ew_device_error", "ew_version")
+           "ew_get_path", "ew_set_schedule", "ew_get_schedule", "ew_set_pointer_check",
+           "ew_plan_query", "ew_last_launch", "ew_status_string", "ew_last_cuda_error",
+           "ew_device_error", "ew_selftest_bounded_wait", "ew_version")
 
 
 class EwError(RuntimeError):
@@ -59,7 +63,7 @@ class Plan(ctypes.Structure):
 class LaunchRecord(ctypes.Structure):
     _fields_ = [("launches", ctypes.c_int32), ("path", ctypes.c_int32),
                 ("vec_bytes", ctypes.c_int32), ("grid", ctypes.c_int32),
-                ("block", ctypes.c_int32), ("smem", ctypes.c_int32),
+                ("block", ctypes.c_int32), ("smem", ctypes.c_int32), ("schedule", ctypes.c_int32),
                 ("head", ctypes.c_int64), ("nvec", ctypes.c_int64), ("tail", ctypes.c_int64)]
 
     def as_dict(self):
@@ -86,12 +90,16 @@ def lib():
     L.ew_copy.argtypes = [ctypes.c_int, vp, vp, i64, vp]
     L.ew_gather_stride.argtypes = [ctypes.c_int, vp, vp, i64, i64, vp]
     for name in ("ew_add", "ew_saxpy", "ew_relu", "ew_copy", "ew_gather_stride",
-                 "ew_set_path", "ew_set_pointer_check", "ew_plan_query", "ew_last_launch",
-                 "ew_device_error"):
+                 "ew_set_path", "ew_set_schedule", "ew_set_pointer_check", "ew_plan_query",
+                 "ew_last_launch", "ew_device_error", "ew_selftest_bounded_wait"):
         getattr(L, name).restype = ctypes.c_int
     L.ew_set_path.argtypes = [ctypes.c_int]
     L.ew_get_path.argtypes = []
     L.ew_get_path.restype = ctypes.c_int
+    L.ew_set_schedule.argtypes = [ctypes.c_int]
+    L.ew_get_schedule.argtypes = []
+    L.ew_get_schedule.restype = ctypes.c_int
+    L.ew_selftest_bounded_wait.argtypes = [i64, vp]
     L.ew_set_pointer_check.argtypes = [ctypes.c_int]
     L.ew_plan_query.argtypes = [ctypes.c_int, ctypes.POINTER(vp), i32, i64, ctypes.POINTER(Plan)]
     L.ew_last_launch.argtypes = [ctypes.POINTER(LaunchRecord)]
@@ -200,6 +208,17 @@ def get_path():
     return PATH_NAMES[lib().ew_get_path()]
 
 
+def set_schedule(schedule):
+    """Select the block schedule: 'auto', 'oneshot' or 'persistent'."""
+    code = ({v: k for k, v in SCHED_NAMES.items()}[schedule] if isinstance(schedule, str)
+            else int(schedule))
+    check(lib().ew_set_schedule(code), "ew_set_schedule")
+
+
+def get_schedule():
+    return SCHED_NAMES[lib().ew_get_schedule()]
+
+
 def set_pointer_check(enable):
     check(lib().ew_set_pointer_check(1 if enable else 0), "ew_set_pointer_check")
 
@@ -218,6 +237,13 @@ def last_launch():
     return rec.as_dict()
 
 
+def selftest_bounded_wait(limit_ns, stream=None):
+    """Enqueue the bounded-wait self-test (its wait must give up after limit_ns)."""
+    import torch
+    check(lib().ew_selftest_bounded_wait(int(limit_ns), _stream(stream, torch.cuda.current_device())),
+          "ew_selftest_bounded_wait")
+
+
 def device_error(stream=None):
     """Synchronise ``stream``, then read and clear the device error word."""
     import torch
@@ -227,5 +253,5 @@ def device_error(stream=None):
 
 
 __all__ = ["ew_add", "ew_saxpy", "ew_relu", "ew_copy", "ew_gather_stride", "set_path",
-           "get_path", "set_pointer_check", "plan_query", "last_launch", "device_error",
-           "lib", "EwError", "EXPORTS"]
+           "get_path", "set_schedule", "get_schedule", "set_pointer_check", "plan_query",
+           "last_launch", "device_error", "selftest_bounded_wait", "lib", "EwError", "EXPORTS"]

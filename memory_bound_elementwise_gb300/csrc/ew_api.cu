@@ -4,14 +4,17 @@
 // Validation happens entirely on the host, before any CUDA runtime call, so
 // argument errors never reach the GPU.
 //
-// Launch geometry ("逐元素操作算子" §二: a grid sized by the SM count rather
-// than by N; CUDA-MODE lecture notes §4.2 wave quantization and §4.4 the
-// occupancy calculator): grid = min(SMs x resident blocks per SM from the
-// occupancy API, blocks needed to give every thread one unrolled iteration).
-// The grid is thus at most one full wave and each thread strides through the
-// body, so there is no partial last wave of blocks.
+// Launch geometry.  The body is cut into chunks of kBlock threads x U vectors
+// ("逐元素操作算子" §二: the launch is sized from N with a ceil-div, and a
+// grid-stride loop decouples the grid from N).  One-shot schedule (default):
+// one block per chunk, so the block scheduler keeps every SM busy until the
+// last chunk (CUDA-MODE lecture notes §4.2: a partial last wave idles SMs; here
+// the waves are many and short).  Persistent schedule: SMs x resident blocks
+// per SM from the occupancy API (CUDA-MODE lecture notes §4.4), each block
+// striding over the chunks.
 #include <algorithm>
 #include <atomic>
+#include <climits>
 #include <cstdlib>
 #include <cstring>
 #include <map>
@@ -28,6 +31,7 @@ using namespace ew;
 namespace {
 
 std::atomic<int> g_path{EW_PATH_AUTO};
+std::atomic<int> g_schedule{EW_SCHED_AUTO};
 std::atomic<int> g_pointer_check{-1};  // -1: not yet read from the environment
 
 thread_local int t_last_cuda_error = 0;
@@ -75,13 +79,27 @@ ew_plan make_plan(int path, int e, const uintptr_t *p, int np, int64_t n) {
     pl.nvec = (n - head) / per;
     pl.tail = n - head - pl.nvec * per;
     pl.path = (vb == 32) ? EW_PATH_V256 : (vb == 16) ? EW_PATH_V128 : EW_PATH_SCALAR;
-    if (path == EW_PATH_TMA && vb >= 16) pl.path = EW_PATH_TMA;
     return pl;
 }
 
 int resolved_path() {
     const int p = g_path.load(std::memory_order_relaxed);
     return p == EW_PATH_AUTO ? EW_PATH_V256 : p;
+}
+int resolved_schedule() {
+    const int s = g_schedule.load(std::memory_order_relaxed);
+    return s == EW_SCHED_AUTO ? EW_SCHED_ONESHOT : s;
+}
+
+// Bulk-copy split: 16-byte aligned head, whole tiles, then the remainder.
+struct TmaPlan { int64_t head, ntiles, rem0; };
+TmaPlan make_tma_plan(const ew_plan &pl16, int e, int64_t n) {
+    TmaPlan t{};
+    t.head = pl16.head;
+    const int64_t per_tile = kTmaTile / e;
+    t.ntiles = (n - t.head) / per_tile;
+    t.rem0 = t.head + t.ntiles * per_tile;
+    return t;
 }
 
 // ---------------------------------------------------------------- devices
@@ -141,22 +159,48 @@ ew_status check_device_pointers(const void *const *p, int np) {
     return EW_OK;
 }
 
+int clamp_grid(int64_t blocks) {
+    return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(blocks, INT_MAX)));
+}
+
 // ---------------------------------------------------------------- dispatch
 
 const StreamEntry *table_for(int dt) {
     return dt == EW_F32 ? stream_table_f32() : dt == EW_F16 ? stream_table_f16() : stream_table_bf16();
 }
 
+ew_status run_tma(int op, ew_dtype dt, const void *in0, const void *in1, void *out, int64_t n,
+                  float alpha, const ew_plan &pl16, cudaStream_t s) {
+    const TmaEntry *ent = tma_entry(op, dt);
+    const int e = elem_size(dt);
+    const TmaPlan tp = make_tma_plan(pl16, e, n);
+    TmaArgs a{in0, in1, out, n, tp.head, tp.ntiles, tp.rem0, alpha, kWaitLimitNs};
+    const int grid = clamp_grid((tp.ntiles + kTmaStages - 1) / kTmaStages);
+    cudaError_t ce = ent->launch(a, grid, s);
+    if (ce != cudaSuccess) return cuda_fail(ce);
+    t_last.launches = 1;
+    t_last.path = EW_PATH_TMA;
+    t_last.vec_bytes = 16;
+    t_last.grid = grid;
+    t_last.block = kTmaBlock;
+    t_last.smem = ent->smem_bytes;
+    t_last.schedule = EW_SCHED_ONESHOT;
+    t_last.head = tp.head;
+    t_last.nvec = tp.ntiles;
+    t_last.tail = n - tp.rem0;
+    return EW_OK;
+}
+
 // Common path of add / saxpy / relu / copy once arguments are valid.
 ew_status run_stream(int op, ew_dtype dt, const void *in0, const void *in1, void *out,
                      int64_t n, float alpha, cudaStream_t s) {
-    t_last = ew_launch_record{};
     const int e = elem_size(dt);
     const void *ptrs[3] = {in0, out, in1};
     const int np = (in1 != nullptr) ? 3 : 2;
     uintptr_t up[3];
     for (int k = 0; k < np; ++k) up[k] = reinterpret_cast<uintptr_t>(ptrs[k]);
-    const ew_plan pl = make_plan(resolved_path(), e, up, np, n);
+    const int path = resolved_path();
+    const ew_plan pl = make_plan(path, e, up, np, n);
 
     if (pointer_check_enabled()) {
         ew_status st = check_device_pointers(ptrs, np);
@@ -166,6 +210,9 @@ ew_status run_stream(int op, ew_dtype dt, const void *in0, const void *in1, void
     cudaError_t ce = device_info(&dev, &sms);
     if (ce != cudaSuccess) return cuda_fail(ce);
 
+    if (path == EW_PATH_TMA && pl.vec_bytes >= 16 && tma_entry(op, dt) != nullptr)
+        return run_tma(op, dt, in0, in1, out, n, alpha, make_plan(EW_PATH_V128, e, up, np, n), s);
+
     StreamArgs a{in0, in1, out, n, pl.head, pl.nvec, pl.head + pl.nvec * (pl.vec_bytes / e), alpha};
 
     // copy of 16-bit elements is one kernel for both 16-bit formats
@@ -173,22 +220,27 @@ ew_status run_stream(int op, ew_dtype dt, const void *in0, const void *in1, void
     const StreamEntry &ent = table_for(tdt)[op * 5 + vec_index(pl.vec_bytes)];
     if (ent.launch == nullptr) return EW_ERR_INVALID_VALUE;
 
-    int occ = 1;
-    ce = blocks_per_sm(dev, ent.kernel, kBlock, 0, &occ);
-    if (ce != cudaSuccess) return cuda_fail(ce);
     const int64_t per_block = static_cast<int64_t>(kBlock) * ent.unroll;
-    const int64_t want = std::max<int64_t>((pl.nvec + per_block - 1) / per_block,
-                                           (pl.head + pl.tail + kBlock - 1) / kBlock);
-    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(sms) * occ)));
+    const int64_t nchunks = (pl.nvec + per_block - 1) / per_block;
+    const int sched = resolved_schedule();
+    int64_t blocks = nchunks;
+    if (sched == EW_SCHED_PERSISTENT) {
+        int occ = 1;
+        ce = blocks_per_sm(dev, ent.kernel, kBlock, 0, &occ);
+        if (ce != cudaSuccess) return cuda_fail(ce);
+        blocks = std::min<int64_t>(nchunks, static_cast<int64_t>(sms) * occ);
+    }
+    const int grid = clamp_grid(blocks);
 
     ce = ent.launch(a, grid, s);
     if (ce != cudaSuccess) return cuda_fail(ce);
     t_last.launches = 1;
-    t_last.path = pl.path == EW_PATH_TMA ? EW_PATH_V256 : pl.path;
+    t_last.path = pl.path;
     t_last.vec_bytes = pl.vec_bytes;
     t_last.grid = grid;
     t_last.block = kBlock;
     t_last.smem = 0;
+    t_last.schedule = sched;
     t_last.head = pl.head;
     t_last.nvec = pl.nvec;
     t_last.tail = pl.tail;
@@ -275,17 +327,29 @@ ew_status ew_gather_stride(ew_dtype dt, const void *in, void *out, int64_t n, in
     int dev = 0, sms = 0;
     cudaError_t ce = device_info(&dev, &sms);
     if (ce != cudaSuccess) return cuda_fail(ce);
-    const GatherEntry *g = (dt == EW_F32) ? gather_entry_4() : gather_entry_2();
-    int occ = 1;
-    ce = blocks_per_sm(dev, g->kernel, kBlock, 0, &occ);
-    if (ce != cudaSuccess) return cuda_fail(ce);
-    const int64_t per_block = static_cast<int64_t>(kBlock) * g->unroll;
-    const int64_t want = (n + per_block - 1) / per_block;
-    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(sms) * occ)));
     const uint64_t un = static_cast<uint64_t>(n);
-    const uint64_t nthr = static_cast<uint64_t>(grid) * kBlock;
-    GatherArgs ga{in, out, un, static_cast<uint64_t>(stride) % un,
-                  static_cast<uint64_t>((static_cast<unsigned __int128>(static_cast<uint64_t>(stride)) * nthr) % un)};
+    const uint64_t s_mod = static_cast<uint64_t>(stride) % un;
+    const int sched = resolved_schedule();
+    const bool oneshot = sched == EW_SCHED_ONESHOT && un <= (uint64_t(1) << 32);
+    GatherArgs ga{in, out, un, s_mod, 0, 0};
+    const GatherEntry *g;
+    int grid;
+    if (oneshot) {
+        g = (dt == EW_F32) ? gather_oneshot_4() : gather_oneshot_2();
+        const int64_t per_block = static_cast<int64_t>(kBlock) * g->unroll;
+        grid = clamp_grid((n + per_block - 1) / per_block);
+        ga.step_mod = (s_mod * static_cast<uint64_t>(kBlock)) % un;  // s_mod < 2^32
+        ga.barrett_m = ~uint64_t(0) / un;
+    } else {
+        g = (dt == EW_F32) ? gather_stride_4() : gather_stride_2();
+        int occ = 1;
+        ce = blocks_per_sm(dev, g->kernel, kBlock, 0, &occ);
+        if (ce != cudaSuccess) return cuda_fail(ce);
+        const int64_t per_block = static_cast<int64_t>(kBlock) * g->unroll;
+        grid = clamp_grid(std::min<int64_t>((n + per_block - 1) / per_block, int64_t(sms) * occ));
+        const uint64_t nthr = static_cast<uint64_t>(grid) * kBlock;
+        ga.step_mod = static_cast<uint64_t>((static_cast<unsigned __int128>(s_mod) * nthr) % un);
+    }
     ce = g->launch(ga, grid, reinterpret_cast<cudaStream_t>(s));
     if (ce != cudaSuccess) return cuda_fail(ce);
     t_last.launches = 1;
@@ -293,6 +357,7 @@ ew_status ew_gather_stride(ew_dtype dt, const void *in, void *out, int64_t n, in
     t_last.vec_bytes = elem_size(dt);
     t_last.grid = grid;
     t_last.block = kBlock;
+    t_last.schedule = oneshot ? EW_SCHED_ONESHOT : EW_SCHED_PERSISTENT;
     t_last.nvec = n;
     return EW_OK;
 }
@@ -305,6 +370,17 @@ ew_status ew_set_path(ew_path path) {
 }
 
 ew_path ew_get_path(void) { return static_cast<ew_path>(g_path.load(std::memory_order_relaxed)); }
+
+ew_status ew_set_schedule(ew_schedule sched) {
+    const int v = static_cast<int>(sched);
+    if (v < EW_SCHED_AUTO || v > EW_SCHED_PERSISTENT) return EW_ERR_INVALID_VALUE;
+    g_schedule.store(v, std::memory_order_relaxed);
+    return EW_OK;
+}
+
+ew_schedule ew_get_schedule(void) {
+    return static_cast<ew_schedule>(g_schedule.load(std::memory_order_relaxed));
+}
 
 ew_status ew_set_pointer_check(int enable) {
     if (enable != 0 && enable != 1) return EW_ERR_INVALID_VALUE;
@@ -319,7 +395,19 @@ ew_status ew_plan_query(ew_dtype dt, const void *const *ptrs, int32_t nptrs, int
     if (st != EW_OK) return st;
     uintptr_t up[4];
     for (int k = 0; k < nptrs; ++k) up[k] = reinterpret_cast<uintptr_t>(ptrs[k]);
-    *out = make_plan(resolved_path(), elem_size(dt), up, nptrs, n);
+    const int e = elem_size(dt);
+    const int path = resolved_path();
+    ew_plan pl = make_plan(path, e, up, nptrs, n);
+    if (path == EW_PATH_TMA && pl.vec_bytes >= 16) {
+        const ew_plan p16 = make_plan(EW_PATH_V128, e, up, nptrs, n);
+        const TmaPlan tp = make_tma_plan(p16, e, n);
+        pl.path = EW_PATH_TMA;
+        pl.vec_bytes = 16;
+        pl.head = tp.head;
+        pl.nvec = tp.ntiles;
+        pl.tail = n - tp.rem0;
+    }
+    *out = pl;
     return EW_OK;
 }
 
@@ -352,6 +440,17 @@ ew_status ew_device_error(ew_stream_t s, int32_t *code) {
     return *code != 0 ? EW_ERR_TIMEOUT : EW_OK;
 }
 
-int ew_version(void) { return 100; }
+ew_status ew_selftest_bounded_wait(int64_t limit_ns, ew_stream_t s) {
+    t_last = ew_launch_record{};
+    if (limit_ns < 1 || limit_ns > 10000000000LL) return EW_ERR_INVALID_VALUE;
+    cudaError_t e = launch_wait_selftest(static_cast<uint64_t>(limit_ns), reinterpret_cast<cudaStream_t>(s));
+    if (e != cudaSuccess) return cuda_fail(e);
+    t_last.launches = 1;
+    t_last.grid = 1;
+    t_last.block = 32;
+    return EW_OK;
+}
+
+int ew_version(void) { return 200; }
 
 }  // extern "C"

@@ -52,7 +52,8 @@ struct GatherArgs {
     void *out;
     uint64_t n;
     uint64_t s_mod;      // stride mod n
-    uint64_t step_mod;   // (stride * grid_threads) mod n
+    uint64_t step_mod;   // one-shot: (stride * kBlock) mod n; grid-stride: (stride * grid threads) mod n
+    uint64_t barrett_m;  // floor((2^64 - 1) / n), one-shot kernel only
 };
 using GatherLaunchFn = cudaError_t (*)(const GatherArgs &, int grid, cudaStream_t);
 struct GatherEntry {
@@ -60,18 +61,40 @@ struct GatherEntry {
     GatherLaunchFn launch;
     int unroll;
 };
-const GatherEntry *gather_entry_4();  // binary32
-const GatherEntry *gather_entry_2();  // 16-bit types
+const GatherEntry *gather_oneshot_4();  // binary32, n <= 2^32
+const GatherEntry *gather_stride_4();   // binary32, any n
+const GatherEntry *gather_oneshot_2();  // 16-bit types
+const GatherEntry *gather_stride_2();
 
-// Bulk-copy (cp.async.bulk) staging variant of the streaming kernels.
+// Bulk-copy (cp.async.bulk) staging variant of the streaming kernels: each
+// CTA moves kTmaStages tiles of kTmaTile bytes per input through shared memory.
+constexpr int kTmaTile = 8192;
+constexpr int kTmaStages = 2;
+constexpr int kTmaBlock = 128;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded mbarrier waits give up after 1 s
+
+struct TmaArgs {
+    const void *in0;
+    const void *in1;
+    void *out;
+    int64_t n;
+    int64_t head;     // elements [0, head) one by one (reach 16-byte alignment)
+    int64_t ntiles;   // whole tiles after the head
+    int64_t rem0;     // elements [rem0, n) one by one
+    float alpha;
+    uint64_t wait_limit_ns;
+};
+using TmaLaunchFn = cudaError_t (*)(const TmaArgs &, int grid, cudaStream_t);
 struct TmaEntry {
     const void *kernel;
-    StreamLaunchFn launch;  // grid = persistent CTAs; smem fixed per kernel
+    TmaLaunchFn launch;
     int smem_bytes;
-    int block;
 };
-// Returns nullptr where no bulk-copy kernel exists for (op, dtype).
+// nullptr where no bulk-copy kernel exists for (op, dtype).
 const TmaEntry *tma_entry(int op, int dtype);
+// One CTA that arms an mbarrier no copy will complete and must give up after
+// limit_ns, recording error code 99 (checks the bounded-wait path).
+cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t s);
 // Device error word written by bounded waits (read and cleared by the host).
 cudaError_t read_and_clear_device_error(cudaStream_t s, int32_t *code);
 

@@ -1,17 +1,21 @@
 // ew_kernels.cuh -- the streaming (load, operate, store) kernel and the
-// strided-gather kernel, as templates instantiated per operator and width by
+// strided-gather kernels, as templates instantiated per operator and width by
 // ew_kernels_{f32,f16,bf16}.cu.
 //
 // Streaming kernel ("逐元素操作算子" §二: template kernel, grid-stride loop,
 // float4 body with scalar tail; "HyperAI elementwise add", Versions 5-6:
 // several wide loads in flight per thread):
-//   * persistent grid: at most (SM count x resident blocks per SM) blocks, each
-//     thread walks the body with a grid stride;
-//   * each iteration issues U independent VB-byte loads per input before any
-//     arithmetic, then U VB-byte stores;
+//   * the body is cut into chunks of kBlock*U vectors; block b takes chunks
+//     b, b + gridDim.x, ... (one chunk per block when the grid covers them all);
+//   * each thread issues U independent VB-byte loads per input before any
+//     arithmetic, then U VB-byte stores, lanes of a warp on consecutive vectors;
 //   * the few elements before the first VB-aligned address (head) and after
-//     the last whole vector (tail) are done one by one by the first threads of
-//     the grid, in the same launch.
+//     the last whole vector (tail) are done one by one by block 0, in the same
+//     launch.
+// With one chunk per block (the default "one-shot" schedule) the hardware
+// block scheduler hands chunks to whichever SM frees a slot first, which
+// balances the SMs at the end of the array; a grid of SMs x resident blocks
+// (the "persistent" schedule) walks the same chunks with a grid stride.
 #pragma once
 
 #include "ew_device.cuh"
@@ -28,39 +32,48 @@ template <class Op, int VB, int U>
 __global__ void __launch_bounds__(kBlock) stream_kernel(const StreamArgs a) {
     const Op op = make_op<Op>(a.alpha);
     constexpr int E = Op::kElem;
+    constexpr int64_t kChunk = static_cast<int64_t>(kBlock) * U;  // vectors per chunk
     const char *in0 = static_cast<const char *>(a.in0);
     const char *in1 = static_cast<const char *>(a.in1);
     char *out = static_cast<char *>(a.out);
-    const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
 
-    // scalar head [0, head) and tail [tail0, n)
-    if (t < a.head) apply_one(op, in0, in1, out, t * E);
-    if (t < a.n - a.tail0) apply_one(op, in0, in1, out, (a.tail0 + t) * E);
+    // scalar head [0, head) and tail [tail0, n): fewer than 32 elements in all
+    if (blockIdx.x == 0) {
+        const int64_t t = threadIdx.x;
+        if (t < a.head) apply_one(op, in0, in1, out, t * E);
+        if (t < a.n - a.tail0) apply_one(op, in0, in1, out, (a.tail0 + t) * E);
+    }
 
-    // vector body
     const int64_t base = a.head * E;
     const char *b0 = in0 + base;
     const char *b1 = (Op::kIn == 2) ? in1 + base : nullptr;
     char *bo = out + base;
     const int64_t nvec = a.nvec;
-    int64_t v = t;
-    for (; v + (U - 1) * nthr < nvec; v += U * nthr) {
-        Vec<VB> x[U], y[U];
+    const int64_t nchunks = (nvec + kChunk - 1) / kChunk;
+    for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+        const int64_t v0 = c * kChunk + threadIdx.x;
+        if ((c + 1) * kChunk <= nvec) {  // whole chunk: no bounds checks
+            Vec<VB> x[U], y[U];
 #pragma unroll
-        for (int j = 0; j < U; ++j) {
-            x[j] = ld<VB>(b0 + (v + j * nthr) * VB);
-            if constexpr (Op::kIn == 2) y[j] = ld<VB>(b1 + (v + j * nthr) * VB);
-            else y[j] = x[j];
+            for (int j = 0; j < U; ++j) {
+                x[j] = ld<VB>(b0 + (v0 + j * kBlock) * VB);
+                if constexpr (Op::kIn == 2) y[j] = ld<VB>(b1 + (v0 + j * kBlock) * VB);
+                else y[j] = x[j];
+            }
+#pragma unroll
+            for (int j = 0; j < U; ++j) st<VB>(bo + (v0 + j * kBlock) * VB, apply<Op, VB>(op, x[j], y[j]));
+        } else {  // last, partial chunk
+#pragma unroll
+            for (int j = 0; j < U; ++j) {
+                const int64_t v = v0 + j * kBlock;
+                if (v < nvec) {
+                    const Vec<VB> x = ld<VB>(b0 + v * VB);
+                    Vec<VB> y = x;
+                    if constexpr (Op::kIn == 2) y = ld<VB>(b1 + v * VB);
+                    st<VB>(bo + v * VB, apply<Op, VB>(op, x, y));
+                }
+            }
         }
-#pragma unroll
-        for (int j = 0; j < U; ++j) st<VB>(bo + (v + j * nthr) * VB, apply<Op, VB>(op, x[j], y[j]));
-    }
-    for (; v < nvec; v += nthr) {
-        const Vec<VB> x = ld<VB>(b0 + v * VB);
-        Vec<VB> y = x;
-        if constexpr (Op::kIn == 2) y = ld<VB>(b1 + v * VB);
-        st<VB>(bo + v * VB, apply<Op, VB>(op, x, y));
     }
 }
 
@@ -70,7 +83,7 @@ cudaError_t launch_stream(const StreamArgs &a, int grid, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-// Loads in flight per thread per input, by width: about 64 bytes each.
+// Loads in flight per thread per input, by width: 64 bytes each.
 template <int VB> struct UnrollFor { static constexpr int value = VB >= 32 ? 2 : VB == 16 ? 4 : 8; };
 
 template <class Op, int VB>
@@ -85,31 +98,55 @@ constexpr StreamEntry kNoEntry{nullptr, nullptr, 0};
 // out[i] = in[(s*i) mod n] ("CUDA-MODE lecture notes" §3.2, non-coalesced copy,
 // s = 2 on the page).  One output element per access, as on the page, so a
 // warp's load touches every s-th element of a span of 32*s elements while its
-// store covers 32 consecutive elements.  With i = v + j*T (T = grid threads),
-// (s*i) mod n advances by (s*T) mod n per unrolled slot: the index needs one
-// modular product per thread and conditional subtractions afterwards.
+// store covers 32 consecutive elements.
 
-__device__ __forceinline__ uint64_t mulmod_u64(uint64_t a, uint64_t b, uint64_t n) {
-    // a, b < n <= 2^63: doubling and adding stay below 2^64
-    uint64_t r = 0;
-    while (b != 0) {
-        if (b & 1u) {
-            r += a;
-            if (r >= n) r -= n;
-        }
-        a += a;
-        if (a >= n) a -= n;
-        b >>= 1;
-    }
-    return r;
-}
 __device__ __forceinline__ uint64_t addmod_u64(uint64_t a, uint64_t b, uint64_t n) {
     const uint64_t r = a + b;  // a, b < n <= 2^63
     return r >= n ? r - n : r;
 }
+__device__ __forceinline__ uint64_t mulmod_u64(uint64_t a, uint64_t b, uint64_t n) {
+    // a, b < n <= 2^63: doubling and adding stay below 2^64
+    uint64_t r = 0;
+    while (b != 0) {
+        if (b & 1u) r = addmod_u64(r, a, n);
+        a = addmod_u64(a, a, n);
+        b >>= 1;
+    }
+    return r;
+}
 
+// One-shot gather for n <= 2^32: thread handles outputs i0 + k*kBlock (k < U)
+// of its block's chunk.  (s mod n) * i0 < 2^64 is reduced mod n with the
+// precomputed m = floor((2^64 - 1) / n): q = floor(x*m / 2^64) undershoots
+// floor(x/n) by at most 2, so r = x - q*n needs at most two subtractions of n.
+// Later slots add (s*kBlock) mod n with one conditional subtraction.
 template <int E, int U>
-__global__ void __launch_bounds__(kBlock) gather_kernel(const GatherArgs g) {
+__global__ void __launch_bounds__(kBlock) gather_oneshot_kernel(const GatherArgs g) {
+    const char *in = static_cast<const char *>(g.in);
+    char *out = static_cast<char *>(g.out);
+    const uint64_t n = g.n;
+    const uint64_t i0 = static_cast<uint64_t>(blockIdx.x) * (kBlock * U) + threadIdx.x;
+    if (i0 >= n) return;
+    const uint64_t x = g.s_mod * i0;
+    uint64_t j = x - __umul64hi(x, g.barrett_m) * n;
+    j = (j >= n) ? j - n : j;
+    j = (j >= n) ? j - n : j;
+    Vec<E> v[U];
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+        if (i0 + k * kBlock < n) v[k] = ld<E>(in + j * E);
+        j = addmod_u64(j, g.step_mod, n);
+    }
+#pragma unroll
+    for (int k = 0; k < U; ++k)
+        if (i0 + k * kBlock < n) st<E>(out + (i0 + k * kBlock) * E, v[k]);
+}
+
+// Grid-stride gather for any n: with i = v + k*T (T = grid threads),
+// (s*i) mod n advances by (s*T) mod n per slot, so each thread needs one
+// modular product and then conditional subtractions.
+template <int E, int U>
+__global__ void __launch_bounds__(kBlock) gather_stride_kernel(const GatherArgs g) {
     const char *in = static_cast<const char *>(g.in);
     char *out = static_cast<char *>(g.out);
     const uint64_t n = g.n;
@@ -136,8 +173,13 @@ __global__ void __launch_bounds__(kBlock) gather_kernel(const GatherArgs g) {
 }
 
 template <int E, int U>
-cudaError_t launch_gather(const GatherArgs &g, int grid, cudaStream_t s) {
-    gather_kernel<E, U><<<grid, kBlock, 0, s>>>(g);
+cudaError_t launch_gather_oneshot(const GatherArgs &g, int grid, cudaStream_t s) {
+    gather_oneshot_kernel<E, U><<<grid, kBlock, 0, s>>>(g);
+    return cudaGetLastError();
+}
+template <int E, int U>
+cudaError_t launch_gather_stride(const GatherArgs &g, int grid, cudaStream_t s) {
+    gather_stride_kernel<E, U><<<grid, kBlock, 0, s>>>(g);
     return cudaGetLastError();
 }
 

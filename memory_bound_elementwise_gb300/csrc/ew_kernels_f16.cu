@@ -19,13 +19,17 @@ const StreamEntry kTable[OP_COUNT][5] = {
     {e16<OpCopy<2>>(0), e16<OpCopy<2>>(1), e16<OpCopy<2>>(2), e16<OpCopy<2>>(3), e16<OpCopy<2>>(4)},
 };
 
-constexpr int kGatherUnroll = 8;
-const GatherEntry kGather2{reinterpret_cast<const void *>(&gather_kernel<2, kGatherUnroll>),
-                           &launch_gather<2, kGatherUnroll>, kGatherUnroll};
+constexpr int kGatherOneshotUnroll = 4;
+constexpr int kGatherStrideUnroll = 8;
+const GatherEntry kGatherOneshot{reinterpret_cast<const void *>(&gather_oneshot_kernel<2, kGatherOneshotUnroll>),
+                                 &launch_gather_oneshot<2, kGatherOneshotUnroll>, kGatherOneshotUnroll};
+const GatherEntry kGatherStride{reinterpret_cast<const void *>(&gather_stride_kernel<2, kGatherStrideUnroll>),
+                                &launch_gather_stride<2, kGatherStrideUnroll>, kGatherStrideUnroll};
 }  // namespace
 
 const StreamEntry *stream_table_f16() { return &kTable[0][0]; }
 
-const GatherEntry *gather_entry_2() { return &kGather2; }
+const GatherEntry *gather_oneshot_2() { return &kGatherOneshot; }
+const GatherEntry *gather_stride_2() { return &kGatherStride; }
 
 }  // namespace ew

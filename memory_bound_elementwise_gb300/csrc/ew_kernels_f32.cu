@@ -17,13 +17,17 @@ const StreamEntry kTable[OP_COUNT][5] = {
     {e32<OpCopy<4>>(0), e32<OpCopy<4>>(1), e32<OpCopy<4>>(2), e32<OpCopy<4>>(3), kNoEntry},
 };
 
-constexpr int kGatherUnroll = 8;
-const GatherEntry kGather4{reinterpret_cast<const void *>(&gather_kernel<4, kGatherUnroll>),
-                           &launch_gather<4, kGatherUnroll>, kGatherUnroll};
+constexpr int kGatherOneshotUnroll = 4;
+constexpr int kGatherStrideUnroll = 8;
+const GatherEntry kGatherOneshot{reinterpret_cast<const void *>(&gather_oneshot_kernel<4, kGatherOneshotUnroll>),
+                                 &launch_gather_oneshot<4, kGatherOneshotUnroll>, kGatherOneshotUnroll};
+const GatherEntry kGatherStride{reinterpret_cast<const void *>(&gather_stride_kernel<4, kGatherStrideUnroll>),
+                                &launch_gather_stride<4, kGatherStrideUnroll>, kGatherStrideUnroll};
 }  // namespace
 
 const StreamEntry *stream_table_f32() { return &kTable[0][0]; }
 
-const GatherEntry *gather_entry_4() { return &kGather4; }
+const GatherEntry *gather_oneshot_4() { return &kGatherOneshot; }
+const GatherEntry *gather_stride_4() { return &kGatherStride; }
 
 }  // namespace ew

@@ -1,11 +1,198 @@
-// ew_tma.cu -- bulk-copy staging variant and the device error word.
+// ew_tma.cu -- bulk-copy staging variant of the streaming kernels, and the
+// device error word that bounded waits report through.
+//
+// Each CTA owns kTmaStages consecutive tiles of kTmaTile bytes per input.
+// Thread 0 arms one mbarrier per tile and issues every tile's global->shared
+// bulk copy (cp.async.bulk ... mbarrier::complete_tx) up front; then, tile by
+// tile, the CTA waits for the bytes, applies the operator in shared memory
+// (result over the first input's buffer), makes the writes visible to the
+// async proxy and thread 0 bulk-stores the tile (cp.async.bulk.global.shared).
+// Latency is hidden across CTAs: many such CTAs are resident per SM and the
+// block scheduler hands out the next tiles as CTAs finish.  No multicast, no
+// clusters.  Elements before the first 16-byte aligned address and after the
+// last whole tile are done one by one by block 0.
+//
+// Every mbarrier wait is bounded (%globaltimer): when it gives up the CTA
+// records an error code, lets copies already in flight land (again bounded),
+// drains its bulk stores and returns; the host reads the code with
+// ew_device_error.
+#include <type_traits>
+
 #include "ew_internal.h"
+#include "ew_kernels.cuh"
 
 namespace ew {
 
-// Written by a kernel whose bounded wait gave up (the value names the wait
-// site); read and cleared by the host through ew_device_error.
 __device__ int32_t g_device_error = 0;
+
+namespace {
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t phase) {
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(done) : "r"(smem_addr(bar)), "r"(phase) : "memory");
+    return done != 0;
+}
+// true when the phase completed, false when limit_ns passed first
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t phase, uint64_t limit_ns) {
+    const uint64_t t0 = global_timer_ns();
+    uint32_t spins = 0;
+    while (!mbar_try_wait(bar, phase)) {
+        if ((++spins & 255u) == 0u && global_timer_ns() - t0 > limit_ns) return false;
+    }
+    return true;
+}
+__device__ __forceinline__ void bulk_load(void *dst_smem, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(smem_addr(dst_smem)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void bulk_store(void *dst, const void *src_smem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 :: "l"(dst), "r"(smem_addr(src_smem)), "r"(bytes) : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_store_drain() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void fence_to_async_proxy() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void record_error(int32_t code) { atomicCAS(&g_device_error, 0, code); }
+
+template <class Op> struct IsCopy : std::false_type {};
+template <int E> struct IsCopy<OpCopy<E>> : std::true_type {};
+
+template <class Op>
+__global__ void __launch_bounds__(kTmaBlock) tma_kernel(const TmaArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int s_failed;
+    constexpr int NIN = Op::kIn, E = Op::kElem, T = kTmaTile, S = kTmaStages;
+    unsigned char *buf0 = smem;
+    unsigned char *buf1 = smem + S * T;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + NIN * S * T);
+    const Op op = make_op<Op>(a.alpha);
+    const char *in0 = static_cast<const char *>(a.in0);
+    const char *in1 = static_cast<const char *>(a.in1);
+    char *out = static_cast<char *>(a.out);
+
+    if (blockIdx.x == 0) {  // scalar head and remainder
+        for (int64_t i = threadIdx.x; i < a.head; i += kTmaBlock) apply_one(op, in0, in1, out, i * E);
+        for (int64_t i = a.rem0 + threadIdx.x; i < a.n; i += kTmaBlock) apply_one(op, in0, in1, out, i * E);
+    }
+    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * S;
+    if (t0 >= a.ntiles) return;
+    const int cnt = static_cast<int>(a.ntiles - t0 < S ? a.ntiles - t0 : S);
+    const char *g0 = in0 + a.head * E;
+    const char *g1 = (NIN == 2) ? in1 + a.head * E : nullptr;
+    char *go = out + a.head * E;
+
+    if (threadIdx.x == 0) {
+        s_failed = 0;
+        for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+        mbar_init_fence();
+        for (int s = 0; s < cnt; ++s) {
+            mbar_arrive_expect_tx(&full[s], NIN * T);
+            bulk_load(buf0 + s * T, g0 + (t0 + s) * T, T, &full[s]);
+            if constexpr (NIN == 2) bulk_load(buf1 + s * T, g1 + (t0 + s) * T, T, &full[s]);
+        }
+    }
+    __syncthreads();
+    int s = 0;
+    for (; s < cnt; ++s) {
+        if (threadIdx.x == 0 && !mbar_wait_bounded(&full[s], 0, a.wait_limit_ns)) {
+            s_failed = 1;
+            record_error(1);
+        }
+        __syncthreads();
+        if (s_failed) break;
+        if constexpr (!IsCopy<Op>::value) {
+            uint4 *x4 = reinterpret_cast<uint4 *>(buf0 + s * T);
+            const uint4 *y4 = reinterpret_cast<const uint4 *>(buf1 + s * T);
+#pragma unroll
+            for (int i = threadIdx.x; i < T / 16; i += kTmaBlock) {
+                uint4 x = x4[i];
+                const uint4 y = (NIN == 2) ? y4[i] : x;
+                x.x = op.word(x.x, y.x);
+                x.y = op.word(x.y, y.y);
+                x.z = op.word(x.z, y.z);
+                x.w = op.word(x.w, y.w);
+                x4[i] = x;
+            }
+            fence_to_async_proxy();
+            __syncthreads();
+        }
+        if (threadIdx.x == 0) bulk_store(go + (t0 + s) * T, buf0 + s * T, T);
+    }
+    if (threadIdx.x == 0) {
+        bulk_store_drain();
+        if (s_failed)  // let copies still in flight land before the CTA exits
+            for (int r = s; r < cnt; ++r) (void)mbar_wait_bounded(&full[r], 0, a.wait_limit_ns);
+    }
+}
+
+template <class Op>
+cudaError_t launch_tma(const TmaArgs &a, int grid, cudaStream_t s) {
+    constexpr int smem = Op::kIn * kTmaStages * kTmaTile + kTmaStages * 8;
+    tma_kernel<Op><<<grid, kTmaBlock, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <class Op>
+constexpr TmaEntry tma_entry_of() {
+    return TmaEntry{reinterpret_cast<const void *>(&tma_kernel<Op>), &launch_tma<Op>,
+                    Op::kIn * kTmaStages * kTmaTile + kTmaStages * 8};
+}
+
+const TmaEntry kTma[OP_COUNT][DT_COUNT] = {
+    {tma_entry_of<OpAddF32>(), tma_entry_of<OpAddF16>(), tma_entry_of<OpAddBF16>()},
+    {tma_entry_of<OpSaxpyF32>(), tma_entry_of<OpSaxpyF16>(), tma_entry_of<OpSaxpyBF16>()},
+    {tma_entry_of<OpReluF32>(), tma_entry_of<OpReluF16>(), tma_entry_of<OpReluBF16>()},
+    {tma_entry_of<OpCopy<4>>(), tma_entry_of<OpCopy<2>>(), tma_entry_of<OpCopy<2>>()},
+};
+
+// Arms an mbarrier for 16 bytes that no copy will deliver: the bounded wait
+// must give up, record code 99 and return.  Nothing is in flight.
+__global__ void wait_selftest_kernel(uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        mbar_init_fence();
+        mbar_arrive_expect_tx(&bar, 16);
+        if (!mbar_wait_bounded(&bar, 0, limit_ns)) record_error(99);
+    }
+}
+
+}  // namespace
+
+const TmaEntry *tma_entry(int op, int dtype) {
+    if (op < 0 || op >= OP_COUNT || dtype < 0 || dtype >= DT_COUNT) return nullptr;
+    return &kTma[op][dtype];
+}
+
+cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t s) {
+    wait_selftest_kernel<<<1, 32, 0, s>>>(limit_ns);
+    return cudaGetLastError();
+}
 
 cudaError_t read_and_clear_device_error(cudaStream_t s, int32_t *code) {
     int32_t v = 0;
@@ -20,7 +207,5 @@ cudaError_t read_and_clear_device_error(cudaStream_t s, int32_t *code) {
     *code = v;
     return e;
 }
-
-const TmaEntry *tma_entry(int, int) { return nullptr; }
 
 }  // namespace ew

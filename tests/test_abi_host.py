@@ -76,6 +76,10 @@ def test_argument_errors_are_caught_on_the_host():
     assert L.ew_set_path(9) == INVALID
     assert L.ew_set_path(-1) == INVALID
     assert L.ew_set_pointer_check(2) == INVALID
+    assert L.ew_set_schedule(3) == INVALID
+    assert L.ew_set_schedule(-1) == INVALID
+    assert L.ew_selftest_bounded_wait(0, None) == INVALID
+    assert L.ew_selftest_bounded_wait(10 ** 11, None) == INVALID
     assert ew.last_launch()["launches"] == 0
 
 
@@ -129,6 +133,25 @@ def test_plan_different_offsets_fall_back_to_shared_width():
     # bf16 offsets 2 and 6 bytes: agree modulo 4 -> packed pairs after a 1-element head
     p = plan(2, [P + 2, P + 6], n)
     assert p["vec_bytes"] == 4 and p["head"] == 1 and p["nvec"] == (n - 1) // 2
+
+
+def test_plan_bulk_copy_tiles():
+    # 8 KiB tiles after a head that reaches 16-byte alignment
+    n = (1 << 20) + 3
+    p = plan(0, [P, P + (1 << 24), P + (2 << 24)], n, "tma")
+    assert p == {"path": 4, "vec_bytes": 16, "head": 0, "nvec": n // 2048, "tail": n % 2048}
+    p = plan(2, [P + 2, P + 2 + 4096, P + 2 + 8192], 100_000, "tma")
+    assert p["path"] == 4 and p["head"] == 7
+    assert p["head"] + p["nvec"] * 4096 + p["tail"] == 100_000
+    # pointers that disagree modulo 16 cannot use bulk copies
+    p = plan(0, [P + 4, P, P + 8], 100_000, "tma")
+    assert p["path"] != 4
+
+
+def test_schedule_roundtrip():
+    for name in ("oneshot", "persistent", "auto"):
+        ew.set_schedule(name)
+        assert ew.get_schedule() == name
 
 
 def test_plan_forced_widths():

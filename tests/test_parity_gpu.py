@@ -21,7 +21,7 @@ from tests.gpu_util import GuardedBuffer, assert_bits_equal, ESIZE
 pytestmark = pytest.mark.gpu
 
 DTYPES = ["f32", "f16", "bf16"]
-PATHS = ["auto", "scalar", "v128", "v256"]
+PATHS = ["auto", "scalar", "v128", "v256", "tma"]
 SMALL_N = [1, 2, 3, 5, 7, 8, 9, 15, 16, 17, 31, 32, 33, 64, 255, 257, 1000, 4099, 70001]
 DT_CODE = {"f32": 0, "f16": 1, "bf16": 2}
 
@@ -29,8 +29,11 @@ DT_CODE = {"f32": 0, "f16": 1, "bf16": 2}
 @pytest.fixture(autouse=True)
 def _reset_path():
     ew.set_path("auto")
+    ew.set_schedule("auto")
     yield
     ew.set_path("auto")
+    ew.set_schedule("auto")
+    assert ew.device_error() == (0, 0), "a bounded device wait gave up during the test"
 
 
 def _stream():
@@ -74,7 +77,7 @@ def make_inputs(dtype, n, seed, specials=True):
     return x, y
 
 
-def check_case(op, dtype, n, offs, seed, path="auto"):
+def check_case(op, dtype, n, offs, seed, path="auto", schedule="auto"):
     x, y = make_inputs(dtype, n, seed)
     nin = {"add": 2, "saxpy": 2, "relu": 1, "copy": 1}[op]
     if op == "saxpy":
@@ -91,6 +94,7 @@ def check_case(op, dtype, n, offs, seed, path="auto"):
         bo = GuardedBuffer(n, dtype, offs[1])
         bufs, outb = [bx, bo], bo
     ew.set_path(path)
+    ew.set_schedule(schedule)
     run_op(op, dtype, bufs, n)
     rec = ew.last_launch()
     torch.cuda.synchronize()
@@ -112,18 +116,78 @@ def test_small_sizes_every_offset(op, dtype):
             check_case(op, dtype, n, [off] * nin, seed=1000 + n * 37 + off)
 
 
+@pytest.mark.parametrize("schedule", ["oneshot", "persistent"])
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("op", ["add", "saxpy", "relu", "copy"])
-def test_forced_paths(op, dtype, path):
-    for n in (1, 33, 1000, 70001):
+def test_forced_paths(op, dtype, path, schedule):
+    for n in (1, 33, 1000, 70001, 600_001):
         for off in (0, 1, 3):
             nin = 3 if op == "add" else 2
-            rec = check_case(op, dtype, n, [off] * nin, seed=2000 + n + off, path=path)
+            rec = check_case(op, dtype, n, [off] * nin, seed=2000 + n + off, path=path,
+                             schedule=schedule)
             if path == "scalar":
                 assert rec["vec_bytes"] == ESIZE[dtype]
             elif path == "v128":
                 assert rec["vec_bytes"] <= 16
+            elif path == "tma":
+                assert rec["path"] == 4 and rec["vec_bytes"] == 16
+            if path != "tma" and rec["nvec"] > 0:
+                assert rec["schedule"] == (1 if schedule == "oneshot" else 2)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("op", ["add", "saxpy", "relu", "copy"])
+def test_tma_tile_boundaries(op, dtype):
+    """Sizes around the 8 KiB bulk-copy tile and the 2-tile CTA, at offsets that
+    keep or break 16-byte alignment (the latter falls back to vector loads)."""
+    per_tile = 8192 // ESIZE[dtype]
+    sizes = [1, per_tile - 1, per_tile, per_tile + 1, 2 * per_tile, 2 * per_tile + 5,
+             3 * per_tile + 7, 5 * per_tile - 3, 70001]
+    for n in sizes:
+        for off in (0, 1, 16 // ESIZE[dtype], 3):
+            nin = 3 if op == "add" else 2
+            rec = check_case(op, dtype, n, [off] * nin, seed=2500 + n + off, path="tma")
+            assert rec["path"] == 4
+            assert rec["head"] + rec["nvec"] * per_tile + rec["tail"] == n
+
+
+def test_bounded_wait_gives_up_and_reports():
+    """The self-test block arms an mbarrier that nothing completes: its wait
+    must end after the limit with code 99, and the word must read clear after."""
+    import time
+    t0 = time.perf_counter()
+    ew.selftest_bounded_wait(50_000_000)  # 50 ms
+    st, code = ew.device_error()
+    elapsed = time.perf_counter() - t0
+    assert (st, code) == (7, 99)
+    assert 0.04 < elapsed < 5.0
+    assert ew.device_error() == (0, 0)
+    # the context is still usable afterwards
+    x = torch.arange(1000, dtype=torch.float32, device="cuda")
+    y = ew.ew_relu(x - 500)
+    torch.cuda.synchronize()
+    assert float(y.sum()) == float(sum(range(1, 500)))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_gather_schedules_agree(dtype):
+    L = ew.lib()
+    for sched in ("oneshot", "persistent"):
+        ew.set_schedule(sched)
+        for n in (1, 5, 4097, 300_001):
+            x = inputs.random_bits(n, dtype, 6500 + n)
+            for s in (2, 3, n + 1, (1 << 33) + 1):
+                bi = GuardedBuffer(n, dtype, 1).fill(x)
+                bo = GuardedBuffer(n, dtype, 0)
+                assert L.ew_gather_stride(DT_CODE[dtype], bi.view.data_ptr(), bo.view.data_ptr(),
+                                          n, s, _stream()) == 0
+                rec = ew.last_launch()
+                assert rec["schedule"] == (1 if sched == "oneshot" else 2)
+                torch.cuda.synchronize()
+                assert_bits_equal(bo.host(), oracle.gather_stride(x, s), dtype, False,
+                                  "gather %s n=%d s=%d" % (sched, n, s))
+                assert bi.guards_intact() and bo.guards_intact()
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
@@ -325,6 +389,15 @@ def test_config_copy_and_gather_f32_2p26():
 
 def test_config_add_f32_2p28():
     _full("add", "f32", 1 << 28, inputs.seed_for("add_f32"), inputs.seed_for("add_f32", 1))
+
+
+@pytest.mark.parametrize("path,schedule", [("tma", "auto"), ("v256", "persistent")])
+def test_config_add_f32_2p28_other_variants(path, schedule):
+    """The headline workload through the bulk-copy path and the persistent schedule."""
+    ew.set_path(path)
+    ew.set_schedule(schedule)
+    rec = _full("add", "f32", 1 << 28, inputs.seed_for("add_f32"), inputs.seed_for("add_f32", 1))
+    assert rec["path"] == (4 if path == "tma" else 3)
 
 
 def test_beyond_2p31_elements_f16():
