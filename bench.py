@@ -55,7 +55,61 @@ def parse():
     p.add_argument("--no-aux", action="store_true", help="skip the other workloads")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     p.add_argument("--path", default="auto", help="kernel variant: auto, scalar, v128, v256, tma")
+    p.add_argument("--schedule", default="auto", help="block schedule: auto, oneshot, persistent")
+    p.add_argument("--profile-case", default=None, choices=sorted(PROFILE_CASES),
+                   help="run only warmup+steps launches of one workload at --n (for ncu captures)")
     return p.parse_args()
+
+
+# op, dtype, element offset of every pointer, input distribution
+PROFILE_CASES = {
+    "add_f32": ("add", "f32", 0),
+    "add_bf16_off1": ("add", "bf16", 1),
+    "saxpy_f32": ("saxpy", "f32", 0),
+    "relu_f32": ("relu", "f32", 0),
+    "copy_f32": ("copy", "f32", 0),
+    "gather2_f32": ("gather", "f32", 0),
+}
+
+
+def run_profile_case(args):
+    """Launch one workload warmup+steps times on the current stream (used under
+    ncu: the launch list and the per-kernel counters come from this)."""
+    import torch
+
+    import memory_bound_elementwise_gb300 as ew
+    from memory_bound_elementwise_gb300 import inputs
+    op, dtype, off = PROFILE_CASES[args.profile_case]
+    ew.set_path(args.path)
+    ew.set_schedule(args.schedule)
+    n = args.n
+    e = 4 if dtype == "f32" else 2
+    dev = torch.device("cuda", 0)
+
+    def buf(arr):
+        raw = torch.empty(arr.size * e + 256, dtype=torch.uint8, device=dev)
+        raw[off * e: off * e + arr.size * e].copy_(torch.from_numpy(np.ascontiguousarray(arr).view(np.uint8)))
+        return raw, raw.data_ptr() + off * e
+
+    x = inputs.as_dtype(inputs.uniform(n, inputs.seed_for("add_f32")), dtype)
+    rx, px = buf(x)
+    ry, py = buf(inputs.as_dtype(inputs.uniform(n, inputs.seed_for("add_f32", 1)), dtype))
+    rz, pz = buf(np.zeros_like(x))
+    L = ew.lib()
+    s = torch.cuda.current_stream().cuda_stream
+    code = {"f32": 0, "f16": 1, "bf16": 2}[dtype]
+    call = {"add": lambda: L.ew_add(code, px, py, pz, n, s),
+            "saxpy": lambda: L.ew_saxpy(code, 2.5, px, py, n, s),
+            "relu": lambda: L.ew_relu(code, px, pz, n, s),
+            "copy": lambda: L.ew_copy(code, px, pz, n, s),
+            "gather": lambda: L.ew_gather_stride(code, px, pz, n, 2, s)}[op]
+    for _ in range(args.warmup + args.steps):
+        st = call()
+        if st != 0:
+            raise ew.EwError(st, args.profile_case)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": args.profile_case, "n": n, "launches": args.warmup + args.steps,
+                      "launch": ew.last_launch()}))
 
 
 # ---------------------------------------------------------------- helpers
@@ -358,6 +412,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     stream = torch.cuda.Stream(dev)
     ew.set_path(args.path)
+    ew.set_schedule(args.schedule)
     n = args.n
     lo, hi = weak_scaling_range(n, rank)
 
@@ -473,7 +528,9 @@ def run_ours(args):
 
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.profile_case:
+        run_profile_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
