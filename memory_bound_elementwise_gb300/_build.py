@@ -39,15 +39,18 @@ def nvcc():
 
 
 def _inputs_digest():
+    """SHA-256 over the kernel sources, the public header and the compiler
+    flags, independent of where the repository sits on disk."""
     h = hashlib.sha256()
-    files = sorted(os.listdir(CSRC)) + ["../../include/ew.h"]
-    for name in files:
-        path = os.path.normpath(os.path.join(CSRC, name))
-        if os.path.isfile(path):
-            h.update(name.encode())
-            with open(path, "rb") as f:
-                h.update(f.read())
-    h.update(" ".join(ARCH + NVCC_FLAGS).encode())
+    files = [os.path.join(CSRC, name) for name in sorted(os.listdir(CSRC))
+             if name.endswith((".cu", ".cuh", ".h"))]
+    files.append(os.path.join(INCLUDE, "ew.h"))
+    for path in files:
+        h.update(os.path.relpath(path, ROOT).encode())
+        with open(path, "rb") as f:
+            h.update(f.read())
+    flags = [f for f in ARCH + NVCC_FLAGS if f not in (INCLUDE, CSRC)]
+    h.update(" ".join(flags).encode())
     return h.hexdigest()
 
 
