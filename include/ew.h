@@ -30,8 +30,11 @@
  *   copy/gather  raw element bits.
  *
  * Common conventions
- *   Pointers   device pointers (cudaMalloc, cudaMallocAsync, or any memory the
- *              current device can address), owned by the caller.  The library
+ *   Pointers   any memory the current device can address, owned by the caller:
+ *              device memory (cudaMalloc, cudaMallocAsync), managed memory,
+ *              page-locked host memory, and on devices with pageable memory
+ *              access (GB300 with its Grace CPU) plain host memory too, which
+ *              the kernels then read and write over the CPU-GPU link.  The library
  *              allocates no memory and keeps no reference after a call returns.
  *              Each pointer must be aligned to the element size (4 bytes for
  *              EW_F32, 2 for EW_F16/EW_BF16), else EW_ERR_INVALID_VALUE.  Any
@@ -154,8 +157,10 @@ EW_API ew_status ew_set_schedule(ew_schedule schedule);
 EW_API ew_schedule ew_get_schedule(void);
 
 /* Enable (1) or disable (0, the default) a cudaPointerGetAttributes check of
- * every pointer before launch; a pointer the device cannot access then gives
- * EW_ERR_NOT_DEVICE_POINTER.  Process-wide. */
+ * every pointer before launch: device, managed and page-locked host memory
+ * pass, pageable host memory passes only on a device with pageable memory
+ * access; anything else gives EW_ERR_NOT_DEVICE_POINTER.  Process-wide.  The
+ * environment variable EW_CHECK_POINTERS=1 enables it at start-up. */
 EW_API ew_status ew_set_pointer_check(int enable);
 
 /* How an ew_add / ew_saxpy / ew_relu / ew_copy call with these pointers is

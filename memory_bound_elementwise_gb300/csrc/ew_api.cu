@@ -104,12 +104,12 @@ TmaPlan make_tma_plan(const ew_plan &pl16, int e, int64_t n) {
 
 // ---------------------------------------------------------------- devices
 
-struct DevInfo { int sms = 0; };
+struct DevInfo { int sms = 0; int pageable_access = 0; };
 std::mutex g_mu;
 std::map<int, DevInfo> g_dev;
 std::map<std::pair<int, const void *>, int> g_occ;
 
-cudaError_t device_info(int *dev, int *sms) {
+cudaError_t device_info(int *dev, int *sms, int *pageable_access = nullptr) {
     cudaError_t e = cudaGetDevice(dev);
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lk(g_mu);
@@ -118,9 +118,12 @@ cudaError_t device_info(int *dev, int *sms) {
         DevInfo d;
         e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, *dev);
         if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&d.pageable_access, cudaDevAttrPageableMemoryAccess, *dev);
+        if (e != cudaSuccess) return e;
         it = g_dev.emplace(*dev, d).first;
     }
     *sms = it->second.sms;
+    if (pageable_access) *pageable_access = it->second.pageable_access;
     return cudaSuccess;
 }
 
@@ -148,13 +151,21 @@ bool pointer_check_enabled() {
     return v == 1;
 }
 
+// Device memory, managed memory and page-locked host memory are reachable
+// from kernels; plain pageable host memory only where the device reports
+// pageable memory access (e.g. coherent CPU-GPU systems).
 ew_status check_device_pointers(const void *const *p, int np) {
+    int dev = 0, sms = 0, pageable = 0;
+    cudaError_t e = device_info(&dev, &sms, &pageable);
+    if (e != cudaSuccess) return cuda_fail(e);
     for (int k = 0; k < np; ++k) {
         cudaPointerAttributes at{};
-        cudaError_t e = cudaPointerGetAttributes(&at, p[k]);
+        e = cudaPointerGetAttributes(&at, p[k]);
         if (e != cudaSuccess) { cudaGetLastError(); return EW_ERR_NOT_DEVICE_POINTER; }
-        if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged)
-            return EW_ERR_NOT_DEVICE_POINTER;
+        const bool reachable = at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged ||
+                               at.type == cudaMemoryTypeHost ||
+                               (at.type == cudaMemoryTypeUnregistered && pageable == 1);
+        if (!reachable) return EW_ERR_NOT_DEVICE_POINTER;
     }
     return EW_OK;
 }

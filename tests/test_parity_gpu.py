@@ -280,19 +280,38 @@ def test_launch_record_and_grid():
     torch.cuda.synchronize()
 
 
-def test_pointer_check_rejects_host_memory():
-    import ctypes
-    host = (ctypes.c_float * 64)()
-    d = torch.zeros(64, device="cuda")
+def test_pointer_check_and_host_resident_buffers():
+    """With the pointer check on, pageable host memory is accepted exactly when
+    the device can access it (pageable memory access), and then computed over
+    the CPU-GPU link like device memory; page-locked host memory always is."""
+    n = 100_003
+    a, b = inputs.uniform(n, 7100), inputs.uniform(n, 7101)
+    want = oracle.add("f32", a, b)
     ew.set_pointer_check(True)
     try:
-        st = ew.lib().ew_add(0, ctypes.addressof(host), d.data_ptr(), d.data_ptr(), 64, _stream())
-        assert st == 5
-        st = ew.lib().ew_add(0, d.data_ptr(), d.data_ptr(), d.data_ptr(), 64, _stream())
-        assert st == 0
+        # pageable host memory (numpy arrays): reachable on coherent CPU-GPU
+        # systems such as GB300, rejected elsewhere
+        c = np.empty_like(a)
+        st = ew.lib().ew_add(0, a.ctypes.data, b.ctypes.data, c.ctypes.data, n, _stream())
+        assert st in (0, 5)
+        if st == 0:
+            torch.cuda.synchronize()
+            assert_bits_equal(c, want, "f32", True, "pageable host buffers")
+        # page-locked host memory
+        ta, tb = torch.from_numpy(a).pin_memory(), torch.from_numpy(b).pin_memory()
+        tc = torch.empty(n).pin_memory()
+        assert ew.lib().ew_add(0, ta.data_ptr(), tb.data_ptr(), tc.data_ptr(), n, _stream()) == 0
+        torch.cuda.synchronize()
+        assert_bits_equal(tc.numpy(), want, "f32", True, "pinned host buffers")
+        # mixed: host inputs, device output
+        d = torch.empty(n, device="cuda")
+        assert ew.lib().ew_add(0, ta.data_ptr(), tb.data_ptr(), d.data_ptr(), n, _stream()) == 0
+        torch.cuda.synchronize()
+        assert_bits_equal(d.cpu().numpy(), want, "f32", True, "host inputs, device output")
     finally:
         ew.set_pointer_check(False)
     torch.cuda.synchronize()
+
 
 
 def test_device_error_word_starts_clear():
