@@ -350,7 +350,32 @@ def aux_measurements(torch, ew, inputs, metrics, stream, peak, dev):
     rx, px = dev_of(x, "f32")
     ry, py = dev_of(np.zeros_like(x), "f32")
     record("relu_f32_2p28", "relu", "f32", n28, lambda: L.ew_relu(0, px, py, n28, s))
-    record("relu_f32_2p28_inplace", "relu", "f32", n28, lambda: L.ew_relu(0, py, py, n28, s))
+    # in place on fresh data: refill from the pristine copy before each launch
+    # (outside the event pair), so every timed launch sees ~50% negatives
+    kern_ms = []
+    for _ in range(13):
+        with torch.cuda.stream(stream):
+            ry.copy_(rx, non_blocking=True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        st = L.ew_relu(0, py, py, n28, s)
+        e1.record(stream)
+        if st != 0:
+            raise ew.EwError(st, "relu in place")
+        torch.cuda.synchronize()
+        kern_ms.append(e0.elapsed_time(e1))
+    kern = sum(kern_ms[3:]) / len(kern_ms[3:]) / 1e3
+    nb = metrics.algorithmic_bytes("relu", "f32", n28)
+    out["relu_f32_2p28_inplace_fresh"] = {"gbps": metrics.gbps(nb, kern), "frac": metrics.gbps(nb, kern) / peak,
+                                          "kernel_ms": kern * 1e3, "bytes_per_launch": nb,
+                                          "launch": ew.last_launch()}
+    # in place again on the now non-negative data: nothing changes, so no vector
+    # is stored (page's case B: 4 bytes per element, read only)
+    total, kern = time_launches(torch, stream, lambda: L.ew_relu(0, py, py, n28, s), 50, 3)
+    nb = 4 * n28
+    out["relu_f32_2p28_inplace_nonnegative"] = {
+        "gbps": metrics.gbps(nb, kern), "frac": metrics.gbps(nb, kern) / peak, "kernel_ms": kern * 1e3,
+        "bytes_per_launch": nb, "note": "read-only bytes: unchanged vectors are not stored"}
     del rx, ry
     n26 = 1 << 26
     x = inputs.uniform(n26, inputs.seed_for("copy_f32"), 0.0, 1.0)
@@ -370,12 +395,24 @@ def aux_measurements(torch, ew, inputs, metrics, stream, peak, dev):
            steps=500)
     del ra, rb, rc
     # the headline workload through the other variants: persistent schedule, bulk-copy path
-    a = inputs.uniform(n28, inputs.seed_for("add_f32"))
-    b = inputs.uniform(n28, inputs.seed_for("add_f32", 1))
+    a = inputs.normal(n28, inputs.seed_for("add_f32"))
+    b = inputs.normal(n28, inputs.seed_for("add_f32", 1))
     ra, pa = dev_of(a, "f32")
     rb, pb = dev_of(b, "f32")
     rc, pc = dev_of(np.zeros_like(a), "f32")
     del a, b
+    # bias add + ReLU fused in one pass, against ew_add then ew_relu in place
+    record("add_relu_f32_2p28_fused", "add_relu", "f32", n28, lambda: L.ew_add_relu(0, pa, pb, pc, n28, s))
+
+    def unfused():
+        st = L.ew_add(0, pa, pb, pc, n28, s)
+        return st if st != 0 else L.ew_relu(0, pc, pc, n28, s)
+    total, kern = time_launches(torch, stream, unfused, 50, 3)
+    nb = metrics.algorithmic_bytes("add_relu", "f32", n28)
+    out["add_then_relu_f32_2p28_unfused"] = {
+        "gbps": metrics.gbps(nb, kern), "frac": metrics.gbps(nb, kern) / peak, "kernel_ms": kern * 1e3,
+        "bytes_per_launch": nb, "note": "two launches per step (add, then ReLU in place); GB/s counts the "
+                                        "fused operation's 12 bytes per element"}
     for label, path, sched in (("persistent", "auto", "persistent"), ("tma", "tma", "auto")):
         ew.set_path(path)
         ew.set_schedule(sched)

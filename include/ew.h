@@ -127,8 +127,18 @@ EW_API ew_status ew_add(ew_dtype dtype, const void *a, const void *b, void *c, i
 EW_API ew_status ew_saxpy(ew_dtype dtype, float alpha, const void *x, void *y, int64_t n,
                    ew_stream_t stream);
 
-/* y = max(x, 0).  x: n inputs; y: n outputs (y == x computes in place). */
+/* y = max(x, 0).  x: n inputs; y: n outputs (y == x computes in place).  In
+ * place, a vector the operation leaves unchanged (no negative element and no
+ * -0) is not written back: CUDA-MODE lecture notes §5.2, example 1, case B,
+ * where a non-negative element needs no write. */
 EW_API ew_status ew_relu(ew_dtype dtype, const void *x, void *y, int64_t n, ew_stream_t stream);
+
+/* C = max(A + B, 0): the sum rounded as in ew_add, then ReLU as in ew_relu, in
+ * one pass over memory (a bias add fused with its activation; kernel fusion as
+ * CUDA-MODE lecture notes §5.3 lists it for memory-bound work).  Arguments and
+ * aliasing as in ew_add. */
+EW_API ew_status ew_add_relu(ew_dtype dtype, const void *a, const void *b, void *c, int64_t n,
+                             ew_stream_t stream);
 
 /* out = in.  in == out is a no-op that launches nothing. */
 EW_API ew_status ew_copy(ew_dtype dtype, const void *in, void *out, int64_t n, ew_stream_t stream);

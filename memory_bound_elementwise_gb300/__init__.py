@@ -10,6 +10,7 @@ Tensor entry points (same names as the C ABI)::
     ew_add(a, b, c=None)            C = A + B
     ew_saxpy(alpha, x, y)           y = alpha*x + y, in place
     ew_relu(x, y=None)              y = max(x, 0)  (y = x for in place)
+    ew_add_relu(a, b, c=None)       C = max(A + B, 0), one pass
     ew_copy(x, out)                 out = x
     ew_gather_stride(x, out, s)     out[i] = x[(s*i) mod n]
 
@@ -40,7 +41,8 @@ STATUS_NAMES = {0: "EW_OK", 1: "EW_ERR_INVALID_VALUE", 2: "EW_ERR_NULL_POINTER",
                 5: "EW_ERR_NOT_DEVICE_POINTER", 6: "EW_ERR_CUDA", 7: "EW_ERR_TIMEOUT"}
 
 # Every function declared in include/ew.h.
-EXPORTS = ("ew_add", "ew_saxpy", "ew_relu", "ew_copy", "ew_gather_stride", "ew_set_path",
+EXPORTS = ("ew_add", "ew_saxpy", "ew_relu", "ew_add_relu", "ew_copy", "ew_gather_stride",
+           "ew_set_path",
            "ew_get_path", "ew_set_schedule", "ew_get_schedule", "ew_set_pointer_check",
            "ew_plan_query", "ew_last_launch", "ew_status_string", "ew_last_cuda_error",
            "ew_device_error", "ew_selftest_bounded_wait", "ew_version")
@@ -87,9 +89,10 @@ def lib():
     L.ew_add.argtypes = [ctypes.c_int, vp, vp, vp, i64, vp]
     L.ew_saxpy.argtypes = [ctypes.c_int, f32, vp, vp, i64, vp]
     L.ew_relu.argtypes = [ctypes.c_int, vp, vp, i64, vp]
+    L.ew_add_relu.argtypes = [ctypes.c_int, vp, vp, vp, i64, vp]
     L.ew_copy.argtypes = [ctypes.c_int, vp, vp, i64, vp]
     L.ew_gather_stride.argtypes = [ctypes.c_int, vp, vp, i64, i64, vp]
-    for name in ("ew_add", "ew_saxpy", "ew_relu", "ew_copy", "ew_gather_stride",
+    for name in ("ew_add", "ew_saxpy", "ew_relu", "ew_add_relu", "ew_copy", "ew_gather_stride",
                  "ew_set_path", "ew_set_schedule", "ew_set_pointer_check", "ew_plan_query",
                  "ew_last_launch", "ew_device_error", "ew_selftest_bounded_wait"):
         getattr(L, name).restype = ctypes.c_int
@@ -181,6 +184,17 @@ def ew_relu(x, y=None, stream=None):
     return y
 
 
+def ew_add_relu(a, b, c=None, stream=None):
+    """C = max(A + B, 0) in one pass (c may be a or b); returns c."""
+    import torch
+    if c is None:
+        c = torch.empty_like(a)
+    dt, n = _check_tensors(a, b, c)
+    check(lib().ew_add_relu(dt, a.data_ptr(), b.data_ptr(), c.data_ptr(), n,
+                            _stream(stream, a.device)), "ew_add_relu")
+    return c
+
+
 def ew_copy(x, out, stream=None):
     """out = x (raw bits); returns out."""
     dt, n = _check_tensors(x, out)
@@ -252,6 +266,6 @@ def device_error(stream=None):
     return st, code.value
 
 
-__all__ = ["ew_add", "ew_saxpy", "ew_relu", "ew_copy", "ew_gather_stride", "set_path",
+__all__ = ["ew_add", "ew_saxpy", "ew_relu", "ew_add_relu", "ew_copy", "ew_gather_stride", "set_path",
            "get_path", "set_schedule", "get_schedule", "set_pointer_check", "plan_query",
            "last_launch", "device_error", "selftest_bounded_wait", "lib", "EwError", "EXPORTS"]

@@ -204,7 +204,7 @@ ew_status run_tma(int op, ew_dtype dt, const void *in0, const void *in1, void *o
 
 // Common path of add / saxpy / relu / copy once arguments are valid.
 ew_status run_stream(int op, ew_dtype dt, const void *in0, const void *in1, void *out,
-                     int64_t n, float alpha, cudaStream_t s) {
+                     int64_t n, float alpha, cudaStream_t s, bool skip_unchanged = false) {
     const int e = elem_size(dt);
     const void *ptrs[3] = {in0, out, in1};
     const int np = (in1 != nullptr) ? 3 : 2;
@@ -224,7 +224,8 @@ ew_status run_stream(int op, ew_dtype dt, const void *in0, const void *in1, void
     if (path == EW_PATH_TMA && pl.vec_bytes >= 16 && tma_entry(op, dt) != nullptr)
         return run_tma(op, dt, in0, in1, out, n, alpha, make_plan(EW_PATH_V128, e, up, np, n), s);
 
-    StreamArgs a{in0, in1, out, n, pl.head, pl.nvec, pl.head + pl.nvec * (pl.vec_bytes / e), alpha};
+    StreamArgs a{in0, in1, out, n, pl.head, pl.nvec, pl.head + pl.nvec * (pl.vec_bytes / e), alpha,
+                 skip_unchanged ? 1 : 0};
 
     // copy of 16-bit elements is one kernel for both 16-bit formats
     const int tdt = (op == OP_COPY && dt == EW_BF16) ? EW_F16 : dt;
@@ -310,7 +311,19 @@ ew_status ew_relu(ew_dtype dt, const void *x, void *y, int64_t n, ew_stream_t s)
     ew_status st = check_common(dt, n, p, 2);
     if (st != EW_OK || n == 0) return st;
     if ((st = check_alias(x, y, n * elem_size(dt))) != EW_OK) return st;
-    return run_stream(OP_RELU, dt, x, nullptr, y, n, 0.0f, reinterpret_cast<cudaStream_t>(s));
+    // in place, a vector that ReLU leaves unchanged is not stored again
+    return run_stream(OP_RELU, dt, x, nullptr, y, n, 0.0f, reinterpret_cast<cudaStream_t>(s), x == y);
+}
+
+ew_status ew_add_relu(ew_dtype dt, const void *a, const void *b, void *c, int64_t n, ew_stream_t s) {
+    t_last = ew_launch_record{};
+    const void *p[3] = {a, b, c};
+    ew_status st = check_common(dt, n, p, 3);
+    if (st != EW_OK || n == 0) return st;
+    const int64_t bytes = n * elem_size(dt);
+    if ((st = check_alias(a, c, bytes)) != EW_OK) return st;
+    if ((st = check_alias(b, c, bytes)) != EW_OK) return st;
+    return run_stream(OP_ADD_RELU, dt, a, b, c, n, 0.0f, reinterpret_cast<cudaStream_t>(s));
 }
 
 ew_status ew_copy(ew_dtype dt, const void *in, void *out, int64_t n, ew_stream_t s) {
@@ -462,6 +475,6 @@ ew_status ew_selftest_bounded_wait(int64_t limit_ns, ew_stream_t s) {
     return EW_OK;
 }
 
-int ew_version(void) { return 200; }
+int ew_version(void) { return 300; }
 
 }  // extern "C"

@@ -239,12 +239,59 @@ struct OpReluBF16 {
     __device__ __forceinline__ uint16_t half(uint16_t x, uint16_t) const { return relu_b16<0x7f80u>(x); }
 };
 
+// Fused bias add + ReLU: C = max(A + B, 0) with the sum rounded first, i.e.
+// exactly relu(add(A, B)) in one pass (12 bytes per binary32 element instead
+// of 12 + 8 for the two separate passes).
+struct OpAddReluF32 {
+    static constexpr int kIn = 2, kElem = 4;
+    __device__ __forceinline__ uint32_t word(uint32_t a, uint32_t b) const { return relu_b32(add_f32(a, b)); }
+    __device__ __forceinline__ uint16_t half(uint16_t, uint16_t) const { return 0; }
+};
+struct OpAddReluF16 {
+    static constexpr int kIn = 2, kElem = 2;
+    __device__ __forceinline__ uint32_t word(uint32_t a, uint32_t b) const {
+        return relu_b16x2<0x7c00u>(add_f16x2(a, b));
+    }
+    __device__ __forceinline__ uint16_t half(uint16_t a, uint16_t b) const {
+        return relu_b16<0x7c00u>(add_f16(a, b));
+    }
+};
+struct OpAddReluBF16 {
+    static constexpr int kIn = 2, kElem = 2;
+    __device__ __forceinline__ uint32_t word(uint32_t a, uint32_t b) const {
+        return relu_b16x2<0x7f80u>(add_bf16x2(a, b));
+    }
+    __device__ __forceinline__ uint16_t half(uint16_t a, uint16_t b) const {
+        return relu_b16<0x7f80u>(add_bf16(a, b));
+    }
+};
+
 template <int E>
 struct OpCopy {
     static constexpr int kIn = 1, kElem = E;
     __device__ __forceinline__ uint32_t word(uint32_t x, uint32_t) const { return x; }
     __device__ __forceinline__ uint16_t half(uint16_t x, uint16_t) const { return x; }
 };
+
+// Operators whose output can equal their only input bit for bit; for such an
+// operator computed in place, a vector whose result equals what is already in
+// memory need not be stored.
+template <class Op> struct MaySkipUnchanged { static constexpr bool value = false; };
+template <> struct MaySkipUnchanged<OpReluF32> { static constexpr bool value = true; };
+template <> struct MaySkipUnchanged<OpReluF16> { static constexpr bool value = true; };
+template <> struct MaySkipUnchanged<OpReluBF16> { static constexpr bool value = true; };
+
+template <int VB>
+__device__ __forceinline__ bool same_bits(const Vec<VB> &x, const Vec<VB> &y) {
+    if constexpr (VB == 2) {
+        return x.h == y.h;
+    } else {
+        uint32_t diff = 0;
+#pragma unroll
+        for (int k = 0; k < Vec<VB>::kWords; ++k) diff |= x.w[k] ^ y.w[k];
+        return diff == 0;
+    }
+}
 
 // Apply an operator to a whole vector.
 template <class Op, int VB>

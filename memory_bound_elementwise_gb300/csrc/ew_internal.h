@@ -10,7 +10,7 @@ namespace ew {
 constexpr int kBlock = 256;  // threads per block for the LSU kernels
 
 // Operator ids of the streaming (contiguous) kernels.
-enum OpId : int { OP_ADD = 0, OP_SAXPY = 1, OP_RELU = 2, OP_COPY = 3, OP_COUNT = 4 };
+enum OpId : int { OP_ADD = 0, OP_SAXPY = 1, OP_RELU = 2, OP_COPY = 3, OP_ADD_RELU = 4, OP_COUNT = 5 };
 // dtype ids match ew_dtype.
 enum DtId : int { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2, DT_COUNT = 3 };
 
@@ -31,6 +31,7 @@ struct StreamArgs {
     int64_t nvec;
     int64_t tail0;
     float alpha;
+    int32_t skip_unchanged;  // in-place ReLU: store only vectors whose bits change
 };
 
 using StreamLaunchFn = cudaError_t (*)(const StreamArgs &, int grid, cudaStream_t);

@@ -61,7 +61,13 @@ __global__ void __launch_bounds__(kBlock) stream_kernel(const StreamArgs a) {
                 else y[j] = x[j];
             }
 #pragma unroll
-            for (int j = 0; j < U; ++j) st<VB>(bo + (v0 + j * kBlock) * VB, apply<Op, VB>(op, x[j], y[j]));
+            for (int j = 0; j < U; ++j) {
+                const Vec<VB> z = apply<Op, VB>(op, x[j], y[j]);
+                if constexpr (MaySkipUnchanged<Op>::value) {
+                    if (a.skip_unchanged && same_bits<VB>(z, x[j])) continue;
+                }
+                st<VB>(bo + (v0 + j * kBlock) * VB, z);
+            }
         } else {  // last, partial chunk
 #pragma unroll
             for (int j = 0; j < U; ++j) {
@@ -70,7 +76,11 @@ __global__ void __launch_bounds__(kBlock) stream_kernel(const StreamArgs a) {
                     const Vec<VB> x = ld<VB>(b0 + v * VB);
                     Vec<VB> y = x;
                     if constexpr (Op::kIn == 2) y = ld<VB>(b1 + v * VB);
-                    st<VB>(bo + v * VB, apply<Op, VB>(op, x, y));
+                    const Vec<VB> z = apply<Op, VB>(op, x, y);
+                    if constexpr (MaySkipUnchanged<Op>::value) {
+                        if (a.skip_unchanged && same_bits<VB>(z, x)) continue;
+                    }
+                    st<VB>(bo + v * VB, z);
                 }
             }
         }

@@ -17,6 +17,7 @@ const StreamEntry kTable[OP_COUNT][5] = {
     {eb<OpSaxpyBF16>(0), eb<OpSaxpyBF16>(1), eb<OpSaxpyBF16>(2), eb<OpSaxpyBF16>(3), eb<OpSaxpyBF16>(4)},
     {eb<OpReluBF16>(0), eb<OpReluBF16>(1), eb<OpReluBF16>(2), eb<OpReluBF16>(3), eb<OpReluBF16>(4)},
     {kNoEntry, kNoEntry, kNoEntry, kNoEntry, kNoEntry},
+    {eb<OpAddReluBF16>(0), eb<OpAddReluBF16>(1), eb<OpAddReluBF16>(2), eb<OpAddReluBF16>(3), eb<OpAddReluBF16>(4)},
 };
 }  // namespace
 

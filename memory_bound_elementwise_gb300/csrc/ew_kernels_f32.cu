@@ -15,6 +15,7 @@ const StreamEntry kTable[OP_COUNT][5] = {
     {e32<OpSaxpyF32>(0), e32<OpSaxpyF32>(1), e32<OpSaxpyF32>(2), e32<OpSaxpyF32>(3), kNoEntry},
     {e32<OpReluF32>(0), e32<OpReluF32>(1), e32<OpReluF32>(2), e32<OpReluF32>(3), kNoEntry},
     {e32<OpCopy<4>>(0), e32<OpCopy<4>>(1), e32<OpCopy<4>>(2), e32<OpCopy<4>>(3), kNoEntry},
+    {e32<OpAddReluF32>(0), e32<OpAddReluF32>(1), e32<OpAddReluF32>(2), e32<OpAddReluF32>(3), kNoEntry},
 };
 
 constexpr int kGatherOneshotUnroll = 4;

@@ -168,6 +168,7 @@ const TmaEntry kTma[OP_COUNT][DT_COUNT] = {
     {tma_entry_of<OpSaxpyF32>(), tma_entry_of<OpSaxpyF16>(), tma_entry_of<OpSaxpyBF16>()},
     {tma_entry_of<OpReluF32>(), tma_entry_of<OpReluF16>(), tma_entry_of<OpReluBF16>()},
     {tma_entry_of<OpCopy<4>>(), tma_entry_of<OpCopy<2>>(), tma_entry_of<OpCopy<2>>()},
+    {tma_entry_of<OpAddReluF32>(), tma_entry_of<OpAddReluF16>(), tma_entry_of<OpAddReluBF16>()},
 };
 
 // Arms an mbarrier for 16 bytes that no copy will deliver: the bounded wait

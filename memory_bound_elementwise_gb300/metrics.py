@@ -10,6 +10,8 @@ Bytes are the ones the operation must move at least once, counted per element:
 * relu    y = max(x, 0)    read x, write y           -> 2
   (CUDA-MODE lecture notes §5.2 example 1, case A: 4 B read + 4 B written)
 * copy    out = in         read in, write out        -> 2
+* add_relu C = max(A + B, 0), fused: 3, against 3 + 2 for the two passes
+  (CUDA-MODE lecture notes §5.3, kernel fusion)
 * gather  out[i] = in[(s*i) mod n]: one element read and one written per
   output -> 2 (logical bytes; the sectors actually fetched are larger and are
   reported separately from the profiler).
@@ -21,6 +23,7 @@ ELEM_SIZE = {"f32": 4, "f16": 2, "bf16": 2}
 
 TRANSFERS_PER_ELEMENT = {
     "add": 3,
+    "add_relu": 3,
     "saxpy": 3,
     "relu": 2,
     "copy": 2,
@@ -38,5 +41,5 @@ def gbps(nbytes: float, seconds: float) -> float:
 
 def arithmetic_intensity(op: str, dtype: str) -> float:
     """FLOP (or compare) per algorithmic byte for one element."""
-    flops = {"add": 1, "saxpy": 2, "relu": 1, "copy": 0, "gather": 0}[op]
+    flops = {"add": 1, "add_relu": 2, "saxpy": 2, "relu": 1, "copy": 0, "gather": 0}[op]
     return flops / (TRANSFERS_PER_ELEMENT[op] * ELEM_SIZE[dtype])

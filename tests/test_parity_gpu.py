@@ -51,6 +51,8 @@ def run_op(op, dtype, bufs, n, alpha=2.5):
         st = L.ew_saxpy(dt, alpha, p[0], p[1], n, _stream())
     elif op == "relu":
         st = L.ew_relu(dt, p[0], p[1], n, _stream())
+    elif op == "add_relu":
+        st = L.ew_add_relu(dt, p[0], p[1], p[2], n, _stream())
     elif op == "copy":
         st = L.ew_copy(dt, p[0], p[1], n, _stream())
     else:
@@ -65,6 +67,8 @@ def expected(op, dtype, x, y, alpha=2.5):
         return oracle.saxpy(dtype, alpha, x, y)
     if op == "relu":
         return oracle.relu(dtype, x)
+    if op == "add_relu":  # the unfused definition: round the sum, then ReLU
+        return oracle.relu(dtype, oracle.add(dtype, x, y))
     return oracle.copy(x)
 
 
@@ -79,7 +83,7 @@ def make_inputs(dtype, n, seed, specials=True):
 
 def check_case(op, dtype, n, offs, seed, path="auto", schedule="auto"):
     x, y = make_inputs(dtype, n, seed)
-    nin = {"add": 2, "saxpy": 2, "relu": 1, "copy": 1}[op]
+    nin = {"add": 2, "add_relu": 2, "saxpy": 2, "relu": 1, "copy": 1}[op]
     if op == "saxpy":
         bx = GuardedBuffer(n, dtype, offs[0]).fill(x)
         by = GuardedBuffer(n, dtype, offs[1]).fill(y)
@@ -99,7 +103,7 @@ def check_case(op, dtype, n, offs, seed, path="auto", schedule="auto"):
     rec = ew.last_launch()
     torch.cuda.synchronize()
     want = expected(op, dtype, x, y)
-    assert_bits_equal(outb.host(), want, dtype, nan_as_class=op in ("add", "saxpy"),
+    assert_bits_equal(outb.host(), want, dtype, nan_as_class=op in ("add", "saxpy", "add_relu"),
                       what="%s %s n=%d offs=%s path=%s" % (op, dtype, n, offs, path))
     for b in bufs:
         assert b.guards_intact(), "guard zone written: %s %s n=%d offs=%s" % (op, dtype, n, offs)
@@ -107,23 +111,23 @@ def check_case(op, dtype, n, offs, seed, path="auto", schedule="auto"):
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
-@pytest.mark.parametrize("op", ["add", "saxpy", "relu", "copy"])
+@pytest.mark.parametrize("op", ["add", "saxpy", "relu", "copy", "add_relu"])
 def test_small_sizes_every_offset(op, dtype):
     per = 32 // ESIZE[dtype]
     for n in SMALL_N:
         for off in range(per):
-            nin = 3 if op == "add" else 2
+            nin = 3 if op in ("add", "add_relu") else 2
             check_case(op, dtype, n, [off] * nin, seed=1000 + n * 37 + off)
 
 
 @pytest.mark.parametrize("schedule", ["oneshot", "persistent"])
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("dtype", DTYPES)
-@pytest.mark.parametrize("op", ["add", "saxpy", "relu", "copy"])
+@pytest.mark.parametrize("op", ["add", "saxpy", "relu", "copy", "add_relu"])
 def test_forced_paths(op, dtype, path, schedule):
     for n in (1, 33, 1000, 70001, 600_001):
         for off in (0, 1, 3):
-            nin = 3 if op == "add" else 2
+            nin = 3 if op in ("add", "add_relu") else 2
             rec = check_case(op, dtype, n, [off] * nin, seed=2000 + n + off, path=path,
                              schedule=schedule)
             if path == "scalar":
@@ -137,7 +141,7 @@ def test_forced_paths(op, dtype, path, schedule):
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
-@pytest.mark.parametrize("op", ["add", "saxpy", "relu", "copy"])
+@pytest.mark.parametrize("op", ["add", "saxpy", "relu", "copy", "add_relu"])
 def test_tma_tile_boundaries(op, dtype):
     """Sizes around the 8 KiB bulk-copy tile and the 2-tile CTA, at offsets that
     keep or break 16-byte alignment (the latter falls back to vector loads)."""
@@ -146,7 +150,7 @@ def test_tma_tile_boundaries(op, dtype):
              3 * per_tile + 7, 5 * per_tile - 3, 70001]
     for n in sizes:
         for off in (0, 1, 16 // ESIZE[dtype], 3):
-            nin = 3 if op == "add" else 2
+            nin = 3 if op in ("add", "add_relu") else 2
             rec = check_case(op, dtype, n, [off] * nin, seed=2500 + n + off, path="tma")
             assert rec["path"] == 4
             assert rec["head"] + rec["nvec"] * per_tile + rec["tail"] == n
@@ -226,6 +230,27 @@ def test_in_place(dtype):
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
+def test_in_place_relu_skips_unchanged_vectors(dtype):
+    """In place, vectors ReLU leaves unchanged are not stored; results must be
+    the same as computing every element, including on a second pass where
+    nothing changes and on inputs that are mostly non-negative."""
+    n = 300_007
+    L = ew.lib()
+    x = inputs.as_dtype(inputs.normal(n, 4500), dtype)
+    mostly_pos = inputs.as_dtype(np.abs(inputs.normal(n, 4501)), dtype)
+    mostly_pos[::997] = inputs.as_dtype(np.float32([-1.0]), dtype)[0]  # a few negatives
+    for src in (x, mostly_pos):
+        for off in (0, 1, 3):
+            b = GuardedBuffer(n, dtype, off).fill(src)
+            want = oracle.relu(dtype, src)
+            for _ in range(2):
+                assert L.ew_relu(DT_CODE[dtype], b.view.data_ptr(), b.view.data_ptr(), n, _stream()) == 0
+                torch.cuda.synchronize()
+                assert_bits_equal(b.host(), want, dtype, False, "relu in place off=%d" % off)
+            assert b.guards_intact()
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
 def test_every_bit_pattern_add_relu(dtype):
     """All 16-bit patterns (or 2^20 random binary32 patterns) as inputs."""
     if dtype == "f32":
@@ -245,6 +270,10 @@ def test_every_bit_pattern_add_relu(dtype):
     run_op("relu", dtype, [bx, bo], n)
     torch.cuda.synchronize()
     assert_bits_equal(bo.host(), oracle.relu(dtype, x), dtype, False, "relu all patterns")
+    run_op("add_relu", dtype, [bx, by, bo], n)
+    torch.cuda.synchronize()
+    assert_bits_equal(bo.host(), oracle.relu(dtype, oracle.add(dtype, x, y)), dtype, True,
+                      "add_relu all patterns")
     by.fill(y)
     run_op("saxpy", dtype, [bx, by], n, alpha=-1.5)
     torch.cuda.synchronize()
@@ -404,6 +433,17 @@ def test_config_copy_and_gather_f32_2p26():
     torch.cuda.synchronize()
     assert_bits_equal(bo.host(), oracle.gather_stride(x, 2), "f32", False, "gather 2^26")
     assert bo.guards_intact() and bi.guards_intact()
+
+
+def test_add_relu_f32_2p26():
+    n = 1 << 26
+    a = inputs.normal(n, inputs.seed_for("add_f32"))
+    b = inputs.normal(n, inputs.seed_for("add_f32", 1))
+    ba, bb, bc = GuardedBuffer(n, "f32").fill(a), GuardedBuffer(n, "f32").fill(b), GuardedBuffer(n, "f32")
+    run_op("add_relu", "f32", [ba, bb, bc], n)
+    torch.cuda.synchronize()
+    assert_bits_equal(bc.host(), oracle.relu("f32", oracle.add("f32", a, b)), "f32", True, "add_relu 2^26")
+    assert bc.guards_intact()
 
 
 def test_config_add_f32_2p28():
