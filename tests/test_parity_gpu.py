@@ -280,6 +280,26 @@ def test_every_bit_pattern_add_relu(dtype):
     assert_bits_equal(by.host(), oracle.saxpy(dtype, -1.5, x, y), dtype, True, "saxpy all patterns")
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_add_16bit_every_pattern_against_4096_partners(dtype):
+    """2^28 operand pairs per 16-bit format: every bit pattern as A against
+    4096 seeded patterns as B (specials included), packed add on the GPU
+    against the oracle's correctly rounded sum."""
+    allp = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    partners = inputs.random_bits(4096, dtype, 8800)
+    partners[:inputs.SPECIAL_BITS[dtype].size] = inputs.SPECIAL_BITS[dtype]
+    x = np.tile(allp, partners.size)
+    y = np.repeat(partners, allp.size)
+    n = x.size
+    bx = GuardedBuffer(n, dtype).fill(x)
+    by = GuardedBuffer(n, dtype).fill(y)
+    bo = GuardedBuffer(n, dtype)
+    run_op("add", dtype, [bx, by, bo], n)
+    torch.cuda.synchronize()
+    assert_bits_equal(bo.host(), oracle.add(dtype, x, y), dtype, True, "add 2^28 pairs")
+    assert bo.guards_intact()
+
+
 @pytest.mark.parametrize("dtype", ["f32", "f16"])
 def test_gather_small(dtype):
     L = ew.lib()
