@@ -72,6 +72,8 @@ PROFILE_CASES = {
     "relu_f32": ("relu", "f32", 0),
     "copy_f32": ("copy", "f32", 0),
     "gather2_f32": ("gather", "f32", 0),
+    "add_relu_f32": ("add_relu", "f32", 0),
+    "relu_inplace_f32": ("relu_inplace", "f32", 0),
 }
 
 
@@ -94,7 +96,7 @@ def run_profile_case(args):
         raw[off * e: off * e + arr.size * e].copy_(torch.from_numpy(np.ascontiguousarray(arr).view(np.uint8)))
         return raw, raw.data_ptr() + off * e
 
-    x = inputs.as_dtype(inputs.uniform(n, inputs.seed_for("add_f32")), dtype)
+    x = inputs.as_dtype(inputs.normal(n, inputs.seed_for("add_f32")), dtype)
     rx, px = buf(x)
     ry, py = buf(inputs.as_dtype(inputs.uniform(n, inputs.seed_for("add_f32", 1)), dtype))
     rz, pz = buf(np.zeros_like(x))
@@ -105,7 +107,9 @@ def run_profile_case(args):
             "saxpy": lambda: L.ew_saxpy(code, 2.5, px, py, n, s),
             "relu": lambda: L.ew_relu(code, px, pz, n, s),
             "copy": lambda: L.ew_copy(code, px, pz, n, s),
-            "gather": lambda: L.ew_gather_stride(code, px, pz, n, 2, s)}[op]
+            "gather": lambda: L.ew_gather_stride(code, px, pz, n, 2, s),
+            "add_relu": lambda: L.ew_add_relu(code, px, py, pz, n, s),
+            "relu_inplace": lambda: L.ew_relu(code, px, px, n, s)}[op]
     for _ in range(args.warmup + args.steps):
         st = call()
         if st != 0:
