@@ -375,7 +375,11 @@ def aux_measurements(torch, ew, inputs, metrics, stream, peak, dev):
                                           "launch": ew.last_launch()}
     # in place again on the now non-negative data: nothing changes, so no vector
     # is stored (page's case B: 4 bytes per element, read only)
-    total, kern = time_launches(torch, stream, lambda: L.ew_relu(0, py, py, n28, s), 50, 3)
+    def relu_again():
+        st = L.ew_relu(0, py, py, n28, s)
+        if st != 0:
+            raise ew.EwError(st, "relu in place")
+    total, kern = time_launches(torch, stream, relu_again, 50, 3)
     nb = 4 * n28
     out["relu_f32_2p28_inplace_nonnegative"] = {
         "gbps": metrics.gbps(nb, kern), "frac": metrics.gbps(nb, kern) / peak, "kernel_ms": kern * 1e3,
@@ -409,8 +413,9 @@ def aux_measurements(torch, ew, inputs, metrics, stream, peak, dev):
     record("add_relu_f32_2p28_fused", "add_relu", "f32", n28, lambda: L.ew_add_relu(0, pa, pb, pc, n28, s))
 
     def unfused():
-        st = L.ew_add(0, pa, pb, pc, n28, s)
-        return st if st != 0 else L.ew_relu(0, pc, pc, n28, s)
+        for st in (L.ew_add(0, pa, pb, pc, n28, s), L.ew_relu(0, pc, pc, n28, s)):
+            if st != 0:
+                raise ew.EwError(st, "add then relu")
     total, kern = time_launches(torch, stream, unfused, 50, 3)
     nb = metrics.algorithmic_bytes("add_relu", "f32", n28)
     out["add_then_relu_f32_2p28_unfused"] = {

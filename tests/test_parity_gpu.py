@@ -498,3 +498,30 @@ def test_beyond_2p31_elements_f16():
     assert torch.equal(tc[full:], want[:n - full])
     del ta, tb, tc
     torch.cuda.empty_cache()
+
+
+def test_gather_beyond_2p32_elements_f16():
+    """n > 2^32 switches the gather to the grid-stride kernel (the one-shot
+    index needs s*i < 2^64): input is a seeded 2^20-element tile repeated on the
+    device; 200k sampled outputs and both ends are checked against the oracle's
+    index map and the tile."""
+    tile_n = 1 << 20
+    n = (1 << 32) + 5
+    s = 3
+    tile = inputs.random_bits(tile_n, "f16", 8200)
+    reps = -(-n // tile_n)
+    tin = torch.from_numpy(tile.view(np.int16)).cuda().repeat(reps)[:n].contiguous()
+    tout = torch.empty_like(tin)
+    assert ew.lib().ew_gather_stride(1, tin.data_ptr(), tout.data_ptr(), n, s, _stream()) == 0
+    rec = ew.last_launch()
+    assert rec["schedule"] == 2  # grid-stride kernel above 2^32 elements
+    torch.cuda.synchronize()
+    g = inputs.rng(8201)
+    idx = np.concatenate([np.arange(0, 1000), np.arange(n - 1000, n),
+                          g.integers(0, n, size=200_000, dtype=np.int64)])
+    got = tout[torch.from_numpy(idx).cuda()].cpu().numpy().view(np.uint16)
+    src = np.array([oracle.gather_index(int(i), s, n) for i in idx], dtype=np.int64)
+    want = tile[src % tile_n]
+    assert np.array_equal(got, want)
+    del tin, tout
+    torch.cuda.empty_cache()
