@@ -443,6 +443,12 @@ def aux_measurements(torch, ew, inputs, metrics, stream, peak, dev):
     g = metrics.gbps(2 * big.numel(), kern)
     out["memcpy_d2d_2GiB"] = {"gbps": g, "frac": g / peak, "kernel_ms": kern * 1e3,
                               "note": "library device-to-device copy (torch copy_), read+write bytes"}
+    for ent in out.values():  # against the copy ceiling measured in this run
+        ent["frac_of_d2d"] = ent["gbps"] / g
+    out["gather2_f32_2p26"]["sectors_per_request"] = {
+        "gather": 8.0, "contiguous_copy_32bit_lanes": 4.0,
+        "source": "ncu l1tex__average_t_sectors_per_request_pipe_lsu_mem_global_op_ld.ratio, "
+                  "profiles/gather2_f32_2p26.md"}
     return out
 
 

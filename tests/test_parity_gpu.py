@@ -204,6 +204,25 @@ def test_mixed_offsets_fall_back(dtype):
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
+def test_saxpy_special_alphas(dtype):
+    """alpha = +-0, +-inf, NaN, a subnormal, the largest binary32, 1/3: the
+    fused multiply-add must match the oracle for every input class."""
+    n = 4099
+    L = ew.lib()
+    alphas = [0.0, -0.0, float("inf"), float("-inf"), float("nan"),
+              float(np.float32(1e-40)), float(np.finfo(np.float32).max), float(np.float32(1 / 3))]
+    for k, alpha in enumerate(alphas):
+        x, y = make_inputs(dtype, n, 4600 + k)
+        bx = GuardedBuffer(n, dtype, 1).fill(x)
+        by = GuardedBuffer(n, dtype, 1).fill(y)
+        assert L.ew_saxpy(DT_CODE[dtype], alpha, bx.view.data_ptr(), by.view.data_ptr(), n, _stream()) == 0
+        torch.cuda.synchronize()
+        assert_bits_equal(by.host(), oracle.saxpy(dtype, alpha, x, y), dtype, True,
+                          "saxpy alpha=%r" % alpha)
+        assert by.guards_intact()
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
 def test_in_place(dtype):
     n = 70001
     x, y = make_inputs(dtype, n, 4000)
