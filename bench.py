@@ -18,8 +18,12 @@ A and B i.i.d. uniform[-1, 1) from a seeded generator.  A step is one call of
 * cpu_baseline  the CPU oracle, single-threaded, on the same inputs (rank 0,
               one GPU only); its output is also compared with the GPU's.
 * aux         the other measured workloads (bf16/fp16 add at 2^28 aligned and
-              offset by one element, SAXPY 32M, ReLU 2^28, copy and stride-2
-              gather at 2^26, fp32 add at 2^20+3): GB/s and fraction of peak.
+              offset by one element, SAXPY 32M, ReLU 2^28 out of place and in
+              place, fused add+ReLU against the unfused pair, copy and stride-2
+              gather at 2^26, fp32 add at 2^20+3, the headline through the
+              persistent schedule and the bulk-copy path, and the library
+              device-to-device copy): GB/s, fraction of the measured peak and
+              of the copy ceiling measured in the same run.
 
 ``--impl reference`` times the CPU oracle instead (the reference arm), on a
 bounded sample of the same workload per step.
