@@ -231,6 +231,22 @@ def host_cpu_model():
     return platform.machine()
 
 
+def device_facts(torch, dev):
+    """SM count, L2 size, driver and runtime versions of the measured GPU."""
+    props = torch.cuda.get_device_properties(dev)
+    facts = {"sms": props.multi_processor_count,
+             "l2_bytes": getattr(props, "L2_cache_size", None),
+             "cuda_runtime": torch.version.cuda}
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=driver_version", "--format=csv,noheader",
+                              "-i", str(dev.index or 0)], stdout=subprocess.PIPE,
+                             stderr=subprocess.DEVNULL, text=True, timeout=20)
+        facts["driver"] = out.stdout.strip() or None
+    except Exception:
+        facts["driver"] = None
+    return facts
+
+
 # ---------------------------------------------------------------- reference arm
 
 def run_reference(args):
@@ -305,8 +321,9 @@ def time_launches(torch, stream, fn, steps, warmup):
     end = t.event()
     torch.cuda.synchronize()
     total = start.elapsed_time(end) / 1e3
-    kern = sum(a.elapsed_time(b) for a, b in pairs) / 1e3 / steps
-    return total, kern
+    per = [a.elapsed_time(b) / 1e3 for a, b in pairs]
+    time_launches.last_per_launch = per
+    return total, sum(per) / steps
 
 
 def aux_measurements(torch, ew, inputs, metrics, stream, peak, dev):
@@ -331,6 +348,7 @@ def aux_measurements(torch, ew, inputs, metrics, stream, peak, dev):
         nbytes = metrics.algorithmic_bytes(op, dtype, n)
         out[name] = {"gbps": metrics.gbps(nbytes, kern), "frac": metrics.gbps(nbytes, kern) / peak,
                      "kernel_ms": kern * 1e3, "step_ms": total / steps * 1e3,
+                     "gelem_per_s": n / kern / 1e9,
                      "bytes_per_launch": nbytes, "launch": ew.last_launch()}
 
     n28 = 1 << 28
@@ -500,6 +518,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     clocks.mark("start")
     total, kern = time_launches(torch, stream, step, args.steps, 0)
+    per_launch = sorted(time_launches.last_per_launch)
     clocks.mark("stop")
     if world > 1:
         dist.barrier()
@@ -590,10 +609,14 @@ def run_ours(args):
                    "l2": "no flush: inputs larger than L2 (3.2 GB working set vs 129 MB L2)",
                    "path": ew.PATH_NAMES.get(rec["path"], rec["path"]), "vec_bytes": rec["vec_bytes"],
                    "grid": rec["grid"], "block": rec["block"],
-                   "gpu": torch.cuda.get_device_name(dev)},
+                   "gpu": torch.cuda.get_device_name(dev), **device_facts(torch, dev)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
-                     "traffic_note": traffic_note, "kernel_ms": kern * 1e3},
+                     "traffic_note": traffic_note, "kernel_ms": kern * 1e3,
+                     "kernel_ms_median": per_launch[len(per_launch) // 2] * 1e3,
+                     "kernel_ms_min": per_launch[0] * 1e3,
+                     "gelem_per_s": n / kern / 1e9,
+                     "frac_of_nominal_8tbs": achieved / 8000.0},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": 8 * n,
                 "d2h_bytes_per_step": 4 * n, "steps": e2e_steps, "result_matches_device": e2e_ok,
                 "how": "ew_add called on pinned host A, B, C: the kernel reads 8N bytes from and "
