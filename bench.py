@@ -483,10 +483,10 @@ def run_ours(args):
     from memory_bound_elementwise_gb300.shard import weak_scaling_range
 
     world, rank, local = dist_env()
-    if world > 1:
-        dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
     stream = torch.cuda.Stream(dev)
     ew.set_path(args.path)
     ew.set_schedule(args.schedule)
