@@ -1,6 +1,6 @@
 """Every pair of 16-bit operands through the GPU's packed add (2^32 pairs per
 format, 16 launches of 2^28), compared with the oracle bit for bit; NaN
-results compare as "both NaN".  Opt-in (EW_SLOW_TESTS=1): a few minutes.
+results compare as "both NaN".  About 35 s on a GB300 with a 16-core host.
 
 The oracle runs in a pool of worker processes started with "spawn" (never
 forked from a process that has touched the GPU).
@@ -15,7 +15,7 @@ import torch
 import memory_bound_elementwise_gb300 as ew
 from tests.gpu_util import is_nan_bits
 
-pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+pytestmark = pytest.mark.gpu
 
 CHUNKS = 16
 PER = (1 << 32) // CHUNKS          # pairs per launch
