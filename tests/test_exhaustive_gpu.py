@@ -1,6 +1,7 @@
-"""Every pair of 16-bit operands through the GPU's packed add (2^32 pairs per
-format, 16 launches of 2^28), compared with the oracle bit for bit; NaN
-results compare as "both NaN".  About 35 s on a GB300 with a 16-core host.
+"""Every pair of 16-bit operands through the GPU's packed add and its SAXPY
+(alpha = 2.5, the pages' coefficient): 2^32 pairs per format and operator, in
+16 launches of 2^28, compared with the oracle bit for bit; NaN results compare
+as "both NaN".  About 35 s per operator on a GB300 with a 16-core host.
 
 The oracle runs in a pool of worker processes started with "spawn" (never
 forked from a process that has touched the GPU).
@@ -22,18 +23,24 @@ PER = (1 << 32) // CHUNKS          # pairs per launch
 B_PER_CHUNK = PER >> 16           # 4096 distinct B patterns per launch
 
 
+ALPHA = 2.5
+
+
 def _oracle_slice(args):
-    dtype, b_lo, b_hi = args
+    op, dtype, b_lo, b_hi = args
     import oracle
     allp = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
     bvals = np.arange(b_lo, b_hi, dtype=np.uint32).astype(np.uint16)
     a = np.tile(allp, bvals.size)
     b = np.repeat(bvals, allp.size)
-    return oracle.add(dtype, a, b)
+    if op == "add":
+        return oracle.add(dtype, a, b)
+    return oracle.saxpy(dtype, ALPHA, a, b)  # x = every pattern, y = B
 
 
+@pytest.mark.parametrize("op", ["add", "saxpy"])
 @pytest.mark.parametrize("dtype,code", [("f16", 1), ("bf16", 2)])
-def test_add_all_operand_pairs(dtype, code):
+def test_all_operand_pairs(op, dtype, code):
     workers = min(16, os.cpu_count() or 4)
     ctx = mp.get_context("spawn")
     allp = torch.arange(1 << 16, dtype=torch.int32).to(torch.int16).cuda()
@@ -46,14 +53,18 @@ def test_add_all_operand_pairs(dtype, code):
             b_lo = chunk * B_PER_CHUNK
             bvals = torch.arange(b_lo, b_lo + B_PER_CHUNK, dtype=torch.int32).to(torch.int16).cuda()
             b = bvals.repeat_interleave(1 << 16)
-            assert L.ew_add(code, a.data_ptr(), b.data_ptr(), c.data_ptr(), PER, s) == 0
+            if op == "add":
+                assert L.ew_add(code, a.data_ptr(), b.data_ptr(), c.data_ptr(), PER, s) == 0
+            else:
+                c.copy_(b)
+                assert L.ew_saxpy(code, ALPHA, a.data_ptr(), c.data_ptr(), PER, s) == 0
             step = B_PER_CHUNK // workers
-            parts = pool.map(_oracle_slice, [(dtype, b_lo + k * step, b_lo + (k + 1) * step)
+            parts = pool.map(_oracle_slice, [(op, dtype, b_lo + k * step, b_lo + (k + 1) * step)
                                              for k in range(workers)])
             want = np.concatenate(parts)
             torch.cuda.synchronize()
             got = c.cpu().numpy().view(np.uint16)
             gn, wn = is_nan_bits(got, dtype), is_nan_bits(want, dtype)
             bad = np.nonzero((got != want) & ~(gn & wn))[0]
-            assert bad.size == 0, "%s chunk %d: %d mismatches, first pair index %d" % (
-                dtype, chunk, bad.size, int(bad[0]))
+            assert bad.size == 0, "%s %s chunk %d: %d mismatches, first pair index %d" % (
+                op, dtype, chunk, bad.size, int(bad[0]))
