@@ -49,6 +49,12 @@ import numpy as np  # noqa: E402
 
 METRIC = "achieved HBM GB/s (and % of GB300 peak) for fp32 add, N=2^28"
 N_HEADLINE = 1 << 28
+# The pages' own number for this metric and workload: fp32 add at 268.4M
+# elements, 1576.5 GB/s for the scalar kernel (Version 1), the best of their
+# table ("HyperAI elementwise add on RTX 5090", step 3: RTX 5090 results).
+# Another machine (RTX 5090, GDDR7): context for vs_baseline, not a target.
+PAGE_BASELINE = {"value": 1576.5, "unit": "GB/s", "hardware": "RTX 5090 (GDDR7)",
+                 "kernel": "V1 FP32 scalar add, N = 268.4M"}
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -279,7 +285,8 @@ def run_reference(args):
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": value / PAGE_BASELINE["value"],
+        "baseline": PAGE_BASELINE, "dtype": "f32",
         "data": "synthetic: A, B i.i.d. uniform[-1,1) binary32, seeded PCG64",
         "config": {"workload": "fp32 add C=A+B, N=2^28 per GPU", "n": args.n,
                    "l2": "CPU run (no GPU L2)"},
@@ -602,7 +609,8 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "scaling": "weak", "vs_baseline": value / PAGE_BASELINE["value"], "baseline": PAGE_BASELINE,
+        "dtype": "f32",
         "data": "synthetic: A, B i.i.d. uniform[-1,1) binary32, seeded PCG64 per rank",
         "config": {"workload": "fp32 add C=A+B, N=2^28 per GPU", "n": n, "slice": [lo, hi],
                    "bytes_per_step_per_gpu": step_bytes,
