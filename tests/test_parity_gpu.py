@@ -196,8 +196,9 @@ def test_gather_schedules_agree(dtype):
 
 @pytest.mark.parametrize("dtype", DTYPES)
 def test_mixed_offsets_fall_back(dtype):
-    for offs in ([1, 0, 3], [0, 2, 4], [4, 0, 8], [2, 6, 10], [0, 0, 1], [5, 5, 13]):
-        for n in (17, 1000, 4099):
+    for offs in ([1, 0, 3], [0, 2, 4], [4, 0, 8], [2, 6, 10], [0, 0, 1], [5, 5, 13],
+                 [0, 1, 0], [1, 1, 0], [1, 0, 0], [0, 1, 1]):
+        for n in (1, 2, 3, 4, 5, 6, 7, 17, 1000, 4099, 70001):
             check_case("add", dtype, n, offs, seed=3000 + n + sum(offs))
             check_case("saxpy", dtype, n, offs[:2], seed=3100 + n + sum(offs))
             check_case("relu", dtype, n, offs[:2], seed=3200 + n + sum(offs))
