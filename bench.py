@@ -378,6 +378,17 @@ def aux_measurements(torch, ew, inputs, metrics, stream, peak, dev):
     record("saxpy_f32_32M_inplace", "saxpy", "f32", n32m,
            lambda: L.ew_saxpy(0, 2.5, px, py, n32m, s), steps=200)
     del rx, ry
+    # SAXPY at larger N, where the fixed cost of a launch is amortised
+    x = inputs.normal(n28, inputs.seed_for("saxpy_f32", 2))
+    y = inputs.normal(n28, inputs.seed_for("saxpy_f32", 3))
+    rx, px = dev_of(x, "f32")
+    ry, py = dev_of(y, "f32")
+    del x, y
+    for lg in (26, 28):
+        m = 1 << lg
+        record("saxpy_f32_2p%d_inplace" % lg, "saxpy", "f32", m,
+               lambda: L.ew_saxpy(0, 2.5, px, py, m, s), steps=100 if lg == 26 else 50)
+    del rx, ry
     x = inputs.normal(n28, inputs.seed_for("relu_f32"))
     inputs.inject_signed_zeros(x)
     rx, px = dev_of(x, "f32")
