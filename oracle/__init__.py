@@ -38,6 +38,7 @@ def lib():
         L.orc_relu_f32.argtypes = [_F32P, _F32P, _I64]
         for name in ("orc_relu_f16", "orc_relu_bf16"):
             getattr(L, name).argtypes = [_U16P, _U16P, _I64]
+        L.orc_select_even_odd_i32.argtypes = [ctypes.c_void_p, ctypes.c_void_p, _I64]
         L.orc_copy.argtypes = [ctypes.c_void_p, ctypes.c_void_p, _I64, _I64]
         L.orc_gather_stride.argtypes = [ctypes.c_void_p, ctypes.c_void_p, _I64, _I64, _I64]
         L.orc_gather_index.argtypes = [_I64, _I64, _I64]
@@ -107,6 +108,16 @@ def relu_inplace(dtype, x):
     x = _arr(x, dtype)
     getattr(lib(), "orc_relu_" + dtype)(_ptr(x, dtype), _ptr(x, dtype), x.size)
     return x
+
+
+def select_even_odd(x):
+    """y = x even ? 2x : x + 1 on int32, wrapping modulo 2^32."""
+    x = np.ascontiguousarray(x)
+    if x.dtype != np.int32:
+        raise TypeError("select_even_odd expects int32, got %s" % x.dtype)
+    y = np.empty_like(x)
+    lib().orc_select_even_odd_i32(x.ctypes.data, y.ctypes.data, x.size)
+    return y
 
 
 def copy(x):

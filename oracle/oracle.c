@@ -28,6 +28,9 @@
  *   gather  out[i] = in[(s*i) mod n]      CUDA-MODE lecture notes, §3.2
  *                                          non-coalesced (s = 2 on the page)
  *   ceil_div(n, t) = (n + t - 1) / t      "逐元素操作算子" §二, launch configuration
+ *   select  y[i] = x[i] even ? 2 x[i] : x[i] + 1 on 32-bit integers
+ *                                          CUDA-MODE lecture notes, §6.1-6.2
+ *                                          (control-divergence example)
  *
  * Readings where the pages are silent (each one is listed with its reason in
  * the design notes):
@@ -38,6 +41,8 @@
  *     fmaf is taken there and the result is rounded once to the 16-bit type.
  *     alpha is a binary32 value and is never rounded to the 16-bit type.
  *   - the gather index s*i is formed without overflow (128-bit product).
+ *   - select works on two's complement 32-bit integers ("x % 2 == 0" on the
+ *     page); 2x and x + 1 wrap modulo 2^32 instead of overflowing.
  *
  * Build: cc -O2 -std=c11 -fPIC -shared -ffp-contract=off -fno-fast-math
  * (see oracle/build.py).  No OpenMP, no intrinsics, no architecture flags.
@@ -246,5 +251,21 @@ ORC_API void orc_gather_stride(const void *in, void *out, int64_t n, int64_t s,
     for (int64_t i = 0; i < n; ++i) {
         int64_t j = orc_gather_index(i, s, n);
         memcpy(dst + i * elem_size, src + j * elem_size, (size_t)elem_size);
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* y = x even ? 2x : x + 1  (32-bit integers, wrapping)                 */
+/* ------------------------------------------------------------------ */
+
+ORC_API void orc_select_even_odd_i32(const int32_t *x, int32_t *y, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        uint32_t u = (uint32_t)x[i];
+        if (x[i] % 2 == 0) {
+            y[i] = (int32_t)(u * 2u);
+        } else {
+            y[i] = (int32_t)(u + 1u);
+        }
     }
 }

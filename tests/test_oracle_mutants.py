@@ -41,6 +41,8 @@ MUTANTS = [
     ("gather_wrong_modulus", "return (int64_t)(p % (uint64_t)n);",
      "return (int64_t)(p % (uint64_t)(n > 2 ? n - 1 : n));", "gather"),
     ("ceil_div_floor", "return (n + t - 1) / t;", "return n / t;", "ceil_div"),
+    ("select_swapped_branches", "if (x[i] % 2 == 0) {\n            y[i] = (int32_t)(u * 2u);",
+     "if (x[i] % 2 != 0) {\n            y[i] = (int32_t)(u * 2u);", "select"),
 ]
 
 

@@ -384,3 +384,27 @@ def test_gather_index_no_overflow():
     for i, s, n in ((big, 3, (1 << 61) - 1), ((1 << 63) - 1, (1 << 63) - 1, 1000003),
                     (5, 2, 7), (0, 9, 1)):
         assert oracle.gather_index(i, s, n) == (i * s) % n
+
+
+# ---------------------------------------------------------------- select
+
+
+def test_select_even_odd_closed_forms_and_wrap():
+    x = np.array([0, 1, 2, 3, -1, -2, -3, 7, 2 ** 31 - 1, -2 ** 31, 2 ** 30, 2 ** 30 + 1],
+                 dtype=np.int32)
+    want = [0, 2, 4, 4, 0, -4, -2, 8, -2 ** 31, 0, -2 ** 31, 2 ** 30 + 2]
+    assert oracle.select_even_odd(x).tolist() == want
+
+
+def test_select_even_odd_brute_force():
+    g = inputs.rng(1234)
+    x = g.integers(-2 ** 31, 2 ** 31, size=100_000, dtype=np.int64).astype(np.int32)
+    got = oracle.select_even_odd(x)
+    for v, r in zip(x[:20000].tolist(), got[:20000].tolist()):
+        w = (2 * v) if v % 2 == 0 else (v + 1)
+        w = (w + 2 ** 31) % 2 ** 32 - 2 ** 31  # two's complement wrap
+        assert r == w
+    # parity: even inputs give even results that are twice the input (mod 2^32)
+    even = (x % 2 == 0)
+    assert np.array_equal(got[even].astype(np.int64) % 2, np.zeros(int(even.sum()), np.int64))
+    assert np.array_equal(got[~even], (x[~even].astype(np.int64) + 1).astype(np.int32))
