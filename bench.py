@@ -433,6 +433,15 @@ def aux_measurements(torch, ew, inputs, metrics, stream, peak, dev):
     record("gather2_f32_2p26", "gather", "f32", n26,
            lambda: L.ew_gather_stride(0, px, py, n26, 2, s), steps=100)
     del rx, ry
+    # the branch-free even/odd select on int32 (CUDA-MODE lecture notes §6)
+    xi = inputs.rng(inputs.seed_for("copy_f32", 7)).integers(-2 ** 31, 2 ** 31, size=n28,
+                                                             dtype=np.int64).astype(np.int32)
+    rx, px = dev_of(xi.view(np.float32), "f32")
+    ry, py = dev_of(np.zeros(n28, np.float32), "f32")
+    del xi
+    record("select_even_odd_i32_2p28", "select", "i32", n28,
+           lambda: L.ew_select_even_odd(3, px, py, n28, s))
+    del rx, ry
     n1 = (1 << 20) + 3
     a = inputs.uniform(n1, inputs.seed_for("add_f32_small"))
     b = inputs.uniform(n1, inputs.seed_for("add_f32_small", 1))

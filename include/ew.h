@@ -79,14 +79,16 @@ typedef struct CUstream_st *ew_stream_t;
 typedef enum {
     EW_F32 = 0,  /* IEEE binary32 */
     EW_F16 = 1,  /* IEEE binary16 */
-    EW_BF16 = 2  /* bfloat16 (upper half of binary32) */
+    EW_BF16 = 2, /* bfloat16 (upper half of binary32) */
+    EW_I32 = 3   /* 32-bit two's complement integer: ew_select_even_odd, ew_copy and
+                    ew_gather_stride only (others return EW_ERR_UNSUPPORTED_DTYPE) */
 } ew_dtype;
 
 typedef enum {
     EW_OK = 0,
     EW_ERR_INVALID_VALUE = 1,     /* n < 0, stride <= 0, misaligned pointer, bad enum */
     EW_ERR_NULL_POINTER = 2,      /* a NULL pointer with n > 0 */
-    EW_ERR_UNSUPPORTED_DTYPE = 3, /* dtype outside ew_dtype */
+    EW_ERR_UNSUPPORTED_DTYPE = 3, /* dtype outside ew_dtype, or not one the operation takes */
     EW_ERR_OVERLAP = 4,           /* partial overlap between an input and the output */
     EW_ERR_NOT_DEVICE_POINTER = 5,/* pointer check enabled and a pointer is not device-accessible */
     EW_ERR_CUDA = 6,              /* CUDA runtime error; see ew_last_cuda_error */
@@ -139,6 +141,13 @@ EW_API ew_status ew_relu(ew_dtype dtype, const void *x, void *y, int64_t n, ew_s
  * aliasing as in ew_add. */
 EW_API ew_status ew_add_relu(ew_dtype dtype, const void *a, const void *b, void *c, int64_t n,
                              ew_stream_t stream);
+
+/* y = x even ? 2x : x + 1, on EW_I32 only, wrapping modulo 2^32: the
+ * control-divergence example of CUDA-MODE lecture notes §6.1-6.2 (an if/else
+ * on x % 2 and its branch-free rewrite compute the same thing), computed
+ * without a branch.  x: n inputs; y: n outputs (y == x computes in place). */
+EW_API ew_status ew_select_even_odd(ew_dtype dtype, const void *x, void *y, int64_t n,
+                                    ew_stream_t stream);
 
 /* out = in.  in == out is a no-op that launches nothing. */
 EW_API ew_status ew_copy(ew_dtype dtype, const void *in, void *out, int64_t n, ew_stream_t stream);

@@ -11,11 +11,13 @@ Tensor entry points (same names as the C ABI)::
     ew_saxpy(alpha, x, y)           y = alpha*x + y, in place
     ew_relu(x, y=None)              y = max(x, 0)  (y = x for in place)
     ew_add_relu(a, b, c=None)       C = max(A + B, 0), one pass
+    ew_select_even_odd(x, y=None)   y = x even ? 2x : x + 1 (int32)
     ew_copy(x, out)                 out = x
     ew_gather_stride(x, out, s)     out[i] = x[(s*i) mod n]
 
 Tensors must be contiguous CUDA tensors of dtype float32, float16 or bfloat16
-on the current device; calls are enqueued on ``stream`` (default: torch's
+(int32 for ew_select_even_odd, ew_copy and ew_gather_stride) on the current
+device; calls are enqueued on ``stream`` (default: torch's
 current stream) and do not synchronise.  ``lib()`` exposes the raw ctypes
 handle with the exact C signatures.
 """
@@ -26,7 +28,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libew.so")
 
 # ew_dtype
-EW_F32, EW_F16, EW_BF16 = 0, 1, 2
+EW_F32, EW_F16, EW_BF16, EW_I32 = 0, 1, 2, 3
 # ew_path
 PATH_AUTO, PATH_SCALAR, PATH_V128, PATH_V256, PATH_TMA = 0, 1, 2, 3, 4
 PATH_NAMES = {PATH_AUTO: "auto", PATH_SCALAR: "scalar", PATH_V128: "v128",
@@ -41,8 +43,8 @@ STATUS_NAMES = {0: "EW_OK", 1: "EW_ERR_INVALID_VALUE", 2: "EW_ERR_NULL_POINTER",
                 5: "EW_ERR_NOT_DEVICE_POINTER", 6: "EW_ERR_CUDA", 7: "EW_ERR_TIMEOUT"}
 
 # Every function declared in include/ew.h.
-EXPORTS = ("ew_add", "ew_saxpy", "ew_relu", "ew_add_relu", "ew_copy", "ew_gather_stride",
-           "ew_set_path",
+EXPORTS = ("ew_add", "ew_saxpy", "ew_relu", "ew_add_relu", "ew_select_even_odd", "ew_copy",
+           "ew_gather_stride", "ew_set_path",
            "ew_get_path", "ew_set_schedule", "ew_get_schedule", "ew_set_pointer_check",
            "ew_plan_query", "ew_last_launch", "ew_status_string", "ew_last_cuda_error",
            "ew_device_error", "ew_selftest_bounded_wait", "ew_version")
@@ -90,9 +92,11 @@ def lib():
     L.ew_saxpy.argtypes = [ctypes.c_int, f32, vp, vp, i64, vp]
     L.ew_relu.argtypes = [ctypes.c_int, vp, vp, i64, vp]
     L.ew_add_relu.argtypes = [ctypes.c_int, vp, vp, vp, i64, vp]
+    L.ew_select_even_odd.argtypes = [ctypes.c_int, vp, vp, i64, vp]
     L.ew_copy.argtypes = [ctypes.c_int, vp, vp, i64, vp]
     L.ew_gather_stride.argtypes = [ctypes.c_int, vp, vp, i64, i64, vp]
-    for name in ("ew_add", "ew_saxpy", "ew_relu", "ew_add_relu", "ew_copy", "ew_gather_stride",
+    for name in ("ew_add", "ew_saxpy", "ew_relu", "ew_add_relu", "ew_select_even_odd", "ew_copy",
+                 "ew_gather_stride",
                  "ew_set_path", "ew_set_schedule", "ew_set_pointer_check", "ew_plan_query",
                  "ew_last_launch", "ew_device_error", "ew_selftest_bounded_wait"):
         getattr(L, name).restype = ctypes.c_int
@@ -130,9 +134,10 @@ def check(status, where):
 
 def _dtype_code(t):
     import torch
-    codes = {torch.float32: EW_F32, torch.float16: EW_F16, torch.bfloat16: EW_BF16}
+    codes = {torch.float32: EW_F32, torch.float16: EW_F16, torch.bfloat16: EW_BF16,
+             torch.int32: EW_I32}
     if t.dtype not in codes:
-        raise TypeError("unsupported dtype %s (float32, float16, bfloat16)" % t.dtype)
+        raise TypeError("unsupported dtype %s (float32, float16, bfloat16, int32)" % t.dtype)
     return codes[t.dtype]
 
 
@@ -193,6 +198,17 @@ def ew_add_relu(a, b, c=None, stream=None):
     check(lib().ew_add_relu(dt, a.data_ptr(), b.data_ptr(), c.data_ptr(), n,
                             _stream(stream, a.device)), "ew_add_relu")
     return c
+
+
+def ew_select_even_odd(x, y=None, stream=None):
+    """y = x even ? 2x : x + 1 on int32 tensors (wrapping); y = x computes in place."""
+    import torch
+    if y is None:
+        y = torch.empty_like(x)
+    dt, n = _check_tensors(x, y)
+    check(lib().ew_select_even_odd(dt, x.data_ptr(), y.data_ptr(), n, _stream(stream, x.device)),
+          "ew_select_even_odd")
+    return y
 
 
 def ew_copy(x, out, stream=None):
@@ -266,6 +282,6 @@ def device_error(stream=None):
     return st, code.value
 
 
-__all__ = ["ew_add", "ew_saxpy", "ew_relu", "ew_add_relu", "ew_copy", "ew_gather_stride", "set_path",
+__all__ = ["ew_add", "ew_saxpy", "ew_relu", "ew_add_relu", "ew_select_even_odd", "ew_copy", "ew_gather_stride", "set_path",
            "get_path", "set_schedule", "get_schedule", "set_pointer_check", "plan_query",
            "last_launch", "device_error", "selftest_bounded_wait", "lib", "EwError", "EXPORTS"]

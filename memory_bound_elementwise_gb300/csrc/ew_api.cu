@@ -37,8 +37,11 @@ std::atomic<int> g_pointer_check{-1};  // -1: not yet read from the environment
 thread_local int t_last_cuda_error = 0;
 thread_local ew_launch_record t_last{};
 
-int elem_size(ew_dtype dt) { return dt == EW_F32 ? 4 : 2; }
-bool dtype_ok(int dt) { return dt == EW_F32 || dt == EW_F16 || dt == EW_BF16; }
+int elem_size(ew_dtype dt) { return (dt == EW_F32 || dt == EW_I32) ? 4 : 2; }
+bool dtype_ok(int dt) { return dt == EW_F32 || dt == EW_F16 || dt == EW_BF16 || dt == EW_I32; }
+bool float_dtype(ew_dtype dt) { return dt == EW_F32 || dt == EW_F16 || dt == EW_BF16; }
+// the kernel tables are per element size: int32 shares the 4-byte table
+int table_dtype(ew_dtype dt) { return dt == EW_I32 ? DT_F32 : static_cast<int>(dt); }
 
 ew_status cuda_fail(cudaError_t e) {
     t_last_cuda_error = static_cast<int>(e);
@@ -176,13 +179,13 @@ int clamp_grid(int64_t blocks) {
 
 // ---------------------------------------------------------------- dispatch
 
-const StreamEntry *table_for(int dt) {
-    return dt == EW_F32 ? stream_table_f32() : dt == EW_F16 ? stream_table_f16() : stream_table_bf16();
+const StreamEntry *table_for(int tdt) {
+    return tdt == DT_F32 ? stream_table_f32() : tdt == DT_F16 ? stream_table_f16() : stream_table_bf16();
 }
 
 ew_status run_tma(int op, ew_dtype dt, const void *in0, const void *in1, void *out, int64_t n,
                   float alpha, const ew_plan &pl16, cudaStream_t s) {
-    const TmaEntry *ent = tma_entry(op, dt);
+    const TmaEntry *ent = tma_entry(op, table_dtype(dt));
     const int e = elem_size(dt);
     const TmaPlan tp = make_tma_plan(pl16, e, n);
     TmaArgs a{in0, in1, out, n, tp.head, tp.ntiles, tp.rem0, alpha, kWaitLimitNs};
@@ -221,14 +224,14 @@ ew_status run_stream(int op, ew_dtype dt, const void *in0, const void *in1, void
     cudaError_t ce = device_info(&dev, &sms);
     if (ce != cudaSuccess) return cuda_fail(ce);
 
-    if (path == EW_PATH_TMA && pl.vec_bytes >= 16 && tma_entry(op, dt) != nullptr)
+    if (path == EW_PATH_TMA && pl.vec_bytes >= 16 && tma_entry(op, table_dtype(dt)) != nullptr)
         return run_tma(op, dt, in0, in1, out, n, alpha, make_plan(EW_PATH_V128, e, up, np, n), s);
 
     StreamArgs a{in0, in1, out, n, pl.head, pl.nvec, pl.head + pl.nvec * (pl.vec_bytes / e), alpha,
                  skip_unchanged ? 1 : 0};
 
     // copy of 16-bit elements is one kernel for both 16-bit formats
-    const int tdt = (op == OP_COPY && dt == EW_BF16) ? EW_F16 : dt;
+    const int tdt = (op == OP_COPY && dt == EW_BF16) ? DT_F16 : table_dtype(dt);
     const StreamEntry &ent = table_for(tdt)[op * 5 + vec_index(pl.vec_bytes)];
     if (ent.launch == nullptr) return EW_ERR_INVALID_VALUE;
 
@@ -287,6 +290,7 @@ extern "C" {
 
 ew_status ew_add(ew_dtype dt, const void *a, const void *b, void *c, int64_t n, ew_stream_t s) {
     t_last = ew_launch_record{};
+    if (!float_dtype(dt)) return EW_ERR_UNSUPPORTED_DTYPE;
     const void *p[3] = {a, b, c};
     ew_status st = check_common(dt, n, p, 3);
     if (st != EW_OK || n == 0) return st;
@@ -298,6 +302,7 @@ ew_status ew_add(ew_dtype dt, const void *a, const void *b, void *c, int64_t n, 
 
 ew_status ew_saxpy(ew_dtype dt, float alpha, const void *x, void *y, int64_t n, ew_stream_t s) {
     t_last = ew_launch_record{};
+    if (!float_dtype(dt)) return EW_ERR_UNSUPPORTED_DTYPE;
     const void *p[2] = {x, y};
     ew_status st = check_common(dt, n, p, 2);
     if (st != EW_OK || n == 0) return st;
@@ -307,6 +312,7 @@ ew_status ew_saxpy(ew_dtype dt, float alpha, const void *x, void *y, int64_t n, 
 
 ew_status ew_relu(ew_dtype dt, const void *x, void *y, int64_t n, ew_stream_t s) {
     t_last = ew_launch_record{};
+    if (!float_dtype(dt)) return EW_ERR_UNSUPPORTED_DTYPE;
     const void *p[2] = {x, y};
     ew_status st = check_common(dt, n, p, 2);
     if (st != EW_OK || n == 0) return st;
@@ -317,6 +323,7 @@ ew_status ew_relu(ew_dtype dt, const void *x, void *y, int64_t n, ew_stream_t s)
 
 ew_status ew_add_relu(ew_dtype dt, const void *a, const void *b, void *c, int64_t n, ew_stream_t s) {
     t_last = ew_launch_record{};
+    if (!float_dtype(dt)) return EW_ERR_UNSUPPORTED_DTYPE;
     const void *p[3] = {a, b, c};
     ew_status st = check_common(dt, n, p, 3);
     if (st != EW_OK || n == 0) return st;
@@ -324,6 +331,16 @@ ew_status ew_add_relu(ew_dtype dt, const void *a, const void *b, void *c, int64_
     if ((st = check_alias(a, c, bytes)) != EW_OK) return st;
     if ((st = check_alias(b, c, bytes)) != EW_OK) return st;
     return run_stream(OP_ADD_RELU, dt, a, b, c, n, 0.0f, reinterpret_cast<cudaStream_t>(s));
+}
+
+ew_status ew_select_even_odd(ew_dtype dt, const void *x, void *y, int64_t n, ew_stream_t s) {
+    t_last = ew_launch_record{};
+    if (dt != EW_I32) return EW_ERR_UNSUPPORTED_DTYPE;
+    const void *p[2] = {x, y};
+    ew_status st = check_common(dt, n, p, 2);
+    if (st != EW_OK || n == 0) return st;
+    if ((st = check_alias(x, y, n * elem_size(dt))) != EW_OK) return st;
+    return run_stream(OP_SELECT, dt, x, nullptr, y, n, 0.0f, reinterpret_cast<cudaStream_t>(s));
 }
 
 ew_status ew_copy(ew_dtype dt, const void *in, void *out, int64_t n, ew_stream_t s) {
@@ -358,14 +375,15 @@ ew_status ew_gather_stride(ew_dtype dt, const void *in, void *out, int64_t n, in
     GatherArgs ga{in, out, un, s_mod, 0, 0};
     const GatherEntry *g;
     int grid;
+    const bool four = elem_size(dt) == 4;
     if (oneshot) {
-        g = (dt == EW_F32) ? gather_oneshot_4() : gather_oneshot_2();
+        g = four ? gather_oneshot_4() : gather_oneshot_2();
         const int64_t per_block = static_cast<int64_t>(kBlock) * g->unroll;
         grid = clamp_grid((n + per_block - 1) / per_block);
         ga.step_mod = (s_mod * static_cast<uint64_t>(kBlock)) % un;  // s_mod < 2^32
         ga.barrett_m = ~uint64_t(0) / un;
     } else {
-        g = (dt == EW_F32) ? gather_stride_4() : gather_stride_2();
+        g = four ? gather_stride_4() : gather_stride_2();
         int occ = 1;
         ce = blocks_per_sm(dev, g->kernel, kBlock, 0, &occ);
         if (ce != cudaSuccess) return cuda_fail(ce);
@@ -446,7 +464,7 @@ const char *ew_status_string(ew_status st) {
         case EW_OK: return "EW_OK";
         case EW_ERR_INVALID_VALUE: return "EW_ERR_INVALID_VALUE: bad size, stride, alignment or enum";
         case EW_ERR_NULL_POINTER: return "EW_ERR_NULL_POINTER: null pointer with n > 0";
-        case EW_ERR_UNSUPPORTED_DTYPE: return "EW_ERR_UNSUPPORTED_DTYPE: dtype is not f32, f16 or bf16";
+        case EW_ERR_UNSUPPORTED_DTYPE: return "EW_ERR_UNSUPPORTED_DTYPE: dtype not supported by this operation";
         case EW_ERR_OVERLAP: return "EW_ERR_OVERLAP: output partially overlaps an input";
         case EW_ERR_NOT_DEVICE_POINTER: return "EW_ERR_NOT_DEVICE_POINTER: pointer not accessible by the device";
         case EW_ERR_CUDA: return "EW_ERR_CUDA: CUDA runtime error (see ew_last_cuda_error)";
@@ -475,6 +493,6 @@ ew_status ew_selftest_bounded_wait(int64_t limit_ns, ew_stream_t s) {
     return EW_OK;
 }
 
-int ew_version(void) { return 300; }
+int ew_version(void) { return 400; }
 
 }  // extern "C"

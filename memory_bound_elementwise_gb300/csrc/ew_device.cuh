@@ -266,6 +266,19 @@ struct OpAddReluBF16 {
     }
 };
 
+// Even/odd select on 32-bit two's complement integers: y = x even ? 2x : x + 1
+// (CUDA-MODE lecture notes §6: the divergent if/else and its branch-free
+// rewrite compute the same thing).  Written without a branch: x + (odd ? 1 : x),
+// wrapping modulo 2^32.
+struct OpSelectEvenOddI32 {
+    static constexpr int kIn = 1, kElem = 4;
+    __device__ __forceinline__ uint32_t word(uint32_t x, uint32_t) const {
+        const uint32_t odd = x & 1u;
+        return x + (odd ? 1u : x);
+    }
+    __device__ __forceinline__ uint16_t half(uint16_t, uint16_t) const { return 0; }
+};
+
 template <int E>
 struct OpCopy {
     static constexpr int kIn = 1, kElem = E;

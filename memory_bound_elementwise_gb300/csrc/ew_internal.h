@@ -10,8 +10,12 @@ namespace ew {
 constexpr int kBlock = 256;  // threads per block for the LSU kernels
 
 // Operator ids of the streaming (contiguous) kernels.
-enum OpId : int { OP_ADD = 0, OP_SAXPY = 1, OP_RELU = 2, OP_COPY = 3, OP_ADD_RELU = 4, OP_COUNT = 5 };
-// dtype ids match ew_dtype.
+enum OpId : int {
+    OP_ADD = 0, OP_SAXPY = 1, OP_RELU = 2, OP_COPY = 3, OP_ADD_RELU = 4, OP_SELECT = 5, OP_COUNT = 6
+};
+// Element-size classes of the kernel tables: the 4-byte table serves binary32
+// and int32, the 16-bit tables binary16 and bfloat16 (ids match ew_dtype for
+// the floating-point types).
 enum DtId : int { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2, DT_COUNT = 3 };
 
 // Vector widths in bytes, indexed 0..4 -> 32, 16, 8, 4, 2.

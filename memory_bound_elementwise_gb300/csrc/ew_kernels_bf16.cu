@@ -18,6 +18,7 @@ const StreamEntry kTable[OP_COUNT][5] = {
     {eb<OpReluBF16>(0), eb<OpReluBF16>(1), eb<OpReluBF16>(2), eb<OpReluBF16>(3), eb<OpReluBF16>(4)},
     {kNoEntry, kNoEntry, kNoEntry, kNoEntry, kNoEntry},
     {eb<OpAddReluBF16>(0), eb<OpAddReluBF16>(1), eb<OpAddReluBF16>(2), eb<OpAddReluBF16>(3), eb<OpAddReluBF16>(4)},
+    {kNoEntry, kNoEntry, kNoEntry, kNoEntry, kNoEntry},
 };
 }  // namespace
 

@@ -18,6 +18,7 @@ const StreamEntry kTable[OP_COUNT][5] = {
     {e16<OpReluF16>(0), e16<OpReluF16>(1), e16<OpReluF16>(2), e16<OpReluF16>(3), e16<OpReluF16>(4)},
     {e16<OpCopy<2>>(0), e16<OpCopy<2>>(1), e16<OpCopy<2>>(2), e16<OpCopy<2>>(3), e16<OpCopy<2>>(4)},
     {e16<OpAddReluF16>(0), e16<OpAddReluF16>(1), e16<OpAddReluF16>(2), e16<OpAddReluF16>(3), e16<OpAddReluF16>(4)},
+    {kNoEntry, kNoEntry, kNoEntry, kNoEntry, kNoEntry},
 };
 
 constexpr int kGatherOneshotUnroll = 4;

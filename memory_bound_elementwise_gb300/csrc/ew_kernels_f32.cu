@@ -1,5 +1,6 @@
-// ew_kernels_f32.cu -- binary32 instantiations of the streaming kernels and
-// the 4-byte strided gather.
+// ew_kernels_f32.cu -- 4-byte instantiations of the streaming kernels
+// (binary32 operators, the int32 even/odd select, 4-byte copy) and the 4-byte
+// strided gather.
 #include "ew_kernels.cuh"
 
 namespace ew {
@@ -16,6 +17,8 @@ const StreamEntry kTable[OP_COUNT][5] = {
     {e32<OpReluF32>(0), e32<OpReluF32>(1), e32<OpReluF32>(2), e32<OpReluF32>(3), kNoEntry},
     {e32<OpCopy<4>>(0), e32<OpCopy<4>>(1), e32<OpCopy<4>>(2), e32<OpCopy<4>>(3), kNoEntry},
     {e32<OpAddReluF32>(0), e32<OpAddReluF32>(1), e32<OpAddReluF32>(2), e32<OpAddReluF32>(3), kNoEntry},
+    {e32<OpSelectEvenOddI32>(0), e32<OpSelectEvenOddI32>(1), e32<OpSelectEvenOddI32>(2),
+     e32<OpSelectEvenOddI32>(3), kNoEntry},
 };
 
 constexpr int kGatherOneshotUnroll = 4;

@@ -169,6 +169,7 @@ const TmaEntry kTma[OP_COUNT][DT_COUNT] = {
     {tma_entry_of<OpReluF32>(), tma_entry_of<OpReluF16>(), tma_entry_of<OpReluBF16>()},
     {tma_entry_of<OpCopy<4>>(), tma_entry_of<OpCopy<2>>(), tma_entry_of<OpCopy<2>>()},
     {tma_entry_of<OpAddReluF32>(), tma_entry_of<OpAddReluF16>(), tma_entry_of<OpAddReluBF16>()},
+    {tma_entry_of<OpSelectEvenOddI32>(), TmaEntry{nullptr, nullptr, 0}, TmaEntry{nullptr, nullptr, 0}},
 };
 
 // Arms an mbarrier for 16 bytes that no copy will deliver: the bounded wait
@@ -187,7 +188,8 @@ __global__ void wait_selftest_kernel(uint64_t limit_ns) {
 
 const TmaEntry *tma_entry(int op, int dtype) {
     if (op < 0 || op >= OP_COUNT || dtype < 0 || dtype >= DT_COUNT) return nullptr;
-    return &kTma[op][dtype];
+    const TmaEntry *e = &kTma[op][dtype];
+    return e->launch != nullptr ? e : nullptr;
 }
 
 cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t s) {

@@ -12,6 +12,7 @@ Bytes are the ones the operation must move at least once, counted per element:
 * copy    out = in         read in, write out        -> 2
 * add_relu C = max(A + B, 0), fused: 3, against 3 + 2 for the two passes
   (CUDA-MODE lecture notes §5.3, kernel fusion)
+* select  y = x even ? 2x : x + 1 on int32 -> 2 (CUDA-MODE lecture notes §6)
 * gather  out[i] = in[(s*i) mod n]: one element read and one written per
   output -> 2 (logical bytes; the sectors actually fetched are larger and are
   reported separately from the profiler).
@@ -19,7 +20,7 @@ Bytes are the ones the operation must move at least once, counted per element:
 GB/s is decimal (10^9 bytes per second), as in the pages' benchmark script.
 """
 
-ELEM_SIZE = {"f32": 4, "f16": 2, "bf16": 2}
+ELEM_SIZE = {"f32": 4, "f16": 2, "bf16": 2, "i32": 4}
 
 TRANSFERS_PER_ELEMENT = {
     "add": 3,
@@ -28,6 +29,7 @@ TRANSFERS_PER_ELEMENT = {
     "relu": 2,
     "copy": 2,
     "gather": 2,
+    "select": 2,
 }
 
 
@@ -41,5 +43,5 @@ def gbps(nbytes: float, seconds: float) -> float:
 
 def arithmetic_intensity(op: str, dtype: str) -> float:
     """FLOP (or compare) per algorithmic byte for one element."""
-    flops = {"add": 1, "add_relu": 2, "saxpy": 2, "relu": 1, "copy": 0, "gather": 0}[op]
+    flops = {"add": 1, "add_relu": 2, "saxpy": 2, "relu": 1, "copy": 0, "gather": 0, "select": 2}[op]
     return flops / (TRANSFERS_PER_ELEMENT[op] * ELEM_SIZE[dtype])

@@ -3,10 +3,10 @@ bit-level comparison against the oracle."""
 import numpy as np
 import torch
 
-TORCH_DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
-BITS_NP = {"f32": np.uint32, "f16": np.uint16, "bf16": np.uint16}
-BITS_T = {"f32": torch.int32, "f16": torch.int16, "bf16": torch.int16}
-ESIZE = {"f32": 4, "f16": 2, "bf16": 2}
+TORCH_DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16, "i32": torch.int32}
+BITS_NP = {"f32": np.uint32, "f16": np.uint16, "bf16": np.uint16, "i32": np.uint32}
+BITS_T = {"f32": torch.int32, "f16": torch.int16, "bf16": torch.int16, "i32": torch.int32}
+ESIZE = {"f32": 4, "f16": 2, "bf16": 2, "i32": 4}
 GUARD_BYTES = 4096
 SENTINEL = 0x5A
 
@@ -30,8 +30,8 @@ class GuardedBuffer:
         return self
 
     def host(self):
-        return self.raw[self.lo:self.lo + self.n * ESIZE[self.dtype]].cpu().numpy().view(
-            np.float32 if self.dtype == "f32" else np.uint16)
+        host_dt = {"f32": np.float32, "i32": np.int32}.get(self.dtype, np.uint16)
+        return self.raw[self.lo:self.lo + self.n * ESIZE[self.dtype]].cpu().numpy().view(host_dt)
 
     def guards_intact(self):
         head = self.raw[:self.lo]

@@ -545,3 +545,62 @@ def test_gather_beyond_2p32_elements_f16():
     assert np.array_equal(got, want)
     del tin, tout
     torch.cuda.empty_cache()
+
+
+def _random_i32(n, seed):
+    g = inputs.rng(seed)
+    x = g.integers(-2 ** 31, 2 ** 31, size=n, dtype=np.int64).astype(np.int32)
+    if n:
+        x[: min(n, 6)] = np.array([0, 1, -1, 2 ** 31 - 1, -2 ** 31, 2 ** 30], dtype=np.int32)[: min(n, 6)]
+    return x
+
+
+@pytest.mark.parametrize("schedule", ["oneshot", "persistent"])
+@pytest.mark.parametrize("path", PATHS)
+def test_select_even_odd_i32(path, schedule):
+    """y = x even ? 2x : x + 1 on int32 at every width, offset, ragged size and
+    schedule, out of place and in place."""
+    L = ew.lib()
+    ew.set_path(path)
+    ew.set_schedule(schedule)
+    for n in (1, 5, 8, 9, 33, 1000, 4099, 70001, 600_001):
+        for off in (0, 1, 3):
+            x = _random_i32(n, 9300 + n + off)
+            want = oracle.select_even_odd(x)
+            bx = GuardedBuffer(n, "i32", off).fill(x)
+            by = GuardedBuffer(n, "i32", off)
+            assert L.ew_select_even_odd(3, bx.view.data_ptr(), by.view.data_ptr(), n, _stream()) == 0
+            torch.cuda.synchronize()
+            assert np.array_equal(by.host(), want), (path, schedule, n, off)
+            assert L.ew_select_even_odd(3, bx.view.data_ptr(), bx.view.data_ptr(), n, _stream()) == 0
+            torch.cuda.synchronize()
+            assert np.array_equal(bx.host(), want), ("in place", path, schedule, n, off)
+            assert bx.guards_intact() and by.guards_intact()
+
+
+def test_select_even_odd_i32_2p28_and_int32_copy_gather():
+    n = 1 << 28
+    x = _random_i32(n, 9400)
+    bx = GuardedBuffer(n, "i32").fill(x)
+    by = GuardedBuffer(n, "i32")
+    L = ew.lib()
+    assert L.ew_select_even_odd(3, bx.view.data_ptr(), by.view.data_ptr(), n, _stream()) == 0
+    torch.cuda.synchronize()
+    assert np.array_equal(by.host(), oracle.select_even_odd(x))
+    m = 1 << 22
+    assert L.ew_copy(3, bx.view.data_ptr(), by.view.data_ptr(), m, _stream()) == 0
+    torch.cuda.synchronize()
+    assert np.array_equal(by.host()[:m], x[:m])
+    assert L.ew_gather_stride(3, bx.view.data_ptr(), by.view.data_ptr(), m, 2, _stream()) == 0
+    torch.cuda.synchronize()
+    assert np.array_equal(by.host()[:m], oracle.gather_stride(x[:m], 2))
+    assert by.guards_intact()
+
+
+def test_binding_select_even_odd():
+    x = torch.from_numpy(_random_i32(10_001, 9500)).cuda()
+    y = ew.ew_select_even_odd(x)
+    torch.cuda.synchronize()
+    assert np.array_equal(y.cpu().numpy(), oracle.select_even_odd(x.cpu().numpy()))
+    with pytest.raises(ew.EwError):
+        ew.ew_select_even_odd(x.float())
