@@ -432,6 +432,10 @@ def aux_measurements(torch, ew, inputs, metrics, stream, peak, dev):
     record("copy_f32_2p26", "copy", "f32", n26, lambda: L.ew_copy(0, px, py, n26, s), steps=200)
     record("gather2_f32_2p26", "gather", "f32", n26,
            lambda: L.ew_gather_stride(0, px, py, n26, 2, s), steps=100)
+    ew.set_path("v256")  # span variant: contiguous 256-bit source spans, lane select
+    record("gather2_f32_2p26_span", "gather", "f32", n26,
+           lambda: L.ew_gather_stride(0, px, py, n26, 2, s), steps=100)
+    ew.set_path("auto")
     del rx, ry
     # the branch-free even/odd select on int32 (CUDA-MODE lecture notes §6)
     xi = inputs.rng(inputs.seed_for("copy_f32", 7)).integers(-2 ** 31, 2 ** 31, size=n28,

@@ -156,7 +156,11 @@ EW_API ew_status ew_copy(ew_dtype dtype, const void *in, void *out, int64_t n, e
  * without overflow.  stride >= 1 (else EW_ERR_INVALID_VALUE).  in and out must
  * not overlap.  As in the page's non-coalesced copy, each thread reads one
  * element per access, so a warp's load touches every stride-th element of a
- * span while its store covers consecutive elements. */
+ * span while its store covers consecutive elements.  With ew_set_path
+ * (EW_PATH_V256) selected, 4-byte elements with (stride mod n) of 2 or 4 and
+ * n <= 2^32 use a span variant instead: each thread loads the contiguous
+ * source span of 8 outputs with 256-bit loads and keeps every stride-th word
+ * (same DRAM sectors, an eighth of the load instructions). */
 EW_API ew_status ew_gather_stride(ew_dtype dtype, const void *in, void *out, int64_t n,
                            int64_t stride, ew_stream_t stream);
 

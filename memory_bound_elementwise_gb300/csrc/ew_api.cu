@@ -371,8 +371,32 @@ ew_status ew_gather_stride(ew_dtype dt, const void *in, void *out, int64_t n, in
     const uint64_t un = static_cast<uint64_t>(n);
     const uint64_t s_mod = static_cast<uint64_t>(stride) % un;
     const int sched = resolved_schedule();
+    // span variant (EW_PATH_V256 only): 4-byte elements, stride 2 or 4, n <= 2^32
+    if (resolved_path() == EW_PATH_V256 && g_path.load(std::memory_order_relaxed) != EW_PATH_AUTO &&
+        elem_size(dt) == 4 && (s_mod == 2 || s_mod == 4) && un <= (uint64_t(1) << 32)) {
+        const GatherEntry *g = gather_span_4(static_cast<int64_t>(s_mod));
+        GatherArgs ga{in, out, un, s_mod, 0, ~uint64_t(0) / un, 0, 0, 0};
+        const uintptr_t o = reinterpret_cast<uintptr_t>(out);
+        ga.head = std::min<int64_t>(static_cast<int64_t>(((32 - o % 32) % 32) / 4), n);
+        ga.nvec = (n - ga.head) / 8;
+        ga.tail0 = ga.head + 8 * ga.nvec;
+        const int64_t per_block = static_cast<int64_t>(kBlock) * g->unroll;
+        const int grid = clamp_grid((ga.nvec + per_block - 1) / per_block);
+        ce = g->launch(ga, grid, reinterpret_cast<cudaStream_t>(s));
+        if (ce != cudaSuccess) return cuda_fail(ce);
+        t_last.launches = 1;
+        t_last.path = EW_PATH_V256;
+        t_last.vec_bytes = 32;
+        t_last.grid = grid;
+        t_last.block = kBlock;
+        t_last.schedule = EW_SCHED_ONESHOT;
+        t_last.head = ga.head;
+        t_last.nvec = ga.nvec;
+        t_last.tail = n - ga.tail0;
+        return EW_OK;
+    }
     const bool oneshot = sched == EW_SCHED_ONESHOT && un <= (uint64_t(1) << 32);
-    GatherArgs ga{in, out, un, s_mod, 0, 0};
+    GatherArgs ga{in, out, un, s_mod, 0, 0, 0, 0, 0};
     const GatherEntry *g;
     int grid;
     const bool four = elem_size(dt) == 4;

@@ -58,7 +58,10 @@ struct GatherArgs {
     uint64_t n;
     uint64_t s_mod;      // stride mod n
     uint64_t step_mod;   // one-shot: (stride * kBlock) mod n; grid-stride: (stride * grid threads) mod n
-    uint64_t barrett_m;  // floor((2^64 - 1) / n), one-shot kernel only
+    uint64_t barrett_m;  // floor((2^64 - 1) / n), one-shot and span kernels
+    int64_t head;        // span kernel: outputs [0, head) one by one (32-byte output alignment)
+    int64_t nvec;        // span kernel: 8-element output vectors after the head
+    int64_t tail0;       // span kernel: outputs [tail0, n) one by one
 };
 using GatherLaunchFn = cudaError_t (*)(const GatherArgs &, int grid, cudaStream_t);
 struct GatherEntry {
@@ -70,6 +73,9 @@ const GatherEntry *gather_oneshot_4();  // binary32, n <= 2^32
 const GatherEntry *gather_stride_4();   // binary32, any n
 const GatherEntry *gather_oneshot_2();  // 16-bit types
 const GatherEntry *gather_stride_2();
+// 4-byte elements, stride 2 or 4 (n <= 2^32): contiguous 256-bit span loads
+// and a lane select; nullptr for other strides.
+const GatherEntry *gather_span_4(int64_t stride);
 
 // Bulk-copy (cp.async.bulk) staging variant of the streaming kernels: each
 // CTA moves kTmaStages tiles of kTmaTile bytes per input through shared memory.

@@ -182,6 +182,75 @@ __global__ void __launch_bounds__(kBlock) gather_stride_kernel(const GatherArgs 
     }
 }
 
+// Span gather for a small stride S (2 or 4) on 4-byte elements.  A thread
+// owns 8 consecutive outputs i0..i0+7 (one 32-byte store); their sources
+// (S*i0 + S*k) mod n lie in the contiguous span j0 .. j0 + 8S - 1 unless the
+// span wraps past n.  When it does not wrap and starts 32-byte aligned, the
+// thread loads the span with S 256-bit loads and keeps every S-th word (the
+// same DRAM sectors as one load per output, an eighth of the load
+// instructions); otherwise it falls back to one load per output.
+template <int S, int U>
+__global__ void __launch_bounds__(kBlock) gather_span_kernel(const GatherArgs g) {
+    const char *in = static_cast<const char *>(g.in);
+    char *out = static_cast<char *>(g.out);
+    const uint64_t n = g.n;
+    if (blockIdx.x == 0) {  // outputs before 32-byte alignment and after the last vector
+        const uint64_t t = threadIdx.x;
+        if (t < static_cast<uint64_t>(g.head)) {
+            const uint64_t x = g.s_mod * t;
+            uint64_t j = x - __umul64hi(x, g.barrett_m) * n;
+            j = (j >= n) ? j - n : j;
+            j = (j >= n) ? j - n : j;
+            st<4>(out + t * 4, ld<4>(in + j * 4));
+        }
+        if (t < n - static_cast<uint64_t>(g.tail0)) {
+            const uint64_t i = static_cast<uint64_t>(g.tail0) + t;
+            const uint64_t x = g.s_mod * i;
+            uint64_t j = x - __umul64hi(x, g.barrett_m) * n;
+            j = (j >= n) ? j - n : j;
+            j = (j >= n) ? j - n : j;
+            st<4>(out + i * 4, ld<4>(in + j * 4));
+        }
+    }
+    constexpr int64_t kChunk = static_cast<int64_t>(kBlock) * U;  // vectors per chunk
+    const int64_t nchunks = (g.nvec + kChunk - 1) / kChunk;
+    for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t v = c * kChunk + threadIdx.x + u * kBlock;
+            if (v >= g.nvec) continue;
+            const uint64_t i0 = static_cast<uint64_t>(g.head) + 8u * static_cast<uint64_t>(v);
+            const uint64_t x = g.s_mod * i0;  // s_mod = S < n <= 2^32
+            uint64_t j0 = x - __umul64hi(x, g.barrett_m) * n;
+            j0 = (j0 >= n) ? j0 - n : j0;
+            j0 = (j0 >= n) ? j0 - n : j0;
+            Vec<32> r;
+            const char *src = in + j0 * 4;
+            if (j0 + 8u * S <= n && (reinterpret_cast<uintptr_t>(src) & 31u) == 0) {
+                Vec<32> span[S];
+#pragma unroll
+                for (int q = 0; q < S; ++q) span[q] = ld<32>(src + q * 32);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) r.w[k] = span[(k * S) / 8].w[(k * S) % 8];
+            } else {
+                uint64_t j = j0;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    r.w[k] = ld<4>(in + j * 4).w[0];
+                    j = addmod_u64(j, static_cast<uint64_t>(S), n);
+                }
+            }
+            st<32>(out + i0 * 4, r);
+        }
+    }
+}
+
+template <int S, int U>
+cudaError_t launch_gather_span(const GatherArgs &g, int grid, cudaStream_t s) {
+    gather_span_kernel<S, U><<<grid, kBlock, 0, s>>>(g);
+    return cudaGetLastError();
+}
+
 template <int E, int U>
 cudaError_t launch_gather_oneshot(const GatherArgs &g, int grid, cudaStream_t s) {
     gather_oneshot_kernel<E, U><<<grid, kBlock, 0, s>>>(g);

@@ -31,6 +31,15 @@ const GatherEntry kGatherStride{reinterpret_cast<const void *>(&gather_stride_ke
 
 const StreamEntry *stream_table_f32() { return &kTable[0][0]; }
 
+constexpr int kGatherSpanUnroll = 2;
+static const GatherEntry kGatherSpan2{reinterpret_cast<const void *>(&gather_span_kernel<2, kGatherSpanUnroll>),
+                               &launch_gather_span<2, kGatherSpanUnroll>, kGatherSpanUnroll};
+static const GatherEntry kGatherSpan4{reinterpret_cast<const void *>(&gather_span_kernel<4, kGatherSpanUnroll>),
+                               &launch_gather_span<4, kGatherSpanUnroll>, kGatherSpanUnroll};
+
+const GatherEntry *gather_span_4(int64_t stride) {
+    return stride == 2 ? &kGatherSpan2 : stride == 4 ? &kGatherSpan4 : nullptr;
+}
 const GatherEntry *gather_oneshot_4() { return &kGatherOneshot; }
 const GatherEntry *gather_stride_4() { return &kGatherStride; }
 

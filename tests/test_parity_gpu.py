@@ -23,7 +23,7 @@ pytestmark = pytest.mark.gpu
 DTYPES = ["f32", "f16", "bf16"]
 PATHS = ["auto", "scalar", "v128", "v256", "tma"]
 SMALL_N = [1, 2, 3, 5, 7, 8, 9, 15, 16, 17, 31, 32, 33, 64, 255, 257, 1000, 4099, 70001]
-DT_CODE = {"f32": 0, "f16": 1, "bf16": 2}
+DT_CODE = {"f32": 0, "f16": 1, "bf16": 2, "i32": 3}
 
 
 @pytest.fixture(autouse=True)
@@ -604,3 +604,28 @@ def test_binding_select_even_odd():
     assert np.array_equal(y.cpu().numpy(), oracle.select_even_odd(x.cpu().numpy()))
     with pytest.raises(ew.EwError):
         ew.ew_select_even_odd(x.float())
+
+
+@pytest.mark.parametrize("dtype", ["f32", "i32"])
+def test_gather_span_variant(dtype):
+    """ew_set_path(v256): strides 2 and 4 load contiguous source spans and
+    select every stride-th word; other strides keep one load per output.
+    Sizes with and without wrap-around, input and output offsets that keep or
+    break the 32-byte span alignment."""
+    L = ew.lib()
+    code = DT_CODE.get(dtype, 3)
+    ew.set_path("v256")
+    for n in (3, 5, 9, 17, 64, 1000, 4096, 4099, 65536, 300_001, 1 << 22):
+        x = inputs.random_bits(n, "f32", 9600 + n)
+        for s in (2, 4, 3, n + 2):
+            for in_off, out_off in ((0, 0), (1, 0), (0, 3), (2, 5)):
+                bi = GuardedBuffer(n, dtype, in_off).fill(x)
+                bo = GuardedBuffer(n, dtype, out_off)
+                assert L.ew_gather_stride(code, bi.view.data_ptr(), bo.view.data_ptr(), n, s, _stream()) == 0
+                rec = ew.last_launch()
+                span = (s % n) in (2, 4)
+                assert rec["path"] == (3 if span else 1), (n, s, rec)
+                torch.cuda.synchronize()
+                assert_bits_equal(bo.host(), oracle.gather_stride(x, s), "f32", False,
+                                  "span gather n=%d s=%d offs=%d,%d" % (n, s, in_off, out_off))
+                assert bi.guards_intact() and bo.guards_intact()
