@@ -84,6 +84,8 @@ PROFILE_CASES = {
     "gather2_f32": ("gather", "f32", 0),
     "add_relu_f32": ("add_relu", "f32", 0),
     "relu_inplace_f32": ("relu_inplace", "f32", 0),
+    "select_i32": ("select", "f32", 0),
+    "gather2_span_f32": ("gather_span", "f32", 0),
 }
 
 
@@ -119,7 +121,11 @@ def run_profile_case(args):
             "copy": lambda: L.ew_copy(code, px, pz, n, s),
             "gather": lambda: L.ew_gather_stride(code, px, pz, n, 2, s),
             "add_relu": lambda: L.ew_add_relu(code, px, py, pz, n, s),
-            "relu_inplace": lambda: L.ew_relu(code, px, px, n, s)}[op]
+            "relu_inplace": lambda: L.ew_relu(code, px, px, n, s),
+            "select": lambda: L.ew_select_even_odd(3, px, pz, n, s),
+            "gather_span": lambda: L.ew_gather_stride(code, px, pz, n, 2, s)}[op]
+    if op == "gather_span":
+        ew.set_path("v256")
     for _ in range(args.warmup + args.steps):
         st = call()
         if st != 0:
