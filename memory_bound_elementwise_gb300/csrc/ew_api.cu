@@ -205,8 +205,7 @@ ew_status run_tma(int op, ew_dtype dt, const void *in0, const void *in1, void *o
     return EW_OK;
 }
 
-// Common path of the streaming operators (add, saxpy, relu, add_relu,
-// select, copy) once their arguments are valid.
+// Common path of add / saxpy / relu / copy once arguments are valid.
 ew_status run_stream(int op, ew_dtype dt, const void *in0, const void *in1, void *out,
                      int64_t n, float alpha, cudaStream_t s, bool skip_unchanged = false) {
     const int e = elem_size(dt);
