@@ -490,6 +490,34 @@ def aux_measurements(torch, ew, inputs, metrics, stream, peak, dev):
     record("copy_f32_2p26_tma", "copy", "f32", n26, lambda: L.ew_copy(0, pa, pb, n26, s), steps=200)
     ew.set_path("auto")
     del ra, rb, rc
+    # chains of short calls, launched back to back without events in between:
+    # programmatic dependent launch on (the default) against off
+    for lg in (20, 23, 25):
+        m = 1 << lg
+        cx = torch.zeros(m, device=dev)
+        cy = torch.zeros(m, device=dev)
+        px2, py2 = cx.data_ptr(), cy.data_ptr()
+        for prog in (True, False):
+            ew.set_programmatic_launch(prog)
+            for _ in range(10):
+                L.ew_saxpy(0, 0.5, px2, py2, m, s)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(200):
+                st = L.ew_saxpy(0, 0.5, px2, py2, m, s)
+                if st != 0:
+                    raise ew.EwError(st, "saxpy chain")
+            e1.record(stream)
+            torch.cuda.synchronize()
+            per = e0.elapsed_time(e1) / 1e3 / 200
+            nb = metrics.algorithmic_bytes("saxpy", "f32", m)
+            out["saxpy_chain_f32_2p%d_%s" % (lg, "pdl" if prog else "plain")] = {
+                "gbps": metrics.gbps(nb, per), "frac": metrics.gbps(nb, per) / peak,
+                "kernel_ms": per * 1e3, "bytes_per_launch": nb,
+                "note": "200 launches back to back, time per launch from one event pair"}
+        ew.set_programmatic_launch(True)
+        del cx, cy
     # device-to-device copy ceiling of this GPU (cudaMemcpyAsync via torch copy_, 2 GiB,
     # read + write bytes), timed on the same stream
     big = torch.empty(1 << 31, dtype=torch.uint8, device=dev)

@@ -49,7 +49,8 @@
  *              accepts no overlap at all.
  *   Streams    every call enqueues at most one kernel on `stream` (NULL = the
  *              legacy default stream) on the calling thread's current device and
- *              returns without synchronising.  Device faults surface at the
+ *              returns without synchronising.  Kernels are launched with
+ *              programmatic dependent launch unless ew_set_programmatic_launch(0).  Device faults surface at the
  *              caller's next synchronisation.
  *   Errors     every call returns an ew_status and never prints or aborts.
  *              Argument errors are detected on the host before any CUDA call.
@@ -178,6 +179,16 @@ EW_API ew_path ew_get_path(void);
  * always runs one-shot. */
 EW_API ew_status ew_set_schedule(ew_schedule schedule);
 EW_API ew_schedule ew_get_schedule(void);
+
+/* Programmatic dependent launch, enabled (1) by default; 0 disables it.  When
+ * enabled, kernels are launched with programmatic stream serialisation: a
+ * call's blocks may be scheduled while the previous kernel on the stream is
+ * still finishing, and wait (griddepcontrol.wait) for it to complete and its
+ * writes to be visible before touching memory.  Results and memory order
+ * between calls are the same either way; chains of short calls run faster.
+ * Process-wide.  EW_ERR_INVALID_VALUE for other values. */
+EW_API ew_status ew_set_programmatic_launch(int enable);
+EW_API int ew_get_programmatic_launch(void);
 
 /* Enable (1) or disable (0, the default) a cudaPointerGetAttributes check of
  * every pointer before launch: device, managed and page-locked host memory

@@ -44,7 +44,8 @@ STATUS_NAMES = {0: "EW_OK", 1: "EW_ERR_INVALID_VALUE", 2: "EW_ERR_NULL_POINTER",
 
 # Every function declared in include/ew.h.
 EXPORTS = ("ew_add", "ew_saxpy", "ew_relu", "ew_add_relu", "ew_select_even_odd", "ew_copy",
-           "ew_gather_stride", "ew_set_path",
+           "ew_gather_stride", "ew_set_path", "ew_set_programmatic_launch",
+           "ew_get_programmatic_launch",
            "ew_get_path", "ew_set_schedule", "ew_get_schedule", "ew_set_pointer_check",
            "ew_plan_query", "ew_last_launch", "ew_status_string", "ew_last_cuda_error",
            "ew_device_error", "ew_selftest_bounded_wait", "ew_version")
@@ -108,6 +109,10 @@ def lib():
     L.ew_get_schedule.restype = ctypes.c_int
     L.ew_selftest_bounded_wait.argtypes = [i64, vp]
     L.ew_set_pointer_check.argtypes = [ctypes.c_int]
+    L.ew_set_programmatic_launch.argtypes = [ctypes.c_int]
+    L.ew_set_programmatic_launch.restype = ctypes.c_int
+    L.ew_get_programmatic_launch.argtypes = []
+    L.ew_get_programmatic_launch.restype = ctypes.c_int
     L.ew_plan_query.argtypes = [ctypes.c_int, ctypes.POINTER(vp), i32, i64, ctypes.POINTER(Plan)]
     L.ew_last_launch.argtypes = [ctypes.POINTER(LaunchRecord)]
     L.ew_status_string.argtypes = [ctypes.c_int]
@@ -249,6 +254,15 @@ def get_schedule():
     return SCHED_NAMES[lib().ew_get_schedule()]
 
 
+def set_programmatic_launch(enable):
+    """Programmatic dependent launch on (default) or off."""
+    check(lib().ew_set_programmatic_launch(1 if enable else 0), "ew_set_programmatic_launch")
+
+
+def get_programmatic_launch():
+    return bool(lib().ew_get_programmatic_launch())
+
+
 def set_pointer_check(enable):
     check(lib().ew_set_pointer_check(1 if enable else 0), "ew_set_pointer_check")
 
@@ -283,5 +297,6 @@ def device_error(stream=None):
 
 
 __all__ = ["ew_add", "ew_saxpy", "ew_relu", "ew_add_relu", "ew_select_even_odd", "ew_copy", "ew_gather_stride", "set_path",
-           "get_path", "set_schedule", "get_schedule", "set_pointer_check", "plan_query",
+           "get_path", "set_schedule", "get_schedule", "set_programmatic_launch",
+           "get_programmatic_launch", "set_pointer_check", "plan_query",
            "last_launch", "device_error", "selftest_bounded_wait", "lib", "EwError", "EXPORTS"]

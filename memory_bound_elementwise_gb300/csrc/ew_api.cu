@@ -33,6 +33,7 @@ namespace {
 std::atomic<int> g_path{EW_PATH_AUTO};
 std::atomic<int> g_schedule{EW_SCHED_AUTO};
 std::atomic<int> g_pointer_check{-1};  // -1: not yet read from the environment
+std::atomic<int> g_programmatic{1};
 
 thread_local int t_last_cuda_error = 0;
 thread_local ew_launch_record t_last{};
@@ -284,6 +285,8 @@ ew_status check_alias(const void *in, const void *out, int64_t bytes) {
 
 }  // namespace
 
+bool ew::programmatic_launch() { return g_programmatic.load(std::memory_order_relaxed) != 0; }
+
 // ---------------------------------------------------------------- C ABI
 
 extern "C" {
@@ -448,6 +451,14 @@ ew_schedule ew_get_schedule(void) {
     return static_cast<ew_schedule>(g_schedule.load(std::memory_order_relaxed));
 }
 
+ew_status ew_set_programmatic_launch(int enable) {
+    if (enable != 0 && enable != 1) return EW_ERR_INVALID_VALUE;
+    g_programmatic.store(enable, std::memory_order_relaxed);
+    return EW_OK;
+}
+
+int ew_get_programmatic_launch(void) { return g_programmatic.load(std::memory_order_relaxed); }
+
 ew_status ew_set_pointer_check(int enable) {
     if (enable != 0 && enable != 1) return EW_ERR_INVALID_VALUE;
     g_pointer_check.store(enable, std::memory_order_relaxed);
@@ -517,6 +528,6 @@ ew_status ew_selftest_bounded_wait(int64_t limit_ns, ew_stream_t s) {
     return EW_OK;
 }
 
-int ew_version(void) { return 400; }
+int ew_version(void) { return 500; }
 
 }  // extern "C"

@@ -14,6 +14,18 @@
 
 namespace ew {
 
+// ---------------------------------------------------------------- launches
+//
+// First statements of every kernel: wait until the grid before this one on
+// the stream has completed and its writes are visible (a no-op when there is
+// none or when launched without programmatic serialisation), then allow the
+// grid after this one to be scheduled.
+
+__device__ __forceinline__ void enter_grid() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- vectors
 
 template <int VB> struct Vec;

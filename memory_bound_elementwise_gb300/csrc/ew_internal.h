@@ -9,6 +9,33 @@ namespace ew {
 
 constexpr int kBlock = 256;  // threads per block for the LSU kernels
 
+// Programmatic dependent launch: when enabled (the default), every kernel is
+// launched with programmatic stream serialisation, starts by waiting for the
+// grid before it on the stream to complete and flush (griddepcontrol.wait),
+// and at once lets the grid after it be scheduled (launch_dependents).  The
+// next call's blocks then take SM slots while this call's last blocks drain;
+// memory order between calls is unchanged.
+bool programmatic_launch();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                          cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    if (programmatic_launch()) {
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 // Operator ids of the streaming (contiguous) kernels.
 enum OpId : int {
     OP_ADD = 0, OP_SAXPY = 1, OP_RELU = 2, OP_COPY = 3, OP_ADD_RELU = 4, OP_SELECT = 5, OP_COUNT = 6

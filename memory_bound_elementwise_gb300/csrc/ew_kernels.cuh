@@ -30,6 +30,7 @@ template <> __device__ __forceinline__ OpSaxpyBF16 make_op<OpSaxpyBF16>(float a)
 
 template <class Op, int VB, int U>
 __global__ void __launch_bounds__(kBlock) stream_kernel(const StreamArgs a) {
+    enter_grid();
     const Op op = make_op<Op>(a.alpha);
     constexpr int E = Op::kElem;
     constexpr int64_t kChunk = static_cast<int64_t>(kBlock) * U;  // vectors per chunk
@@ -89,8 +90,7 @@ __global__ void __launch_bounds__(kBlock) stream_kernel(const StreamArgs a) {
 
 template <class Op, int VB, int U>
 cudaError_t launch_stream(const StreamArgs &a, int grid, cudaStream_t s) {
-    stream_kernel<Op, VB, U><<<grid, kBlock, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(&stream_kernel<Op, VB, U>, grid, kBlock, 0, s, a);
 }
 
 // Loads in flight per thread per input, by width: 64 bytes each.
@@ -132,6 +132,7 @@ __device__ __forceinline__ uint64_t mulmod_u64(uint64_t a, uint64_t b, uint64_t 
 // Later slots add (s*kBlock) mod n with one conditional subtraction.
 template <int E, int U>
 __global__ void __launch_bounds__(kBlock) gather_oneshot_kernel(const GatherArgs g) {
+    enter_grid();
     const char *in = static_cast<const char *>(g.in);
     char *out = static_cast<char *>(g.out);
     const uint64_t n = g.n;
@@ -157,6 +158,7 @@ __global__ void __launch_bounds__(kBlock) gather_oneshot_kernel(const GatherArgs
 // modular product and then conditional subtractions.
 template <int E, int U>
 __global__ void __launch_bounds__(kBlock) gather_stride_kernel(const GatherArgs g) {
+    enter_grid();
     const char *in = static_cast<const char *>(g.in);
     char *out = static_cast<char *>(g.out);
     const uint64_t n = g.n;
@@ -191,6 +193,7 @@ __global__ void __launch_bounds__(kBlock) gather_stride_kernel(const GatherArgs 
 // instructions); otherwise it falls back to one load per output.
 template <int S, int U>
 __global__ void __launch_bounds__(kBlock) gather_span_kernel(const GatherArgs g) {
+    enter_grid();
     const char *in = static_cast<const char *>(g.in);
     char *out = static_cast<char *>(g.out);
     const uint64_t n = g.n;
@@ -247,19 +250,16 @@ __global__ void __launch_bounds__(kBlock) gather_span_kernel(const GatherArgs g)
 
 template <int S, int U>
 cudaError_t launch_gather_span(const GatherArgs &g, int grid, cudaStream_t s) {
-    gather_span_kernel<S, U><<<grid, kBlock, 0, s>>>(g);
-    return cudaGetLastError();
+    return launch_kernel(&gather_span_kernel<S, U>, grid, kBlock, 0, s, g);
 }
 
 template <int E, int U>
 cudaError_t launch_gather_oneshot(const GatherArgs &g, int grid, cudaStream_t s) {
-    gather_oneshot_kernel<E, U><<<grid, kBlock, 0, s>>>(g);
-    return cudaGetLastError();
+    return launch_kernel(&gather_oneshot_kernel<E, U>, grid, kBlock, 0, s, g);
 }
 template <int E, int U>
 cudaError_t launch_gather_stride(const GatherArgs &g, int grid, cudaStream_t s) {
-    gather_stride_kernel<E, U><<<grid, kBlock, 0, s>>>(g);
-    return cudaGetLastError();
+    return launch_kernel(&gather_stride_kernel<E, U>, grid, kBlock, 0, s, g);
 }
 
 }  // namespace ew

@@ -84,6 +84,7 @@ template <int E> struct IsCopy<OpCopy<E>> : std::true_type {};
 
 template <class Op>
 __global__ void __launch_bounds__(kTmaBlock) tma_kernel(const TmaArgs a) {
+    enter_grid();
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_failed;
     constexpr int NIN = Op::kIn, E = Op::kElem, T = kTmaTile, S = kTmaStages;
@@ -153,8 +154,7 @@ __global__ void __launch_bounds__(kTmaBlock) tma_kernel(const TmaArgs a) {
 template <class Op>
 cudaError_t launch_tma(const TmaArgs &a, int grid, cudaStream_t s) {
     constexpr int smem = Op::kIn * kTmaStages * kTmaTile + kTmaStages * 8;
-    tma_kernel<Op><<<grid, kTmaBlock, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(&tma_kernel<Op>, grid, kTmaBlock, smem, s, a);
 }
 
 template <class Op>
@@ -175,6 +175,7 @@ const TmaEntry kTma[OP_COUNT][DT_COUNT] = {
 // Arms an mbarrier for 16 bytes that no copy will deliver: the bounded wait
 // must give up, record code 99 and return.  Nothing is in flight.
 __global__ void wait_selftest_kernel(uint64_t limit_ns) {
+    enter_grid();
     __shared__ __align__(8) uint64_t bar;
     if (threadIdx.x == 0) {
         mbar_init(&bar, 1);
@@ -193,8 +194,7 @@ const TmaEntry *tma_entry(int op, int dtype) {
 }
 
 cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t s) {
-    wait_selftest_kernel<<<1, 32, 0, s>>>(limit_ns);
-    return cudaGetLastError();
+    return launch_kernel(&wait_selftest_kernel, 1, 32, 0, s, limit_ns);
 }
 
 cudaError_t read_and_clear_device_error(cudaStream_t s, int32_t *code) {

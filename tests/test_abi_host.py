@@ -162,6 +162,17 @@ def test_plan_bulk_copy_tiles():
     assert p["path"] != 4
 
 
+def test_programmatic_launch_switch():
+    L = ew.lib()
+    assert L.ew_set_programmatic_launch(2) == INVALID
+    assert L.ew_set_programmatic_launch(-1) == INVALID
+    assert ew.get_programmatic_launch() is True  # on by default
+    ew.set_programmatic_launch(False)
+    assert ew.get_programmatic_launch() is False
+    ew.set_programmatic_launch(True)
+    assert ew.get_programmatic_launch() is True
+
+
 def test_schedule_roundtrip():
     for name in ("oneshot", "persistent", "auto"):
         ew.set_schedule(name)

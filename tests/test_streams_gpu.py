@@ -129,3 +129,39 @@ def test_bf16_tensor_views_with_offsets():
     assert_bits_equal(got, want, "bf16", True, "bf16 views")
     # offsets 6, 2 and 4 bytes agree only modulo 2: one element per access
     assert rec["vec_bytes"] == 2
+
+
+@pytest.mark.parametrize("programmatic", [True, False])
+@pytest.mark.parametrize("path", ["auto", "tma"])
+def test_dependent_chain_of_calls(programmatic, path):
+    """Sixty rounds of SAXPY -> ReLU in place -> add -> copy -> gather on one
+    stream, each call reading what the previous one wrote, with programmatic
+    dependent launch on and off: the result must equal the oracle applied
+    round by round."""
+    n = (1 << 18) + 3
+    x = inputs.normal(n, 9700)
+    y = inputs.normal(n, 9701)
+    ew.set_programmatic_launch(programmatic)
+    ew.set_path(path)
+    try:
+        tx, ty = torch.from_numpy(x).cuda(), torch.from_numpy(y).cuda()
+        tz, tw = torch.empty_like(tx), torch.empty_like(tx)
+        torch.cuda.synchronize()
+        hx, hy = x.copy(), y.copy()
+        for _ in range(60):
+            ew.ew_saxpy(0.75, tx, ty)
+            ew.ew_relu(ty, ty)
+            ew.ew_add(ty, tx, tz)
+            ew.ew_copy(tz, ty)
+            ew.ew_gather_stride(ty, tw, 3)
+            ew.ew_add(tw, tx, ty)
+            hy = oracle.relu("f32", oracle.saxpy("f32", 0.75, hx, hy))
+            hz = oracle.add("f32", hy, hx)
+            hw = oracle.gather_stride(hz, 3)
+            hy = oracle.add("f32", hw, hx)
+        torch.cuda.synchronize()
+        assert_bits_equal(ty.cpu().numpy(), hy, "f32", True, "dependent chain")
+    finally:
+        ew.set_programmatic_launch(True)
+        ew.set_path("auto")
+    assert ew.device_error() == (0, 0)
