@@ -13,6 +13,10 @@
  *                     overview and minimal kernel.
  *   ew_relu           y[i] = max(x[i], 0)
  *                     CUDA-MODE lecture notes (cyqw.cn/news/898472), §5.2 example 1.
+ *   ew_add_relu       C[i] = max(A[i] + B[i], 0) in one pass
+ *                     CUDA-MODE lecture notes, §5.3 (kernel fusion).
+ *   ew_select_even_odd y[i] = x[i] even ? 2 x[i] : x[i] + 1 on 32-bit integers
+ *                     CUDA-MODE lecture notes, §6.1-6.2 (control divergence).
  *   ew_copy           out[i] = in[i]
  *                     CUDA-MODE lecture notes, §3.2 coalesced version.
  *   ew_gather_stride  out[i] = in[(stride * i) mod n]
@@ -27,6 +31,8 @@
  *                exactly to binary32, fmaf there, then one rounding to the format.
  *                alpha is binary32 and is never rounded to the 16-bit format.
  *   relu         x > 0 -> x;  x <= 0 (including -0) -> +0;  NaN -> x unchanged.
+ *   add_relu     relu applied to the rounded sum of add.
+ *   select       two's complement int32, wrapping modulo 2^32.
  *   copy/gather  raw element bits.
  *
  * Common conventions
@@ -37,7 +43,8 @@
  *              the kernels then read and write over the CPU-GPU link.  The library
  *              allocates no memory and keeps no reference after a call returns.
  *              Each pointer must be aligned to the element size (4 bytes for
- *              EW_F32, 2 for EW_F16/EW_BF16), else EW_ERR_INVALID_VALUE.  Any
+ *              EW_F32 and EW_I32, 2 for EW_F16/EW_BF16), else
+ *              EW_ERR_INVALID_VALUE.  Any
  *              such alignment is accepted; the widest vector width that all the
  *              pointers of a call share is used (see ew_plan_query).
  *   Layout     n contiguous elements, index 0 first.
@@ -50,14 +57,16 @@
  *   Streams    every call enqueues at most one kernel on `stream` (NULL = the
  *              legacy default stream) on the calling thread's current device and
  *              returns without synchronising.  Kernels are launched with
- *              programmatic dependent launch unless ew_set_programmatic_launch(0).  Device faults surface at the
- *              caller's next synchronisation.
+ *              programmatic dependent launch unless ew_set_programmatic_launch(0)
+ *              (see there).  Device faults surface at the caller's next
+ *              synchronisation.
  *   Errors     every call returns an ew_status and never prints or aborts.
  *              Argument errors are detected on the host before any CUDA call.
  *              EW_ERR_CUDA: a CUDA runtime call or the launch failed; the
  *              cudaError_t value is kept per thread (ew_last_cuda_error).
- *   Threads    all entry points are thread-safe.  The variant selection
- *              (ew_set_path) is process-wide.
+ *   Threads    all entry points are thread-safe.  The variant selections
+ *              (ew_set_path, ew_set_schedule, ew_set_programmatic_launch,
+ *              ew_set_pointer_check) are process-wide.
  */
 #ifndef EW_H
 #define EW_H
@@ -197,9 +206,10 @@ EW_API int ew_get_programmatic_launch(void);
  * environment variable EW_CHECK_POINTERS=1 enables it at start-up. */
 EW_API ew_status ew_set_pointer_check(int enable);
 
-/* How an ew_add / ew_saxpy / ew_relu / ew_copy call with these pointers is
- * split under the current ew_set_path selection (host arithmetic only; needs no
- * GPU).  ptrs: the call's input and output pointers; nptrs in [1, 4]. */
+/* How an ew_add / ew_saxpy / ew_relu / ew_add_relu / ew_select_even_odd /
+ * ew_copy call with these pointers is split under the current ew_set_path
+ * selection (host arithmetic only; needs no GPU).  ptrs: the call's input and
+ * output pointers; nptrs in [1, 4]. */
 typedef struct {
     int32_t path;      /* ew_path that will run */
     int32_t vec_bytes; /* bytes per access in the body (element size for SCALAR) */

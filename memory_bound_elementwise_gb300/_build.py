@@ -38,13 +38,13 @@ def nvcc():
     raise RuntimeError("nvcc not found")
 
 
-def _inputs_digest():
-    """SHA-256 over the kernel sources, the public header and the compiler
-    flags, independent of where the repository sits on disk."""
+def _kernel_digest():
+    """SHA-256 over the CUDA sources (kernels and dispatch) and the compiler
+    flags, independent of where the repository sits on disk.  Profiler figures
+    are tied to it."""
     h = hashlib.sha256()
     files = [os.path.join(CSRC, name) for name in sorted(os.listdir(CSRC))
              if name.endswith((".cu", ".cuh", ".h"))]
-    files.append(os.path.join(INCLUDE, "ew.h"))
     for path in files:
         h.update(os.path.relpath(path, ROOT).encode())
         with open(path, "rb") as f:
@@ -55,8 +55,16 @@ def _inputs_digest():
 
 
 def source_digest():
-    """SHA-256 over the kernel sources, header and flags (identifies a build)."""
-    return _inputs_digest()
+    """SHA-256 over the kernel sources and flags (what profiler figures were taken on)."""
+    return _kernel_digest()
+
+
+def _inputs_digest():
+    """Build stamp: the kernel sources and flags plus the public header."""
+    h = hashlib.sha256(_kernel_digest().encode())
+    with open(os.path.join(INCLUDE, "ew.h"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
