@@ -232,6 +232,8 @@ class ClockSampler:
 
 
 def host_cpu_model():
+    """CPU model of the host (x86 /proc/cpuinfo, else lscpu, else the machine)."""
+    import platform
     try:
         with open("/proc/cpuinfo") as f:
             for line in f:
@@ -239,7 +241,14 @@ def host_cpu_model():
                     return line.split(":", 1)[1].strip()
     except Exception:
         pass
-    import platform
+    try:
+        out = subprocess.run(["lscpu"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                             text=True, timeout=20).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return "%s %s" % (platform.machine(), line.split(":", 1)[1].strip())
+    except Exception:
+        pass
     return platform.machine()
 
 
