@@ -68,7 +68,7 @@ def parse():
     p.add_argument("--no-aux", action="store_true", help="skip the other workloads")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     p.add_argument("--path", default="auto", help="kernel variant: auto, scalar, v128, v256, tma")
-    p.add_argument("--schedule", default="auto", help="block schedule: auto, oneshot, persistent")
+    p.add_argument("--schedule", default="auto", help="block schedule: auto, oneshot, persistent, laps")
     p.add_argument("--profile-case", default=None, choices=sorted(PROFILE_CASES),
                    help="run only warmup+steps launches of one workload at --n (for ncu captures)")
     return p.parse_args()
@@ -447,6 +447,16 @@ def aux_measurements(torch, ew, inputs, metrics, stream, peak, dev):
     record("copy_f32_2p26", "copy", "f32", n26, lambda: L.ew_copy(0, px, py, n26, s), steps=200)
     record("gather2_f32_2p26", "gather", "f32", n26,
            lambda: L.ew_gather_stride(0, px, py, n26, 2, s), steps=100)
+    record("gather4_f32_2p26", "gather", "f32", n26,
+           lambda: L.ew_gather_stride(0, px, py, n26, 4, s), steps=100)
+    # index order (one block per 1024 consecutive outputs): once the input no
+    # longer fits in L2, each lap fetches it from DRAM again
+    ew.set_schedule("oneshot")
+    record("gather2_f32_2p26_index_order", "gather", "f32", n26,
+           lambda: L.ew_gather_stride(0, px, py, n26, 2, s), steps=100)
+    record("gather4_f32_2p26_index_order", "gather", "f32", n26,
+           lambda: L.ew_gather_stride(0, px, py, n26, 4, s), steps=100)
+    ew.set_schedule("auto")
     ew.set_path("v256")  # span variant: contiguous 256-bit source spans, lane select
     record("gather2_f32_2p26_span", "gather", "f32", n26,
            lambda: L.ew_gather_stride(0, px, py, n26, 2, s), steps=100)

@@ -119,13 +119,26 @@ typedef enum {
 /* How the body's chunks are handed to thread blocks.
  * EW_SCHED_ONESHOT    one block per chunk of 256 threads x 64 bytes per thread
  *                     per input; the hardware block scheduler balances the SMs
- *                     (the default: fastest measured on GB300).
+ *                     (the default: fastest measured on GB300).  The gather
+ *                     walks its outputs in index order.
  * EW_SCHED_PERSISTENT at most SMs x resident blocks per SM, each striding over
- *                     the chunks (the grid-stride design of the pages). */
+ *                     the chunks (the grid-stride design of the pages).
+ * EW_SCHED_LAPS       gather only (the other operators run EW_SCHED_ONESHOT):
+ *                     as i runs over the outputs, (stride * i) mod n sweeps the
+ *                     input s = (stride mod n) times.  One block per chunk of
+ *                     2048 outputs of one sweep ("lap"), with the s laps'
+ *                     blocks interleaved so that the blocks running together
+ *                     read the same stretch of the input and each sector comes
+ *                     from DRAM once.  It applies when 2 <= s <= 64,
+ *                     n <= 2^32 and n >= 2048 s; otherwise EW_SCHED_ONESHOT
+ *                     runs.
+ * EW_SCHED_AUTO       EW_SCHED_LAPS for the gather, EW_SCHED_ONESHOT for the
+ *                     rest.  A gather with n > 2^32 always runs persistent. */
 typedef enum {
     EW_SCHED_AUTO = 0,
     EW_SCHED_ONESHOT = 1,
-    EW_SCHED_PERSISTENT = 2
+    EW_SCHED_PERSISTENT = 2,
+    EW_SCHED_LAPS = 3
 } ew_schedule;
 
 /* ---- operators ------------------------------------------------------- */
@@ -166,7 +179,9 @@ EW_API ew_status ew_copy(ew_dtype dtype, const void *in, void *out, int64_t n, e
  * without overflow.  stride >= 1 (else EW_ERR_INVALID_VALUE).  in and out must
  * not overlap.  As in the page's non-coalesced copy, each thread reads one
  * element per access, so a warp's load touches every stride-th element of a
- * span while its store covers consecutive elements.  With ew_set_path
+ * span while its store covers consecutive elements.  The order in which
+ * blocks take the outputs follows ew_set_schedule (EW_SCHED_LAPS by default).
+ * With ew_set_path
  * (EW_PATH_V256) selected, 4-byte elements with (stride mod n) of 2 or 4 and
  * n <= 2^32 use a span variant instead: each thread loads the contiguous
  * source span of 8 outputs with 256-bit loads and keeps every stride-th word

@@ -90,9 +90,10 @@ int resolved_path() {
     const int p = g_path.load(std::memory_order_relaxed);
     return p == EW_PATH_AUTO ? EW_PATH_V256 : p;
 }
+// schedule of the streaming kernels (lap order exists for the gather only)
 int resolved_schedule() {
     const int s = g_schedule.load(std::memory_order_relaxed);
-    return s == EW_SCHED_AUTO ? EW_SCHED_ONESHOT : s;
+    return (s == EW_SCHED_AUTO || s == EW_SCHED_LAPS) ? EW_SCHED_ONESHOT : s;
 }
 
 // Bulk-copy split: 16-byte aligned head, whole tiles, then the remainder.
@@ -373,12 +374,12 @@ ew_status ew_gather_stride(ew_dtype dt, const void *in, void *out, int64_t n, in
     if (ce != cudaSuccess) return cuda_fail(ce);
     const uint64_t un = static_cast<uint64_t>(n);
     const uint64_t s_mod = static_cast<uint64_t>(stride) % un;
-    const int sched = resolved_schedule();
+    const int sched = g_schedule.load(std::memory_order_relaxed);
     // span variant (EW_PATH_V256 only): 4-byte elements, stride 2 or 4, n <= 2^32
     if (resolved_path() == EW_PATH_V256 && g_path.load(std::memory_order_relaxed) != EW_PATH_AUTO &&
         elem_size(dt) == 4 && (s_mod == 2 || s_mod == 4) && un <= (uint64_t(1) << 32)) {
         const GatherEntry *g = gather_span_4(static_cast<int64_t>(s_mod));
-        GatherArgs ga{in, out, un, s_mod, 0, ~uint64_t(0) / un, 0, 0, 0};
+        GatherArgs ga{in, out, un, s_mod, 0, ~uint64_t(0) / un, 0, 0, 0, 0, 0, 0};
         const uintptr_t o = reinterpret_cast<uintptr_t>(out);
         ga.head = std::min<int64_t>(static_cast<int64_t>(((32 - o % 32) % 32) / 4), n);
         ga.nvec = (n - ga.head) / 8;
@@ -398,12 +399,24 @@ ew_status ew_gather_stride(ew_dtype dt, const void *in, void *out, int64_t n, in
         t_last.tail = n - ga.tail0;
         return EW_OK;
     }
-    const bool oneshot = sched == EW_SCHED_ONESHOT && un <= (uint64_t(1) << 32);
-    GatherArgs ga{in, out, un, s_mod, 0, 0, 0, 0, 0};
+    const bool oneshot = sched != EW_SCHED_PERSISTENT && un <= (uint64_t(1) << 32);
+    const bool lap_order = oneshot && sched != EW_SCHED_ONESHOT;
+    GatherArgs ga{in, out, un, s_mod, 0, 0, 0, 0, 0, 0, 0, 0};
     const GatherEntry *g;
     int grid;
     const bool four = elem_size(dt) == 4;
-    if (oneshot) {
+    const GatherEntry *laps = four ? gather_laps_4() : gather_laps_2();
+    const uint64_t lap_block = static_cast<uint64_t>(kBlock) * laps->unroll;
+    const bool lapped = lap_order && s_mod >= 2 && s_mod <= kMaxLaps && un / s_mod >= lap_block;
+    if (lapped) {
+        // lap order: block b takes chunk b / s of lap b mod s
+        g = laps;
+        const uint64_t lap_len = (un + s_mod - 1) / s_mod;  // the longest lap
+        grid = clamp_grid(static_cast<int64_t>(s_mod * ((lap_len + lap_block - 1) / lap_block)));
+        ga.lap_q = static_cast<uint32_t>(un / s_mod);
+        ga.lap_m = static_cast<uint32_t>(un % s_mod);
+        ga.div_magic = static_cast<uint32_t>((uint64_t(1) << 32) / s_mod + 1);
+    } else if (oneshot) {
         g = four ? gather_oneshot_4() : gather_oneshot_2();
         const int64_t per_block = static_cast<int64_t>(kBlock) * g->unroll;
         grid = clamp_grid((n + per_block - 1) / per_block);
@@ -426,7 +439,7 @@ ew_status ew_gather_stride(ew_dtype dt, const void *in, void *out, int64_t n, in
     t_last.vec_bytes = elem_size(dt);
     t_last.grid = grid;
     t_last.block = kBlock;
-    t_last.schedule = oneshot ? EW_SCHED_ONESHOT : EW_SCHED_PERSISTENT;
+    t_last.schedule = lapped ? EW_SCHED_LAPS : oneshot ? EW_SCHED_ONESHOT : EW_SCHED_PERSISTENT;
     t_last.nvec = n;
     return EW_OK;
 }
@@ -442,7 +455,7 @@ ew_path ew_get_path(void) { return static_cast<ew_path>(g_path.load(std::memory_
 
 ew_status ew_set_schedule(ew_schedule sched) {
     const int v = static_cast<int>(sched);
-    if (v < EW_SCHED_AUTO || v > EW_SCHED_PERSISTENT) return EW_ERR_INVALID_VALUE;
+    if (v < EW_SCHED_AUTO || v > EW_SCHED_LAPS) return EW_ERR_INVALID_VALUE;
     g_schedule.store(v, std::memory_order_relaxed);
     return EW_OK;
 }

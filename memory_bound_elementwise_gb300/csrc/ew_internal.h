@@ -89,6 +89,9 @@ struct GatherArgs {
     int64_t head;        // span kernel: outputs [0, head) one by one (32-byte output alignment)
     int64_t nvec;        // span kernel: 8-element output vectors after the head
     int64_t tail0;       // span kernel: outputs [tail0, n) one by one
+    uint32_t lap_q;      // lap kernel: n / s_mod
+    uint32_t lap_m;      // lap kernel: n mod s_mod
+    uint32_t div_magic;  // lap kernel: floor(2^32 / s_mod) + 1
 };
 using GatherLaunchFn = cudaError_t (*)(const GatherArgs &, int grid, cudaStream_t);
 struct GatherEntry {
@@ -96,6 +99,11 @@ struct GatherEntry {
     GatherLaunchFn launch;
     int unroll;
 };
+// Lap-ordered gather: 2 <= s_mod <= kMaxLaps, n <= 2^32 and n >= s_mod x the
+// outputs of one block.
+constexpr uint64_t kMaxLaps = 64;
+const GatherEntry *gather_laps_4();
+const GatherEntry *gather_laps_2();
 const GatherEntry *gather_oneshot_4();  // binary32, n <= 2^32
 const GatherEntry *gather_stride_4();   // binary32, any n
 const GatherEntry *gather_oneshot_2();  // 16-bit types

@@ -153,6 +153,52 @@ __global__ void __launch_bounds__(kBlock) gather_oneshot_kernel(const GatherArgs
         if (i0 + k * kBlock < n) st<E>(out + (i0 + k * kBlock) * E, v[k]);
 }
 
+// Lap-ordered gather for a small stride (2 <= s <= kMaxLaps, n <= 2^32).  As
+// i runs from 0 to n - 1 the source (s*i) mod n sweeps the input s times.
+// Lap L holds the outputs i in [ceil(L*n/s), ceil((L+1)*n/s)); there the
+// source is s*i - L*n = r_L + s*p, with p the position in the lap and
+// r_L = s*ceil(L*n/s) - L*n < s, so no reduction mod n is needed.  Block b
+// takes chunk b / s of lap b mod s.  The s blocks that the scheduler starts
+// side by side then read the same stretch of the input, and each sector comes
+// from DRAM once.  In index order each lap fetches the whole input again once
+// it no longer fits in L2.  The work is unchanged: one load per output, from
+// the same source.
+//
+// Index arithmetic is 32-bit: with n = q*s + m (q = lap_q, m = lap_m),
+// ceil(L*n/s) = L*q + ceil(L*m/s), where L*m < kMaxLaps^2, and every valid
+// position, source and output index is below n <= 2^32.  Divisions by s use
+// div_magic = floor(2^32 / s) + 1, which over-estimates by at most one.
+__device__ __forceinline__ uint32_t div_by_s(uint32_t a, uint32_t s, uint32_t magic) {
+    const uint32_t q = __umulhi(a, magic);  // floor(a / s) or one more
+    return q * s > a ? q - 1 : q;
+}
+
+template <int E, int U>
+__global__ void __launch_bounds__(kBlock) gather_laps_kernel(const GatherArgs g) {
+    enter_grid();
+    const char *in = static_cast<const char *>(g.in);
+    char *out = static_cast<char *>(g.out);
+    const uint32_t s = static_cast<uint32_t>(g.s_mod);
+    const uint32_t k = div_by_s(blockIdx.x, s, g.div_magic);
+    const uint32_t lap = blockIdx.x - k * s;
+    const uint32_t a0 = lap * g.lap_m, a1 = a0 + g.lap_m;  // L*m, (L+1)*m
+    const uint32_t c0 = div_by_s(a0 + s - 1, s, g.div_magic);  // ceil(L*m/s)
+    const uint32_t c1 = div_by_s(a1 + s - 1, s, g.div_magic);
+    const uint32_t len = g.lap_q + (c1 - c0);  // outputs in this lap
+    const uint32_t p0 = k * (kBlock * U) + threadIdx.x;
+    if (p0 >= len) return;
+    const uint32_t i0 = lap * g.lap_q + c0 + p0;  // first output of this thread
+    const uint32_t j0 = (c0 * s - a0) + s * p0;   // its source
+    const uint32_t jstep = s * kBlock;
+    Vec<E> v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+        if (p0 + u * kBlock < len) v[u] = ld<E>(in + static_cast<size_t>(j0 + u * jstep) * E);
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+        if (p0 + u * kBlock < len) st<E>(out + static_cast<size_t>(i0 + u * kBlock) * E, v[u]);
+}
+
 // Grid-stride gather for any n: with i = v + k*T (T = grid threads),
 // (s*i) mod n advances by (s*T) mod n per slot, so each thread needs one
 // modular product and then conditional subtractions.
@@ -256,6 +302,10 @@ cudaError_t launch_gather_span(const GatherArgs &g, int grid, cudaStream_t s) {
 template <int E, int U>
 cudaError_t launch_gather_oneshot(const GatherArgs &g, int grid, cudaStream_t s) {
     return launch_kernel(&gather_oneshot_kernel<E, U>, grid, kBlock, 0, s, g);
+}
+template <int E, int U>
+cudaError_t launch_gather_laps(const GatherArgs &g, int grid, cudaStream_t s) {
+    return launch_kernel(&gather_laps_kernel<E, U>, grid, kBlock, 0, s, g);
 }
 template <int E, int U>
 cudaError_t launch_gather_stride(const GatherArgs &g, int grid, cudaStream_t s) {

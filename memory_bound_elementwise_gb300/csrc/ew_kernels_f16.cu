@@ -27,11 +27,15 @@ const GatherEntry kGatherOneshot{reinterpret_cast<const void *>(&gather_oneshot_
                                  &launch_gather_oneshot<2, kGatherOneshotUnroll>, kGatherOneshotUnroll};
 const GatherEntry kGatherStride{reinterpret_cast<const void *>(&gather_stride_kernel<2, kGatherStrideUnroll>),
                                 &launch_gather_stride<2, kGatherStrideUnroll>, kGatherStrideUnroll};
+constexpr int kGatherLapsUnroll = 8;
+const GatherEntry kGatherLaps{reinterpret_cast<const void *>(&gather_laps_kernel<2, kGatherLapsUnroll>),
+                              &launch_gather_laps<2, kGatherLapsUnroll>, kGatherLapsUnroll};
 }  // namespace
 
 const StreamEntry *stream_table_f16() { return &kTable[0][0]; }
 
 const GatherEntry *gather_oneshot_2() { return &kGatherOneshot; }
+const GatherEntry *gather_laps_2() { return &kGatherLaps; }
 const GatherEntry *gather_stride_2() { return &kGatherStride; }
 
 }  // namespace ew

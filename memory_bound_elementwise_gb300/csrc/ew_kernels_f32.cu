@@ -27,6 +27,9 @@ const GatherEntry kGatherOneshot{reinterpret_cast<const void *>(&gather_oneshot_
                                  &launch_gather_oneshot<4, kGatherOneshotUnroll>, kGatherOneshotUnroll};
 const GatherEntry kGatherStride{reinterpret_cast<const void *>(&gather_stride_kernel<4, kGatherStrideUnroll>),
                                 &launch_gather_stride<4, kGatherStrideUnroll>, kGatherStrideUnroll};
+constexpr int kGatherLapsUnroll = 8;
+const GatherEntry kGatherLaps{reinterpret_cast<const void *>(&gather_laps_kernel<4, kGatherLapsUnroll>),
+                              &launch_gather_laps<4, kGatherLapsUnroll>, kGatherLapsUnroll};
 }  // namespace
 
 const StreamEntry *stream_table_f32() { return &kTable[0][0]; }
@@ -41,6 +44,7 @@ const GatherEntry *gather_span_4(int64_t stride) {
     return stride == 2 ? &kGatherSpan2 : stride == 4 ? &kGatherSpan4 : nullptr;
 }
 const GatherEntry *gather_oneshot_4() { return &kGatherOneshot; }
+const GatherEntry *gather_laps_4() { return &kGatherLaps; }
 const GatherEntry *gather_stride_4() { return &kGatherStride; }
 
 }  // namespace ew

@@ -120,7 +120,7 @@ def test_small_sizes_every_offset(op, dtype):
             check_case(op, dtype, n, [off] * nin, seed=1000 + n * 37 + off)
 
 
-@pytest.mark.parametrize("schedule", ["oneshot", "persistent"])
+@pytest.mark.parametrize("schedule", ["oneshot", "persistent", "laps"])
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("op", ["add", "saxpy", "relu", "copy", "add_relu"])
@@ -137,7 +137,8 @@ def test_forced_paths(op, dtype, path, schedule):
             elif path == "tma":
                 assert rec["path"] == 4 and rec["vec_bytes"] == 16
             if path != "tma" and rec["nvec"] > 0:
-                assert rec["schedule"] == (1 if schedule == "oneshot" else 2)
+                # lap order exists for the gather only: the streaming kernels run one-shot
+                assert rec["schedule"] == (2 if schedule == "persistent" else 1)
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
@@ -174,10 +175,19 @@ def test_bounded_wait_gives_up_and_reports():
     assert float(y.sum()) == float(sum(range(1, 500)))
 
 
+LAP_BLOCK = 2048  # outputs per block of the lap-ordered gather (256 threads x 8)
+
+
+def _gather_laps(n, s):
+    """Whether ew_gather_stride takes the lap-ordered kernel (schedule 'laps' or 'auto')."""
+    sm = s % n
+    return 2 <= sm <= 64 and n <= 1 << 32 and n // sm >= LAP_BLOCK
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_gather_schedules_agree(dtype):
     L = ew.lib()
-    for sched in ("oneshot", "persistent"):
+    for sched in ("oneshot", "persistent", "laps", "auto"):
         ew.set_schedule(sched)
         for n in (1, 5, 4097, 300_001):
             x = inputs.random_bits(n, dtype, 6500 + n)
@@ -187,7 +197,12 @@ def test_gather_schedules_agree(dtype):
                 assert L.ew_gather_stride(DT_CODE[dtype], bi.view.data_ptr(), bo.view.data_ptr(),
                                           n, s, _stream()) == 0
                 rec = ew.last_launch()
-                assert rec["schedule"] == (1 if sched == "oneshot" else 2)
+                if sched == "persistent":
+                    assert rec["schedule"] == 2
+                elif sched == "oneshot" or not _gather_laps(n, s):
+                    assert rec["schedule"] == 1
+                else:
+                    assert rec["schedule"] == 3
                 torch.cuda.synchronize()
                 assert_bits_equal(bo.host(), oracle.gather_stride(x, s), dtype, False,
                                   "gather %s n=%d s=%d" % (sched, n, s))
@@ -334,6 +349,39 @@ def test_gather_small(dtype):
             assert_bits_equal(bo.host(), oracle.gather_stride(x, s), dtype, False,
                               "gather n=%d s=%d" % (n, s))
             assert bi.guards_intact() and bo.guards_intact()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+def test_gather_lap_order(dtype):
+    """The lap-ordered gather (the default for strides 2..64 once every lap
+    holds a block of outputs): sizes at, just below and just above the
+    threshold n = 2048 s, laps of unequal length (s not dividing n), laps that
+    read the same sources (s | n) and laps on distinct residues (s coprime to
+    n), stride 65 and strides above n, misaligned input and output."""
+    L = ew.lib()
+    ew.set_schedule("auto")
+    cases = []
+    for s in (2, 3, 4, 5, 7, 8, 16, 31, 33, 64, 65):
+        for n in (LAP_BLOCK * s - 1, LAP_BLOCK * s, LAP_BLOCK * s + 1, 3 * LAP_BLOCK * s + 5, 200_003):
+            cases.append((n, s))
+    cases += [(1 << 20, (1 << 20) + 2), (1 << 20, 3 * (1 << 20) + 5), (1 << 20, 2 + (1 << 40) * (1 << 20))]
+    for n, s in cases:
+        x = inputs.random_bits(n, dtype, 6700 + n + s)
+        bi = GuardedBuffer(n, dtype, 3).fill(x)
+        bo = GuardedBuffer(n, dtype, 1)
+        assert L.ew_gather_stride(DT_CODE[dtype], bi.view.data_ptr(), bo.view.data_ptr(),
+                                  n, s, _stream()) == 0
+        rec = ew.last_launch()
+        laps = _gather_laps(n, s)
+        assert rec["schedule"] == (3 if laps else 1), (n, s, rec)
+        if laps:
+            sm = s % n
+            lap_len = -(-n // sm)
+            assert rec["grid"] == sm * -(-lap_len // LAP_BLOCK), (n, s, rec)
+        torch.cuda.synchronize()
+        assert_bits_equal(bo.host(), oracle.gather_stride(x, s), dtype, False,
+                          "lap gather n=%d s=%d" % (n, s))
+        assert bi.guards_intact() and bo.guards_intact()
 
 
 def test_launch_record_and_grid():
