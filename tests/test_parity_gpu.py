@@ -595,6 +595,44 @@ def test_gather_beyond_2p32_elements_f16():
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("n,s", [(1 << 32, 2), ((1 << 32) - 1, 3), (1 << 32, 64), ((1 << 32) - 7, 5)])
+def test_gather_lap_order_at_2p32_int32(n, s):
+    """The lap-ordered gather's 32-bit index arithmetic at its limit n <= 2^32:
+    the input holds its own index (int32, i.e. modulo 2^32), so every output
+    names the source it was read from.  All n outputs are compared with
+    (s*i) mod n computed in int64 by torch, chunk by chunk, and 2,000
+    positions (both ends, every lap boundary, random) with the oracle's
+    128-bit index map."""
+    chunk = 1 << 28
+    tin = torch.empty(n, dtype=torch.int32, device="cuda")
+    for lo in range(0, n, chunk):
+        hi = min(n, lo + chunk)
+        v = torch.arange(lo, hi, dtype=torch.int64, device="cuda")
+        tin[lo:hi] = ((v + (1 << 31)) % (1 << 32) - (1 << 31)).to(torch.int32)
+        del v
+    tout = torch.empty_like(tin)
+    assert ew.lib().ew_gather_stride(3, tin.data_ptr(), tout.data_ptr(), n, s, _stream()) == 0
+    rec = ew.last_launch()
+    assert rec["schedule"] == 3, rec
+    torch.cuda.synchronize()
+    for lo in range(0, n, chunk):
+        hi = min(n, lo + chunk)
+        want = torch.arange(lo, hi, dtype=torch.int64, device="cuda") * s % n
+        got = tout[lo:hi].to(torch.int64) % (1 << 32)
+        assert torch.equal(got, want), "chunk at %d" % lo
+        del want, got
+    g = inputs.rng(8300 + s)
+    bounds = [-(-lap * n // s) for lap in range(s + 1)]
+    idx = sorted({int(i) for b in bounds for i in (b - 1, b, b + 1) if 0 <= i < n}
+                 | set(range(0, 200)) | set(range(n - 200, n))
+                 | {int(i) for i in g.integers(0, n, size=1500, dtype=np.int64)})
+    got = tout[torch.tensor(idx, dtype=torch.int64, device="cuda")].cpu().numpy().view(np.uint32)
+    want = np.array([oracle.gather_index(i, s, n) for i in idx], dtype=np.int64)
+    assert np.array_equal(got.astype(np.int64), want)
+    del tin, tout
+    torch.cuda.empty_cache()
+
+
 def _random_i32(n, seed):
     g = inputs.rng(seed)
     x = g.integers(-2 ** 31, 2 ** 31, size=n, dtype=np.int64).astype(np.int32)
