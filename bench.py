@@ -74,7 +74,7 @@ def parse():
     return p.parse_args()
 
 
-# op, dtype, element offset of every pointer, input distribution
+# op, dtype, element offset of every pointer (or of A, B, C)
 PROFILE_CASES = {
     "add_f32": ("add", "f32", 0),
     "add_bf16_off1": ("add", "bf16", 1),
@@ -86,6 +86,7 @@ PROFILE_CASES = {
     "relu_inplace_f32": ("relu_inplace", "f32", 0),
     "select_i32": ("select", "f32", 0),
     "gather2_span_f32": ("gather_span", "f32", 0),
+    "add_bf16_mixed": ("add", "bf16", (1, 0, 3)),
 }
 
 
@@ -103,15 +104,17 @@ def run_profile_case(args):
     e = 4 if dtype == "f32" else 2
     dev = torch.device("cuda", 0)
 
-    def buf(arr):
+    offs = off if isinstance(off, tuple) else (off, off, off)  # A (x), B (y), C (z)
+
+    def buf(arr, o):
         raw = torch.empty(arr.size * e + 256, dtype=torch.uint8, device=dev)
-        raw[off * e: off * e + arr.size * e].copy_(torch.from_numpy(np.ascontiguousarray(arr).view(np.uint8)))
-        return raw, raw.data_ptr() + off * e
+        raw[o * e: o * e + arr.size * e].copy_(torch.from_numpy(np.ascontiguousarray(arr).view(np.uint8)))
+        return raw, raw.data_ptr() + o * e
 
     x = inputs.as_dtype(inputs.normal(n, inputs.seed_for("add_f32")), dtype)
-    rx, px = buf(x)
-    ry, py = buf(inputs.as_dtype(inputs.uniform(n, inputs.seed_for("add_f32", 1)), dtype))
-    rz, pz = buf(np.zeros_like(x))
+    rx, px = buf(x, offs[0])
+    ry, py = buf(inputs.as_dtype(inputs.uniform(n, inputs.seed_for("add_f32", 1)), dtype), offs[1])
+    rz, pz = buf(np.zeros_like(x), offs[2])
     L = ew.lib()
     s = torch.cuda.current_stream().cuda_stream
     code = {"f32": 0, "f16": 1, "bf16": 2}[dtype]
@@ -383,6 +386,18 @@ def aux_measurements(torch, ew, inputs, metrics, stream, peak, dev):
             rc, pc = dev_of(np.zeros_like(xa), dtype, off)
             record("add_%s_2p28_off%d" % (dtype, off), "add", dtype, n28,
                    lambda: L.ew_add(code, pa, pb, pc, n28, s))
+            del ra, rb, rc
+        if dtype == "bf16":
+            # pointers of different parity (A +1, B +0, C +3 elements): the
+            # realigning bulk-copy kernel (default) against 2-byte accesses
+            ra, pa = dev_of(xa, dtype, 1)
+            rb, pb = dev_of(xb, dtype, 0)
+            rc, pc = dev_of(np.zeros_like(xa), dtype, 3)
+            record("add_bf16_2p28_mixed_parity", "add", dtype, n28, lambda: L.ew_add(code, pa, pb, pc, n28, s))
+            ew.set_path("v256")
+            record("add_bf16_2p28_mixed_parity_2byte", "add", dtype, n28,
+                   lambda: L.ew_add(code, pa, pb, pc, n28, s))
+            ew.set_path("auto")
             del ra, rb, rc
         del xa, xb
     n32m = 32 << 20

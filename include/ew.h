@@ -112,8 +112,13 @@ typedef enum {
     EW_PATH_SCALAR = 1, /* one element per access, grid-stride */
     EW_PATH_V128 = 2,   /* 16-byte vector accesses */
     EW_PATH_V256 = 3,   /* 32-byte vector accesses (sm_100 family) */
-    EW_PATH_TMA = 4     /* bulk async copies (cp.async.bulk) through shared memory;
-                           needs all pointers at one offset modulo 16 bytes */
+    EW_PATH_TMA = 4     /* bulk async copies (cp.async.bulk) through shared memory.
+                           Pointers that disagree modulo 16 bytes take a
+                           realigning kernel: each input tile is copied as the
+                           16-byte aligned span around it and read at its offset
+                           in shared memory.  EW_PATH_AUTO uses that kernel for
+                           16-bit elements whose pointers differ in parity
+                           (2-byte accesses otherwise) from n >= 2^22 */
 } ew_path;
 
 /* How the body's chunks are handed to thread blocks.
@@ -223,8 +228,13 @@ EW_API ew_status ew_set_pointer_check(int enable);
 
 /* How an ew_add / ew_saxpy / ew_relu / ew_add_relu / ew_select_even_odd /
  * ew_copy call with these pointers is split under the current ew_set_path
- * selection (host arithmetic only; needs no GPU).  ptrs: the call's input and
- * output pointers; nptrs in [1, 4]. */
+ * selection (host arithmetic only; needs no GPU).  ptrs: the call's input
+ * pointers, then its output pointer last; nptrs in [1, 4].  When the pointers
+ * disagree modulo 16 bytes, a bulk-copy plan (EW_PATH_TMA, and EW_PATH_AUTO
+ * for 16-bit elements of different parity from n >= 2^22) stages each input
+ * as the aligned span around its tile: the head then aligns the output only
+ * and is at least 16 bytes, and the tail is at least 16 bytes when there is a
+ * tile. */
 typedef struct {
     int32_t path;      /* ew_path that will run */
     int32_t vec_bytes; /* bytes per access in the body (element size for SCALAR) */

@@ -98,6 +98,19 @@ int resolved_schedule() {
 
 // Bulk-copy split: 16-byte aligned head, whole tiles, then the remainder.
 struct TmaPlan { int64_t head, ntiles, rem0; };
+
+// Blocks of a bulk-copy launch: kTmaStages tiles per block, then one block per
+// kTmaBlock elements outside the tiles (head and remainder, one per thread).
+int64_t tma_grid(const TmaPlan &tp, int64_t n) {
+    const int64_t scalar = tp.head + (n - tp.rem0);
+    return (tp.ntiles + kTmaStages - 1) / kTmaStages + (scalar + kTmaBlock - 1) / kTmaBlock;
+}
+
+// The bulk-copy launches have no grid-stride loop: they need a grid of at most
+// INT_MAX blocks (arrays below 2^31 x 16 KiB); beyond it the vector kernels run.
+bool tma_grid_fits(int64_t n, int e) {
+    return n / (kTmaTile / e) / kTmaStages < INT_MAX - 2 * kTmaTile;
+}
 TmaPlan make_tma_plan(const ew_plan &pl16, int e, int64_t n) {
     TmaPlan t{};
     t.head = pl16.head;
@@ -190,8 +203,8 @@ ew_status run_tma(int op, ew_dtype dt, const void *in0, const void *in1, void *o
     const TmaEntry *ent = tma_entry(op, table_dtype(dt));
     const int e = elem_size(dt);
     const TmaPlan tp = make_tma_plan(pl16, e, n);
-    TmaArgs a{in0, in1, out, n, tp.head, tp.ntiles, tp.rem0, alpha, kWaitLimitNs};
-    const int grid = clamp_grid((tp.ntiles + kTmaStages - 1) / kTmaStages);
+    TmaArgs a{in0, in1, out, n, tp.head, tp.ntiles, tp.rem0, alpha, kWaitLimitNs, 0, 0};
+    const int grid = static_cast<int>(tma_grid(tp, n));
     cudaError_t ce = ent->launch(a, grid, s);
     if (ce != cudaSuccess) return cuda_fail(ce);
     t_last.launches = 1;
@@ -204,6 +217,57 @@ ew_status run_tma(int op, ew_dtype dt, const void *in0, const void *in1, void *o
     t_last.head = tp.head;
     t_last.nvec = tp.ntiles;
     t_last.tail = n - tp.rem0;
+    return EW_OK;
+}
+
+// Realigning bulk-copy split, for pointers that disagree modulo 16 bytes:
+// output tiles start 16-byte aligned, and each input is staged as the aligned
+// span around its tile.  At least 16 bytes of elements stay outside the tiles
+// at both ends, so the spans never leave the input arrays.
+TmaPlan make_realign_plan(uintptr_t out, int e, int64_t n) {
+    TmaPlan t{};
+    t.head = static_cast<int64_t>((16 - out % 16) % 16) / e;
+    if (t.head * e < 16) t.head += 16 / e;
+    const int64_t per_tile = kTmaTile / e;
+    const int64_t avail = n - t.head - 16 / e;
+    t.ntiles = avail > 0 ? avail / per_tile : 0;
+    if (t.ntiles == 0) t.head = std::min<int64_t>(t.head, n);
+    t.rem0 = t.head + t.ntiles * per_tile;
+    return t;
+}
+
+// Under EW_PATH_AUTO, 16-bit operands whose pointers differ in parity (2-byte
+// accesses otherwise) take the realigning bulk-copy kernel from this size on.
+constexpr int64_t kRealignAutoMinElems = int64_t(1) << 22;
+
+bool auto_realign(int e, const ew_plan &pl, int64_t n) {
+    return g_path.load(std::memory_order_relaxed) == EW_PATH_AUTO && e == 2 && pl.vec_bytes == 2 &&
+           n >= kRealignAutoMinElems;
+}
+
+ew_status run_tma_realign(int op, ew_dtype dt, const void *in0, const void *in1, void *out, int64_t n,
+                          float alpha, cudaStream_t s) {
+    const TmaEntry *ent = tma_realign_entry(op, table_dtype(dt));
+    const int e = elem_size(dt);
+    const TmaPlan tp = make_realign_plan(reinterpret_cast<uintptr_t>(out), e, n);
+    const int64_t head = tp.head, ntiles = tp.ntiles, rem0 = tp.rem0;
+    const int32_t shift0 = static_cast<int32_t>((reinterpret_cast<uintptr_t>(in0) + head * e) % 16);
+    const int32_t shift1 =
+        in1 != nullptr ? static_cast<int32_t>((reinterpret_cast<uintptr_t>(in1) + head * e) % 16) : 0;
+    TmaArgs a{in0, in1, out, n, head, ntiles, rem0, alpha, kWaitLimitNs, shift0, shift1};
+    const int grid = static_cast<int>(tma_grid(tp, n));
+    cudaError_t ce = ent->launch(a, grid, s);
+    if (ce != cudaSuccess) return cuda_fail(ce);
+    t_last.launches = 1;
+    t_last.path = EW_PATH_TMA;
+    t_last.vec_bytes = 16;
+    t_last.grid = grid;
+    t_last.block = kTmaBlock;
+    t_last.smem = ent->smem_bytes;
+    t_last.schedule = EW_SCHED_ONESHOT;
+    t_last.head = head;
+    t_last.nvec = ntiles;
+    t_last.tail = n - rem0;
     return EW_OK;
 }
 
@@ -226,8 +290,13 @@ ew_status run_stream(int op, ew_dtype dt, const void *in0, const void *in1, void
     cudaError_t ce = device_info(&dev, &sms);
     if (ce != cudaSuccess) return cuda_fail(ce);
 
-    if (path == EW_PATH_TMA && pl.vec_bytes >= 16 && tma_entry(op, table_dtype(dt)) != nullptr)
-        return run_tma(op, dt, in0, in1, out, n, alpha, make_plan(EW_PATH_V128, e, up, np, n), s);
+    if (path == EW_PATH_TMA && tma_entry(op, table_dtype(dt)) != nullptr && tma_grid_fits(n, e)) {
+        if (pl.vec_bytes >= 16)
+            return run_tma(op, dt, in0, in1, out, n, alpha, make_plan(EW_PATH_V128, e, up, np, n), s);
+        return run_tma_realign(op, dt, in0, in1, out, n, alpha, s);
+    }
+    if (auto_realign(e, pl, n) && tma_realign_entry(op, table_dtype(dt)) != nullptr && tma_grid_fits(n, e))
+        return run_tma_realign(op, dt, in0, in1, out, n, alpha, s);
 
     StreamArgs a{in0, in1, out, n, pl.head, pl.nvec, pl.head + pl.nvec * (pl.vec_bytes / e), alpha,
                  skip_unchanged ? 1 : 0};
@@ -488,9 +557,13 @@ ew_status ew_plan_query(ew_dtype dt, const void *const *ptrs, int32_t nptrs, int
     const int e = elem_size(dt);
     const int path = resolved_path();
     ew_plan pl = make_plan(path, e, up, nptrs, n);
-    if (path == EW_PATH_TMA && pl.vec_bytes >= 16) {
-        const ew_plan p16 = make_plan(EW_PATH_V128, e, up, nptrs, n);
-        const TmaPlan tp = make_tma_plan(p16, e, n);
+    if ((path == EW_PATH_TMA || auto_realign(e, pl, n)) && tma_grid_fits(n, e)) {
+        TmaPlan tp;
+        if (pl.vec_bytes >= 16) {
+            tp = make_tma_plan(make_plan(EW_PATH_V128, e, up, nptrs, n), e, n);
+        } else {  // realigning kernel: tiles follow the output, the last pointer
+            tp = make_realign_plan(up[nptrs - 1], e, n);
+        }
         pl.path = EW_PATH_TMA;
         pl.vec_bytes = 16;
         pl.head = tp.head;

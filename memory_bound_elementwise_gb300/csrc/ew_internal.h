@@ -129,6 +129,8 @@ struct TmaArgs {
     int64_t rem0;     // elements [rem0, n) one by one
     float alpha;
     uint64_t wait_limit_ns;
+    int32_t shift0;   // realigning kernel: in0 + head*E lies shift0 bytes past a 16-byte boundary
+    int32_t shift1;   // the same for in1 (the output is 16-byte aligned at element head)
 };
 using TmaLaunchFn = cudaError_t (*)(const TmaArgs &, int grid, cudaStream_t);
 struct TmaEntry {
@@ -138,6 +140,10 @@ struct TmaEntry {
 };
 // nullptr where no bulk-copy kernel exists for (op, dtype).
 const TmaEntry *tma_entry(int op, int dtype);
+// Realigning bulk-copy kernel: inputs at any element offset relative to the
+// output.  Each input tile is copied as the 16-byte aligned span around it and
+// read back at its offset in shared memory.  nullptr where none exists.
+const TmaEntry *tma_realign_entry(int op, int dtype);
 // One CTA that arms an mbarrier no copy will complete and must give up after
 // limit_ns, recording error code 99 (checks the bounded-wait path).
 cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t s);

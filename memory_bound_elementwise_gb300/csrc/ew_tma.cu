@@ -10,12 +10,14 @@
 // Latency is hidden across CTAs: many such CTAs are resident per SM and the
 // block scheduler hands out the next tiles as CTAs finish.  No multicast, no
 // clusters.  Elements before the first 16-byte aligned address and after the
-// last whole tile are done one by one by block 0.
+// last whole tile are done one per thread by extra blocks after the tile
+// blocks.
 //
 // Every mbarrier wait is bounded (%globaltimer): when it gives up the CTA
 // records an error code, lets copies already in flight land (again bounded),
 // drains its bulk stores and returns; the host reads the code with
 // ew_device_error.
+#include <atomic>
 #include <type_traits>
 
 #include "ew_internal.h"
@@ -79,6 +81,20 @@ __device__ __forceinline__ void fence_to_async_proxy() {
 }
 __device__ __forceinline__ void record_error(int32_t code) { atomicCAS(&g_device_error, 0, code); }
 
+// Blocks after the tile blocks take the elements outside the tiles, head
+// [0, head) then remainder [rem0, n), one per thread.  Returns true in those
+// blocks.
+template <class Op>
+__device__ __forceinline__ bool scalar_block(const Op &op, const TmaArgs &a, const char *in0, const char *in1,
+                                             char *out) {
+    const int64_t tile_blocks = (a.ntiles + kTmaStages - 1) / kTmaStages;
+    if (static_cast<int64_t>(blockIdx.x) < tile_blocks) return false;
+    const int64_t k = (static_cast<int64_t>(blockIdx.x) - tile_blocks) * kTmaBlock + threadIdx.x;
+    const int64_t i = k < a.head ? k : a.rem0 + (k - a.head);
+    if (i < a.n) apply_one(op, in0, in1, out, i * Op::kElem);
+    return true;
+}
+
 template <class Op> struct IsCopy : std::false_type {};
 template <int E> struct IsCopy<OpCopy<E>> : std::true_type {};
 
@@ -96,12 +112,8 @@ __global__ void __launch_bounds__(kTmaBlock) tma_kernel(const TmaArgs a) {
     const char *in1 = static_cast<const char *>(a.in1);
     char *out = static_cast<char *>(a.out);
 
-    if (blockIdx.x == 0) {  // scalar head and remainder
-        for (int64_t i = threadIdx.x; i < a.head; i += kTmaBlock) apply_one(op, in0, in1, out, i * E);
-        for (int64_t i = a.rem0 + threadIdx.x; i < a.n; i += kTmaBlock) apply_one(op, in0, in1, out, i * E);
-    }
+    if (scalar_block(op, a, in0, in1, out)) return;
     const int64_t t0 = static_cast<int64_t>(blockIdx.x) * S;
-    if (t0 >= a.ntiles) return;
     const int cnt = static_cast<int>(a.ntiles - t0 < S ? a.ntiles - t0 : S);
     const char *g0 = in0 + a.head * E;
     const char *g1 = (NIN == 2) ? in1 + a.head * E : nullptr;
@@ -151,6 +163,134 @@ __global__ void __launch_bounds__(kTmaBlock) tma_kernel(const TmaArgs a) {
     }
 }
 
+// 16 bytes of a staged input that start `shift` bytes (even, < 16) past the
+// i-th 16-byte chunk of its shared-memory buffer.  Two aligned 16-byte shared
+// loads; a select of words by shift / 4; for shift = 2 mod 4, each output word
+// joins the upper half of one word and the lower half of the next (prmt).
+__device__ __forceinline__ uint4 load_shifted(const uint4 *buf, int i, int shift) {
+    const uint4 lo = buf[i];
+    const uint4 hi = shift != 0 ? buf[i + 1] : lo;
+    const bool by8 = (shift & 8) != 0, by4 = (shift & 4) != 0;
+    const uint32_t b0 = by8 ? lo.z : lo.x, b1 = by8 ? lo.w : lo.y, b2 = by8 ? hi.x : lo.z;
+    const uint32_t b3 = by8 ? hi.y : lo.w, b4 = by8 ? hi.z : hi.x, b5 = by8 ? hi.w : hi.y;
+    const uint32_t c0 = by4 ? b1 : b0, c1 = by4 ? b2 : b1, c2 = by4 ? b3 : b2;
+    const uint32_t c3 = by4 ? b4 : b3, c4 = by4 ? b5 : b4;
+    const uint32_t sel = (shift & 2) != 0 ? 0x5432u : 0x3210u;
+    return make_uint4(__byte_perm(c0, c1, sel), __byte_perm(c1, c2, sel), __byte_perm(c2, c3, sel),
+                      __byte_perm(c3, c4, sel));
+}
+
+// Bulk-copy kernel for inputs whose offsets differ from the output's modulo
+// 16 bytes (where the aligned kernel cannot run).  The output tiles are
+// 16-byte aligned.  For each input, the 16-byte aligned span around its tile
+// (tile + 16 bytes when shift != 0) is bulk-copied to shared memory and read
+// back at the input's shift.  The host keeps at least 16 bytes of elements
+// outside the tiles at both ends, so each span lies inside its input array.
+// Results go to a separate staging buffer per stage, bulk-stored as in
+// tma_kernel.
+template <class Op>
+__global__ void __launch_bounds__(kTmaBlock) tma_realign_kernel(const TmaArgs a) {
+    enter_grid();
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int s_failed;
+    constexpr int NIN = Op::kIn, E = Op::kElem, T = kTmaTile, S = kTmaStages;
+    constexpr int TI = T + 16;                // staged input span
+    constexpr int kStage = NIN * TI + T;      // per stage: inputs, then the output tile
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + S * kStage);
+    const Op op = make_op<Op>(a.alpha);
+    const char *in0 = static_cast<const char *>(a.in0);
+    const char *in1 = static_cast<const char *>(a.in1);
+    char *out = static_cast<char *>(a.out);
+
+    if (scalar_block(op, a, in0, in1, out)) return;
+    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * S;
+    const int cnt = static_cast<int>(a.ntiles - t0 < S ? a.ntiles - t0 : S);
+    const int sh0 = a.shift0, sh1 = (NIN == 2) ? a.shift1 : 0;
+    const char *g0 = in0 + a.head * E - sh0;  // 16-byte aligned
+    const char *g1 = (NIN == 2) ? in1 + a.head * E - sh1 : nullptr;
+    char *go = out + a.head * E;
+    const uint32_t bytes0 = sh0 != 0 ? TI : T, bytes1 = sh1 != 0 ? TI : T;
+
+    if (threadIdx.x == 0) {
+        s_failed = 0;
+        for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+        mbar_init_fence();
+        for (int s = 0; s < cnt; ++s) {
+            unsigned char *st = smem + s * kStage;
+            mbar_arrive_expect_tx(&full[s], bytes0 + (NIN == 2 ? bytes1 : 0u));
+            bulk_load(st, g0 + (t0 + s) * T, bytes0, &full[s]);
+            if constexpr (NIN == 2) bulk_load(st + TI, g1 + (t0 + s) * T, bytes1, &full[s]);
+        }
+    }
+    __syncthreads();
+    int s = 0;
+    for (; s < cnt; ++s) {
+        if (threadIdx.x == 0 && !mbar_wait_bounded(&full[s], 0, a.wait_limit_ns)) {
+            s_failed = 1;
+            record_error(1);
+        }
+        __syncthreads();
+        if (s_failed) break;
+        unsigned char *st = smem + s * kStage;
+        const uint4 *x4 = reinterpret_cast<const uint4 *>(st);
+        const uint4 *y4 = reinterpret_cast<const uint4 *>(st + TI);
+        uint4 *o4 = reinterpret_cast<uint4 *>(st + NIN * TI);
+#pragma unroll 4
+        for (int i = threadIdx.x; i < T / 16; i += kTmaBlock) {
+            const uint4 x = load_shifted(x4, i, sh0);
+            const uint4 y = (NIN == 2) ? load_shifted(y4, i, sh1) : x;
+            o4[i] = make_uint4(op.word(x.x, y.x), op.word(x.y, y.y), op.word(x.z, y.z), op.word(x.w, y.w));
+        }
+        fence_to_async_proxy();
+        __syncthreads();
+        if (threadIdx.x == 0) bulk_store(go + (t0 + s) * T, o4, T);
+    }
+    if (threadIdx.x == 0) {
+        bulk_store_drain();
+        if (s_failed)  // let copies still in flight land before the CTA exits
+            for (int r = s; r < cnt; ++r) (void)mbar_wait_bounded(&full[r], 0, a.wait_limit_ns);
+    }
+}
+
+template <class Op>
+constexpr int realign_smem_bytes() {
+    return kTmaStages * (Op::kIn * (kTmaTile + 16) + kTmaTile) + kTmaStages * 8;
+}
+
+template <class Op>
+cudaError_t launch_tma_realign(const TmaArgs &a, int grid, cudaStream_t s) {
+    constexpr int smem = realign_smem_bytes<Op>();
+    // above the 48 KiB default for two-input operators: opt in once per device
+    static std::atomic<uint64_t> opted_in{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+    if ((opted_in.load(std::memory_order_acquire) & bit) == 0 || bit == 0) {
+        e = cudaFuncSetAttribute(&tma_realign_kernel<Op>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        opted_in.fetch_or(bit, std::memory_order_release);
+    }
+    return launch_kernel(&tma_realign_kernel<Op>, grid, kTmaBlock, smem, s, a);
+}
+
+template <class Op>
+constexpr TmaEntry tma_realign_entry_of() {
+    return TmaEntry{reinterpret_cast<const void *>(&tma_realign_kernel<Op>), &launch_tma_realign<Op>,
+                    realign_smem_bytes<Op>()};
+}
+
+const TmaEntry kTmaRealign[OP_COUNT][DT_COUNT] = {
+    {tma_realign_entry_of<OpAddF32>(), tma_realign_entry_of<OpAddF16>(), tma_realign_entry_of<OpAddBF16>()},
+    {tma_realign_entry_of<OpSaxpyF32>(), tma_realign_entry_of<OpSaxpyF16>(),
+     tma_realign_entry_of<OpSaxpyBF16>()},
+    {tma_realign_entry_of<OpReluF32>(), tma_realign_entry_of<OpReluF16>(), tma_realign_entry_of<OpReluBF16>()},
+    {tma_realign_entry_of<OpCopy<4>>(), tma_realign_entry_of<OpCopy<2>>(), tma_realign_entry_of<OpCopy<2>>()},
+    {tma_realign_entry_of<OpAddReluF32>(), tma_realign_entry_of<OpAddReluF16>(),
+     tma_realign_entry_of<OpAddReluBF16>()},
+    {tma_realign_entry_of<OpSelectEvenOddI32>(), TmaEntry{nullptr, nullptr, 0}, TmaEntry{nullptr, nullptr, 0}},
+};
+
 template <class Op>
 cudaError_t launch_tma(const TmaArgs &a, int grid, cudaStream_t s) {
     constexpr int smem = Op::kIn * kTmaStages * kTmaTile + kTmaStages * 8;
@@ -190,6 +330,12 @@ __global__ void wait_selftest_kernel(uint64_t limit_ns) {
 const TmaEntry *tma_entry(int op, int dtype) {
     if (op < 0 || op >= OP_COUNT || dtype < 0 || dtype >= DT_COUNT) return nullptr;
     const TmaEntry *e = &kTma[op][dtype];
+    return e->launch != nullptr ? e : nullptr;
+}
+
+const TmaEntry *tma_realign_entry(int op, int dtype) {
+    if (op < 0 || op >= OP_COUNT || dtype < 0 || dtype >= DT_COUNT) return nullptr;
+    const TmaEntry *e = &kTmaRealign[op][dtype];
     return e->launch != nullptr ? e : nullptr;
 }
 

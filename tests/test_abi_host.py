@@ -157,9 +157,32 @@ def test_plan_bulk_copy_tiles():
     p = plan(2, [P + 2, P + 2 + 4096, P + 2 + 8192], 100_000, "tma")
     assert p["path"] == 4 and p["head"] == 7
     assert p["head"] + p["nvec"] * 4096 + p["tail"] == 100_000
-    # pointers that disagree modulo 16 cannot use bulk copies
+    # pointers that disagree modulo 16: the realigning kernel's tiles follow the
+    # output (last pointer, 8 bytes past a 16-byte boundary): 2 elements reach
+    # alignment, 4 more keep a 16-byte margin before the first staged span
     p = plan(0, [P + 4, P, P + 8], 100_000, "tma")
-    assert p["path"] != 4
+    assert p == {"path": 4, "vec_bytes": 16, "head": 6, "nvec": (100_000 - 6 - 4) // 2048,
+                 "tail": 100_000 - 6 - (100_000 - 10) // 2048 * 2048}
+    # too short for a tile with both margins: everything one by one
+    p = plan(0, [P + 4, P, P + 8], 2048 + 9, "tma")
+    assert p == {"path": 4, "vec_bytes": 16, "head": 6, "nvec": 0, "tail": 2048 + 3}
+
+
+def test_plan_auto_realigns_16bit_parity_mismatch():
+    # bf16 pointers of different parity take the realigning bulk-copy kernel
+    # under AUTO from 2^22 elements; below that, 2-byte accesses
+    n = 1 << 22
+    p = plan(2, [P + 2, P, P + 6], n)
+    assert p["path"] == 4 and p["vec_bytes"] == 16
+    assert (P + 6 + p["head"] * 2) % 16 == 0 and p["head"] * 2 >= 16
+    assert p["head"] + p["nvec"] * 4096 + p["tail"] == n and p["tail"] * 2 >= 16
+    p = plan(2, [P + 2, P, P + 6], n - 1)
+    assert p["path"] == 1 and p["vec_bytes"] == 2
+    # same parity (4-byte accesses) and fp32 keep the vector kernels
+    assert plan(2, [P + 2, P + 6, P + 10], n)["path"] != 4
+    assert plan(0, [P + 4, P, P + 8], n)["path"] != 4
+    # an explicit vector path never realigns
+    assert plan(2, [P + 2, P, P + 6], n, "v256")["path"] == 1
 
 
 def test_programmatic_launch_switch():

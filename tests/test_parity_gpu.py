@@ -157,6 +157,53 @@ def test_tma_tile_boundaries(op, dtype):
             assert rec["head"] + rec["nvec"] * per_tile + rec["tail"] == n
 
 
+REALIGN_OFFSETS = {2: [[1, 0, 3], [0, 1, 0], [1, 1, 0], [3, 6, 7], [7, 0, 5], [0, 0, 1], [2, 5, 0], [0, 8, 3]],
+                   4: [[1, 0, 3], [0, 1, 0], [3, 2, 1], [0, 0, 1], [2, 0, 2]]}
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("op", ["add", "saxpy", "relu", "copy", "add_relu"])
+def test_tma_realign_mixed_offsets(op, dtype):
+    """EW_PATH_TMA with pointers that disagree modulo 16 bytes runs the
+    realigning bulk-copy kernel: 16-byte aligned output tiles, each input
+    staged as the aligned span around its tile and read at its offset.  Every
+    input shift (2-byte steps for 16-bit types), sizes around one and several
+    tiles and around the 16-byte margins kept at both ends."""
+    e = ESIZE[dtype]
+    per_tile = 8192 // e
+    m = 16 // e
+    sizes = [1, m, 2 * m, 3 * m + per_tile - 1, 3 * m + per_tile, 3 * m + per_tile + 1,
+             3 * per_tile + 7, 70001]
+    nin = 3 if op in ("add", "add_relu") else 2
+    for n in sizes:
+        for offs in REALIGN_OFFSETS[e]:
+            offs = offs[:nin]
+            rec = check_case(op, dtype, n, offs, seed=2700 + n + 7 * sum(offs), path="tma")
+            assert rec["path"] == 4
+            assert rec["head"] + rec["nvec"] * per_tile + rec["tail"] == n
+            if len({(o * e) % 16 for o in offs}) > 1:  # offsets disagree modulo 16 bytes
+                staged = 2 if op in ("add", "add_relu", "saxpy") else 1  # inputs staged per tile
+                assert rec["smem"] == 2 * (staged * (8192 + 16) + 8192) + 16, rec
+                assert rec["head"] * e >= 16 or rec["nvec"] == 0
+                assert rec["nvec"] == 0 or rec["tail"] * e >= 16
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("op", ["add", "saxpy", "relu", "copy", "add_relu"])
+def test_auto_realigns_16bit_parity_mismatch(op, dtype):
+    """Under EW_PATH_AUTO, 16-bit pointers of different parity take the
+    realigning bulk-copy kernel from n = 2^22 (2-byte accesses below)."""
+    nin = 3 if op in ("add", "add_relu") else 2
+    for n, offs in (((1 << 22) + 4099, [1, 0, 3]), ((1 << 22) + 1, [0, 1, 0]), ((1 << 22) - 1, [1, 0, 3]),
+                    ((1 << 22) + 7, [3, 6, 7])):
+        rec = check_case(op, dtype, n, offs[:nin], seed=2900 + n + sum(offs))
+        mismatch = len({o % 2 for o in offs[:nin]}) > 1
+        if n >= 1 << 22 and mismatch:
+            assert rec["path"] == 4 and rec["head"] + rec["nvec"] * 4096 + rec["tail"] == n, rec
+        else:
+            assert rec["path"] != 4, rec
+
+
 def test_bounded_wait_gives_up_and_reports():
     """The self-test block arms an mbarrier that nothing completes: its wait
     must end after the limit with code 99, and the word must read clear after."""
