@@ -112,13 +112,14 @@ typedef enum {
     EW_PATH_SCALAR = 1, /* one element per access, grid-stride */
     EW_PATH_V128 = 2,   /* 16-byte vector accesses */
     EW_PATH_V256 = 3,   /* 32-byte vector accesses (sm_100 family) */
-    EW_PATH_TMA = 4     /* bulk async copies (cp.async.bulk) through shared memory.
-                           Pointers that disagree modulo 16 bytes take a
-                           realigning kernel: each input tile is copied as the
-                           16-byte aligned span around it and read at its offset
-                           in shared memory.  EW_PATH_AUTO uses that kernel for
-                           16-bit elements whose pointers differ in parity
-                           (2-byte accesses otherwise) from n >= 2^22 */
+    EW_PATH_TMA = 4     /* bulk async copies (cp.async.bulk) through shared memory,
+                           for device memory.  Pointers that disagree modulo 16
+                           bytes take a realigning kernel: each input tile is
+                           copied as the 16-byte aligned span around it and read
+                           at its offset in shared memory.  EW_PATH_AUTO uses
+                           that kernel for 16-bit elements whose pointers differ
+                           in parity (2-byte accesses otherwise) from n >= 2^22,
+                           after checking that every pointer is device memory */
 } ew_path;
 
 /* How the body's chunks are handed to thread blocks.
@@ -231,7 +232,8 @@ EW_API ew_status ew_set_pointer_check(int enable);
  * selection (host arithmetic only; needs no GPU).  ptrs: the call's input
  * pointers, then its output pointer last; nptrs in [1, 4].  When the pointers
  * disagree modulo 16 bytes, a bulk-copy plan (EW_PATH_TMA, and EW_PATH_AUTO
- * for 16-bit elements of different parity from n >= 2^22) stages each input
+ * for 16-bit elements of different parity from n >= 2^22, where the call
+ * itself also requires device memory) stages each input
  * as the aligned span around its tile: the head then aligns the output only
  * and is at least 16 bytes, and the tail is at least 16 bytes when there is a
  * tile. */

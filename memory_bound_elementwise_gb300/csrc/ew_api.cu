@@ -188,6 +188,20 @@ ew_status check_device_pointers(const void *const *p, int np) {
     return EW_OK;
 }
 
+// True when every pointer is device memory.  AUTO sends bulk copies only
+// there: host memory reached over the CPU-GPU link keeps the vector kernels.
+bool all_device_memory(const void *const *p, int np) {
+    for (int k = 0; k < np; ++k) {
+        cudaPointerAttributes at{};
+        if (cudaPointerGetAttributes(&at, p[k]) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        if (at.type != cudaMemoryTypeDevice) return false;
+    }
+    return true;
+}
+
 int clamp_grid(int64_t blocks) {
     return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(blocks, INT_MAX)));
 }
@@ -295,7 +309,8 @@ ew_status run_stream(int op, ew_dtype dt, const void *in0, const void *in1, void
             return run_tma(op, dt, in0, in1, out, n, alpha, make_plan(EW_PATH_V128, e, up, np, n), s);
         return run_tma_realign(op, dt, in0, in1, out, n, alpha, s);
     }
-    if (auto_realign(e, pl, n) && tma_realign_entry(op, table_dtype(dt)) != nullptr && tma_grid_fits(n, e))
+    if (auto_realign(e, pl, n) && tma_realign_entry(op, table_dtype(dt)) != nullptr && tma_grid_fits(n, e) &&
+        all_device_memory(ptrs, np))
         return run_tma_realign(op, dt, in0, in1, out, n, alpha, s);
 
     StreamArgs a{in0, in1, out, n, pl.head, pl.nvec, pl.head + pl.nvec * (pl.vec_bytes / e), alpha,

@@ -204,6 +204,29 @@ def test_auto_realigns_16bit_parity_mismatch(op, dtype):
             assert rec["path"] != 4, rec
 
 
+def test_auto_realign_keeps_host_memory_on_vector_kernels():
+    """AUTO sends only device memory to the realigning bulk copy: the same
+    mixed-parity bf16 add on page-locked host buffers runs the vector kernel
+    over the CPU-GPU link, and still matches the oracle."""
+    n = (1 << 22) + 5
+    x, y = make_inputs("bf16", n + 8, 3300)
+    hx = torch.from_numpy(x.view(np.int16)).pin_memory()
+    hy = torch.from_numpy(y.view(np.int16)).pin_memory()
+    hz = torch.zeros(n + 8, dtype=torch.int16).pin_memory()
+    assert ew.lib().ew_add(2, hx.data_ptr() + 2, hy.data_ptr(), hz.data_ptr() + 6, n, _stream()) == 0
+    rec = ew.last_launch()
+    assert rec["path"] != 4 and rec["vec_bytes"] == 2, rec
+    torch.cuda.synchronize()
+    got = hz.numpy().view(np.uint16)[3:3 + n]
+    assert_bits_equal(got, oracle.add("bf16", x[1:1 + n], y[:n]), "bf16", True, "host mixed parity")
+    # device copies of the same arrays take the realigning kernel
+    dx, dy, dz = hx.cuda(), hy.cuda(), hz.cuda()
+    assert ew.lib().ew_add(2, dx.data_ptr() + 2, dy.data_ptr(), dz.data_ptr() + 6, n, _stream()) == 0
+    assert ew.last_launch()["path"] == 4
+    torch.cuda.synchronize()
+    assert_bits_equal(dz.cpu().numpy().view(np.uint16)[3:3 + n], got, "bf16", True, "device mixed parity")
+
+
 def test_bounded_wait_gives_up_and_reports():
     """The self-test block arms an mbarrier that nothing completes: its wait
     must end after the limit with code 99, and the word must read clear after."""

@@ -47,12 +47,13 @@ def test_plan_partitions_and_aligns(dt, n, offsets, path):
             # 16 bytes stay outside the tiles at both ends
             assert (ptrs[-1] + p["head"] * e) % 16 == 0
             assert p["head"] * e >= 16 and p["tail"] * e >= 16
+            assert p["tail"] < per + 16 // e  # less than a tile beyond the end margin
         else:
             # every pointer reaches the vector boundary at the same element
             align = 16 if p["path"] == 4 else vb
             for q in ptrs:
                 assert (q + p["head"] * e) % align == 0
-        assert p["tail"] < per
+            assert p["tail"] < per
     # the width is the widest the pointers share
     if p["path"] != 4 and vb < (CAP[path] or e):
         w = vb * 2
