@@ -119,7 +119,8 @@ typedef enum {
                            at its offset in shared memory.  EW_PATH_AUTO uses
                            that kernel for 16-bit elements whose pointers differ
                            in parity (2-byte accesses otherwise) from n >= 2^22,
-                           after checking that every pointer is device memory */
+                           after checking that every pointer is device memory;
+                           during stream capture it keeps the vector kernel */
 } ew_path;
 
 /* How the body's chunks are handed to thread blocks.

@@ -188,6 +188,18 @@ ew_status check_device_pointers(const void *const *p, int np) {
     return EW_OK;
 }
 
+// True while s is being captured into a CUDA graph, or when that cannot be
+// told.  AUTO then keeps the vector kernels rather than query pointers inside
+// a capture.
+bool stream_capturing(cudaStream_t s) {
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &st) != cudaSuccess) {
+        cudaGetLastError();
+        return true;
+    }
+    return st != cudaStreamCaptureStatusNone;
+}
+
 // True when every pointer is device memory.  AUTO sends bulk copies only
 // there: host memory reached over the CPU-GPU link keeps the vector kernels.
 bool all_device_memory(const void *const *p, int np) {
@@ -310,7 +322,7 @@ ew_status run_stream(int op, ew_dtype dt, const void *in0, const void *in1, void
         return run_tma_realign(op, dt, in0, in1, out, n, alpha, s);
     }
     if (auto_realign(e, pl, n) && tma_realign_entry(op, table_dtype(dt)) != nullptr && tma_grid_fits(n, e) &&
-        all_device_memory(ptrs, np))
+        !stream_capturing(s) && all_device_memory(ptrs, np))
         return run_tma_realign(op, dt, in0, in1, out, n, alpha, s);
 
     StreamArgs a{in0, in1, out, n, pl.head, pl.nvec, pl.head + pl.nvec * (pl.vec_bytes / e), alpha,
@@ -629,6 +641,6 @@ ew_status ew_selftest_bounded_wait(int64_t limit_ns, ew_stream_t s) {
     return EW_OK;
 }
 
-int ew_version(void) { return 500; }
+int ew_version(void) { return 600; }
 
 }  // extern "C"

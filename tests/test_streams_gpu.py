@@ -113,6 +113,37 @@ def test_cuda_graph_capture_and_replay(path):
     assert ew.device_error() == (0, 0)
 
 
+def test_graph_capture_of_mixed_parity_bf16_add():
+    """A 16-bit add with pointers of different parity, captured into a graph:
+    inside the capture AUTO keeps the vector kernel (no pointer queries while
+    capturing); eager calls on the same buffers take the realigning bulk copy.
+    Both give the oracle's bits."""
+    n = (1 << 22) + 3
+    x = inputs.as_dtype(inputs.normal(n + 8, 720), "bf16")
+    y = inputs.as_dtype(inputs.normal(n + 8, 721), "bf16")
+    tx = torch.from_numpy(x.view(np.int16)).cuda()
+    ty = torch.from_numpy(y.view(np.int16)).cuda()
+    tz = torch.zeros(n + 8, dtype=torch.int16, device="cuda")
+    L = ew.lib()
+    want = oracle.add("bf16", x[1:1 + n], y[:n])
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        assert L.ew_add(2, tx.data_ptr() + 2, ty.data_ptr(), tz.data_ptr() + 6, n, s.cuda_stream) == 0
+        rec = ew.last_launch()
+    assert rec["path"] != 4 and rec["vec_bytes"] == 2, rec
+    g.replay()
+    torch.cuda.synchronize()
+    assert_bits_equal(tz.cpu().numpy().view(np.uint16)[3:3 + n], want, "bf16", True, "captured mixed parity")
+    tz.zero_()
+    assert L.ew_add(2, tx.data_ptr() + 2, ty.data_ptr(), tz.data_ptr() + 6, n,
+                    torch.cuda.current_stream().cuda_stream) == 0
+    assert ew.last_launch()["path"] == 4
+    torch.cuda.synchronize()
+    assert_bits_equal(tz.cpu().numpy().view(np.uint16)[3:3 + n], want, "bf16", True, "eager mixed parity")
+
+
 def test_bf16_tensor_views_with_offsets():
     """Binding on sliced views: data_ptr carries the element offset."""
     n = 1 << 20
