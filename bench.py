@@ -87,6 +87,7 @@ PROFILE_CASES = {
     "select_i32": ("select", "f32", 0),
     "gather2_span_f32": ("gather_span", "f32", 0),
     "add_bf16_mixed": ("add", "bf16", (1, 0, 3)),
+    "gather16_f32": ("gather16", "f32", 0),
 }
 
 
@@ -126,7 +127,8 @@ def run_profile_case(args):
             "add_relu": lambda: L.ew_add_relu(code, px, py, pz, n, s),
             "relu_inplace": lambda: L.ew_relu(code, px, px, n, s),
             "select": lambda: L.ew_select_even_odd(3, px, pz, n, s),
-            "gather_span": lambda: L.ew_gather_stride(code, px, pz, n, 2, s)}[op]
+            "gather_span": lambda: L.ew_gather_stride(code, px, pz, n, 2, s),
+            "gather16": lambda: L.ew_gather_stride(code, px, pz, n, 16, s)}[op]
     if op == "gather_span":
         ew.set_path("v256")
     for _ in range(args.warmup + args.steps):
@@ -464,6 +466,12 @@ def aux_measurements(torch, ew, inputs, metrics, stream, peak, dev):
            lambda: L.ew_gather_stride(0, px, py, n26, 2, s), steps=100)
     record("gather4_f32_2p26", "gather", "f32", n26,
            lambda: L.ew_gather_stride(0, px, py, n26, 4, s), steps=100)
+    # stride 16: every lane's load is its own sector; the default is the tiled kernel
+    record("gather16_f32_2p26", "gather", "f32", n26,
+           lambda: L.ew_gather_stride(0, px, py, n26, 16, s), steps=100)
+    ew.set_schedule("laps")
+    record("gather16_f32_2p26_lap_order", "gather", "f32", n26,
+           lambda: L.ew_gather_stride(0, px, py, n26, 16, s), steps=100)
     # index order (one block per 1024 consecutive outputs): once the input no
     # longer fits in L2, each lap fetches it from DRAM again
     ew.set_schedule("oneshot")
@@ -471,6 +479,8 @@ def aux_measurements(torch, ew, inputs, metrics, stream, peak, dev):
            lambda: L.ew_gather_stride(0, px, py, n26, 2, s), steps=100)
     record("gather4_f32_2p26_index_order", "gather", "f32", n26,
            lambda: L.ew_gather_stride(0, px, py, n26, 4, s), steps=100)
+    record("gather16_f32_2p26_index_order", "gather", "f32", n26,
+           lambda: L.ew_gather_stride(0, px, py, n26, 16, s), steps=100)
     ew.set_schedule("auto")
     ew.set_path("v256")  # span variant: contiguous 256-bit source spans, lane select
     record("gather2_f32_2p26_span", "gather", "f32", n26,

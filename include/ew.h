@@ -139,13 +139,23 @@ typedef enum {
  *                     from DRAM once.  It applies when 2 <= s <= 64,
  *                     n <= 2^32 and n >= 2048 s; otherwise EW_SCHED_ONESHOT
  *                     runs.
- * EW_SCHED_AUTO       EW_SCHED_LAPS for the gather, EW_SCHED_ONESHOT for the
- *                     rest.  A gather with n > 2^32 always runs persistent. */
+ * EW_SCHED_TILED      gather only, same range of s and n as EW_SCHED_LAPS (any
+ *                     n >= 1 there): the transpose-like schedule.  A block
+ *                     reads the contiguous input span that its positions of
+ *                     all s laps draw from (32 KiB) once, coalesced, into
+ *                     shared memory with one row per residue mod s, then
+ *                     writes each lap's outputs as one coalesced run.
+ * EW_SCHED_AUTO       for the gather: EW_SCHED_LAPS while s < 32 / (element
+ *                     size), where a warp's strided load still shares 32-byte
+ *                     sectors; EW_SCHED_TILED from there up to s = 64.  For
+ *                     the other operators, EW_SCHED_ONESHOT.  A gather with
+ *                     n > 2^32 always runs persistent. */
 typedef enum {
     EW_SCHED_AUTO = 0,
     EW_SCHED_ONESHOT = 1,
     EW_SCHED_PERSISTENT = 2,
-    EW_SCHED_LAPS = 3
+    EW_SCHED_LAPS = 3,
+    EW_SCHED_TILED = 4
 } ew_schedule;
 
 /* ---- operators ------------------------------------------------------- */
@@ -186,8 +196,9 @@ EW_API ew_status ew_copy(ew_dtype dtype, const void *in, void *out, int64_t n, e
  * without overflow.  stride >= 1 (else EW_ERR_INVALID_VALUE).  in and out must
  * not overlap.  As in the page's non-coalesced copy, each thread reads one
  * element per access, so a warp's load touches every stride-th element of a
- * span while its store covers consecutive elements.  The order in which
- * blocks take the outputs follows ew_set_schedule (EW_SCHED_LAPS by default).
+ * span while its store covers consecutive elements (except under
+ * EW_SCHED_TILED, which stages the input through shared memory).  The order
+ * in which blocks take the outputs follows ew_set_schedule.
  * With ew_set_path
  * (EW_PATH_V256) selected, 4-byte elements with (stride mod n) of 2 or 4 and
  * n <= 2^32 use a span variant instead: each thread loads the contiguous

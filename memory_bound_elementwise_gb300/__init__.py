@@ -34,9 +34,9 @@ PATH_AUTO, PATH_SCALAR, PATH_V128, PATH_V256, PATH_TMA = 0, 1, 2, 3, 4
 PATH_NAMES = {PATH_AUTO: "auto", PATH_SCALAR: "scalar", PATH_V128: "v128",
               PATH_V256: "v256", PATH_TMA: "tma"}
 # ew_schedule
-SCHED_AUTO, SCHED_ONESHOT, SCHED_PERSISTENT, SCHED_LAPS = 0, 1, 2, 3
+SCHED_AUTO, SCHED_ONESHOT, SCHED_PERSISTENT, SCHED_LAPS, SCHED_TILED = 0, 1, 2, 3, 4
 SCHED_NAMES = {SCHED_AUTO: "auto", SCHED_ONESHOT: "oneshot", SCHED_PERSISTENT: "persistent",
-               SCHED_LAPS: "laps"}
+               SCHED_LAPS: "laps", SCHED_TILED: "tiled"}
 # ew_status
 EW_OK = 0
 STATUS_NAMES = {0: "EW_OK", 1: "EW_ERR_INVALID_VALUE", 2: "EW_ERR_NULL_POINTER",
@@ -245,8 +245,9 @@ def get_path():
 
 
 def set_schedule(schedule):
-    """Select the block schedule: 'auto', 'oneshot', 'persistent' or 'laps'
-    (the gather's lap order; the other operators run 'oneshot' under it)."""
+    """Select the block schedule: 'auto', 'oneshot', 'persistent', 'laps' or
+    'tiled' (the gather's lap order and its transposing tiles; the other
+    operators run 'oneshot' under those two)."""
     code = ({v: k for k, v in SCHED_NAMES.items()}[schedule] if isinstance(schedule, str)
             else int(schedule))
     check(lib().ew_set_schedule(code), "ew_set_schedule")

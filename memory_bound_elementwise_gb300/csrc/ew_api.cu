@@ -13,6 +13,7 @@
 // per SM from the occupancy API (CUDA-MODE lecture notes §4.4), each block
 // striding over the chunks.
 #include <algorithm>
+#include <array>
 #include <atomic>
 #include <climits>
 #include <cstdlib>
@@ -93,7 +94,7 @@ int resolved_path() {
 // schedule of the streaming kernels (lap order exists for the gather only)
 int resolved_schedule() {
     const int s = g_schedule.load(std::memory_order_relaxed);
-    return (s == EW_SCHED_AUTO || s == EW_SCHED_LAPS) ? EW_SCHED_ONESHOT : s;
+    return (s == EW_SCHED_AUTO || s == EW_SCHED_LAPS || s == EW_SCHED_TILED) ? EW_SCHED_ONESHOT : s;
 }
 
 // Bulk-copy split: 16-byte aligned head, whole tiles, then the remainder.
@@ -212,6 +213,46 @@ bool all_device_memory(const void *const *p, int np) {
         if (at.type != cudaMemoryTypeDevice) return false;
     }
     return true;
+}
+
+// Row padding, in 4-byte words, of the tiled gather's shared-memory tile.  A
+// warp writes 32 consecutive input elements j to row j mod s, column j / s;
+// with rows a multiple of 32 words plus w apart, element j lands in bank
+// ((j mod s) * w + word of j / s) mod 32.  Chosen once per (s, element size):
+// the w in [1, 32) that puts the fewest distinct words in any bank (one for
+// every s except even s below 32 that are not powers of two, which get two).
+uint32_t tiled_pad_words(uint32_t s, int e) {
+    static const std::array<std::array<uint8_t, kMaxLaps + 1>, 2> table = [] {
+        std::array<std::array<uint8_t, kMaxLaps + 1>, 2> t{};
+        for (int k = 0; k < 2; ++k) {
+            const uint32_t elems_per_word = k == 0 ? 1 : 2;  // 4-byte, 2-byte elements
+            for (uint32_t sv = 2; sv <= kMaxLaps; ++sv) {
+                uint32_t best_w = 1, best = 33;
+                for (uint32_t w = 1; w < 32; ++w) {
+                    // distinct words per bank; rows are 64 * 32 words (a multiple of 32) plus w apart
+                    uint32_t words[32], nw = 0, per_bank[32] = {};
+                    for (uint32_t j = 0; j < 32; ++j) {
+                        const uint32_t word = (j % sv) * (2048 + w) + (j / sv) / elems_per_word;
+                        bool seen = false;
+                        for (uint32_t q = 0; q < nw; ++q) seen = seen || words[q] == word;
+                        if (!seen) {
+                            words[nw++] = word;
+                            ++per_bank[word % 32];
+                        }
+                    }
+                    uint32_t worst = 0;
+                    for (uint32_t b = 0; b < 32; ++b) worst = std::max(worst, per_bank[b]);
+                    if (worst < best) {
+                        best = worst;
+                        best_w = w;
+                    }
+                }
+                t[k][sv] = static_cast<uint8_t>(best_w);
+            }
+        }
+        return t;
+    }();
+    return table[e == 2 ? 1 : 0][s];
 }
 
 int clamp_grid(int64_t blocks) {
@@ -475,7 +516,7 @@ ew_status ew_gather_stride(ew_dtype dt, const void *in, void *out, int64_t n, in
     if (resolved_path() == EW_PATH_V256 && g_path.load(std::memory_order_relaxed) != EW_PATH_AUTO &&
         elem_size(dt) == 4 && (s_mod == 2 || s_mod == 4) && un <= (uint64_t(1) << 32)) {
         const GatherEntry *g = gather_span_4(static_cast<int64_t>(s_mod));
-        GatherArgs ga{in, out, un, s_mod, 0, ~uint64_t(0) / un, 0, 0, 0, 0, 0, 0};
+        GatherArgs ga{in, out, un, s_mod, 0, ~uint64_t(0) / un, 0, 0, 0, 0, 0, 0, 0, 0, 0};
         const uintptr_t o = reinterpret_cast<uintptr_t>(out);
         ga.head = std::min<int64_t>(static_cast<int64_t>(((32 - o % 32) % 32) / 4), n);
         ga.nvec = (n - ga.head) / 8;
@@ -496,8 +537,41 @@ ew_status ew_gather_stride(ew_dtype dt, const void *in, void *out, int64_t n, in
         return EW_OK;
     }
     const bool oneshot = sched != EW_SCHED_PERSISTENT && un <= (uint64_t(1) << 32);
+    const bool small_stride = s_mod >= 2 && s_mod <= kMaxLaps;
+    // AUTO: lap order while a warp's strided load still shares 32-byte
+    // sectors (s < 32 / E); from there on every lane's load is its own sector,
+    // L2 traffic bounds lap order, and the tiled kernel takes over
+    const bool tiled = sched == EW_SCHED_TILED ||
+                       (sched == EW_SCHED_AUTO && s_mod >= static_cast<uint64_t>(32 / elem_size(dt)));
+    if (oneshot && small_stride && tiled) {
+        const int e = elem_size(dt);
+        const GatherEntry *gt = e == 4 ? gather_tiled_4() : gather_tiled_2();
+        GatherArgs ga{in, out, un, s_mod, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+        const uint32_t per_block = (kTiledSpanBytes / e) / static_cast<uint32_t>(s_mod);
+        uint32_t log2p = 0;
+        while ((2u << log2p) <= per_block) ++log2p;  // largest power of two <= per_block
+        ga.tile_p = 1u << log2p;
+        ga.tile_log2p = log2p;
+        ga.tile_pitch = ga.tile_p + tiled_pad_words(static_cast<uint32_t>(s_mod), e) * (4 / e);
+        ga.lap_q = static_cast<uint32_t>(un / s_mod);
+        ga.lap_m = static_cast<uint32_t>(un % s_mod);
+        ga.div_magic = static_cast<uint32_t>((uint64_t(1) << 32) / s_mod + 1);
+        const uint64_t lap_len = (un + s_mod - 1) / s_mod;
+        const int grid = clamp_grid(static_cast<int64_t>((lap_len + ga.tile_p - 1) / ga.tile_p));
+        ce = gt->launch(ga, grid, reinterpret_cast<cudaStream_t>(s));
+        if (ce != cudaSuccess) return cuda_fail(ce);
+        t_last.launches = 1;
+        t_last.path = EW_PATH_SCALAR;
+        t_last.vec_bytes = e;
+        t_last.grid = grid;
+        t_last.block = kBlock;
+        t_last.smem = static_cast<int32_t>(s_mod * ga.tile_pitch * e);
+        t_last.schedule = EW_SCHED_TILED;
+        t_last.nvec = n;
+        return EW_OK;
+    }
     const bool lap_order = oneshot && sched != EW_SCHED_ONESHOT;
-    GatherArgs ga{in, out, un, s_mod, 0, 0, 0, 0, 0, 0, 0, 0};
+    GatherArgs ga{in, out, un, s_mod, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
     const GatherEntry *g;
     int grid;
     const bool four = elem_size(dt) == 4;
@@ -551,7 +625,7 @@ ew_path ew_get_path(void) { return static_cast<ew_path>(g_path.load(std::memory_
 
 ew_status ew_set_schedule(ew_schedule sched) {
     const int v = static_cast<int>(sched);
-    if (v < EW_SCHED_AUTO || v > EW_SCHED_LAPS) return EW_ERR_INVALID_VALUE;
+    if (v < EW_SCHED_AUTO || v > EW_SCHED_TILED) return EW_ERR_INVALID_VALUE;
     g_schedule.store(v, std::memory_order_relaxed);
     return EW_OK;
 }

@@ -91,7 +91,10 @@ struct GatherArgs {
     int64_t tail0;       // span kernel: outputs [tail0, n) one by one
     uint32_t lap_q;      // lap kernel: n / s_mod
     uint32_t lap_m;      // lap kernel: n mod s_mod
-    uint32_t div_magic;  // lap kernel: floor(2^32 / s_mod) + 1
+    uint32_t div_magic;  // lap and tiled kernels: floor(2^32 / s_mod) + 1
+    uint32_t tile_p;     // tiled kernel: lap positions per block (a power of two)
+    uint32_t tile_log2p; // log2(tile_p)
+    uint32_t tile_pitch; // elements per shared-memory row (tile_p plus bank padding)
 };
 using GatherLaunchFn = cudaError_t (*)(const GatherArgs &, int grid, cudaStream_t);
 struct GatherEntry {
@@ -104,6 +107,11 @@ struct GatherEntry {
 constexpr uint64_t kMaxLaps = 64;
 const GatherEntry *gather_laps_4();
 const GatherEntry *gather_laps_2();
+// Tiled (transposing) gather: same range as the lap kernel; a block stages
+// kTiledSpanBytes of input in shared memory.
+constexpr uint32_t kTiledSpanBytes = 32768;
+const GatherEntry *gather_tiled_4();
+const GatherEntry *gather_tiled_2();
 const GatherEntry *gather_oneshot_4();  // binary32, n <= 2^32
 const GatherEntry *gather_stride_4();   // binary32, any n
 const GatherEntry *gather_oneshot_2();  // 16-bit types

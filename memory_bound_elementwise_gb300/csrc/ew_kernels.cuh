@@ -18,6 +18,9 @@
 // (the "persistent" schedule) walks the same chunks with a grid stride.
 #pragma once
 
+#include <cstring>
+#include <type_traits>
+
 #include "ew_device.cuh"
 #include "ew_internal.h"
 
@@ -199,6 +202,106 @@ __global__ void __launch_bounds__(kBlock) gather_laps_kernel(const GatherArgs g)
         if (p0 + u * kBlock < len) st<E>(out + static_cast<size_t>(i0 + u * kBlock) * E, v[u]);
 }
 
+// Tiled gather for a small stride (2 <= s <= kMaxLaps, n <= 2^32): the
+// transpose-like schedule.  Block b owns positions [b*P, (b+1)*P) of every
+// lap.  Their sources r_L + s*p fill the input span [s*b*P, s*(b+1)*P),
+// clipped at n, which the block reads once, coalesced (16-byte loads when the
+// span is 16-byte aligned).  It writes the span to shared memory transposed:
+// element j goes to row j mod s, column j / s.  Row r then holds, in position
+// order, the sources of every lap with r_L = r, so each lap's outputs leave as
+// one coalesced run.  Rows are padded so that a warp's 32 consecutive
+// elements spread over the banks.  Unlike the lap kernel, every input element
+// is loaded once per block, whether one lap, several or none use it.
+template <int E, int U>
+__global__ void __launch_bounds__(kBlock) gather_tiled_kernel(const GatherArgs g) {
+    enter_grid();
+    using W = typename std::conditional<E == 4, uint32_t, uint16_t>::type;
+    constexpr uint32_t kPerVec = 16 / E;
+    extern __shared__ __align__(16) unsigned char tile_raw[];
+    W *tile = reinterpret_cast<W *>(tile_raw);
+    __shared__ uint32_t lap_start[kMaxLaps], lap_len[kMaxLaps], lap_row[kMaxLaps];
+    W *out = static_cast<W *>(g.out);
+    const uint32_t s = static_cast<uint32_t>(g.s_mod);
+    const uint32_t P = g.tile_p, pitch = g.tile_pitch;
+    const uint32_t p0 = blockIdx.x * P;
+    if (threadIdx.x < s) {  // lap L: first output, length, offset of its source row
+        const uint32_t L = threadIdx.x;
+        const uint32_t a0 = L * g.lap_m;
+        const uint32_t c0 = div_by_s(a0 + s - 1, s, g.div_magic);  // ceil(L*m/s)
+        const uint32_t c1 = div_by_s(a0 + g.lap_m + s - 1, s, g.div_magic);
+        lap_start[L] = L * g.lap_q + c0;
+        lap_len[L] = g.lap_q + (c1 - c0);
+        lap_row[L] = (c0 * s - a0) * pitch;
+    }
+    const uint64_t j0 = static_cast<uint64_t>(s) * p0;  // first source of the span
+    const uint32_t span = s * P;
+    const uint32_t avail = g.n - j0 < span ? static_cast<uint32_t>(g.n - j0) : span;
+    const W *src = static_cast<const W *>(g.in) + j0;
+    uint32_t done = 0;  // leading span elements staged by vector loads
+    if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+        const uint4 *src4 = reinterpret_cast<const uint4 *>(src);
+        const uint32_t nv = avail / kPerVec;
+        for (uint32_t base = 0; base < nv; base += U * kBlock) {
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const uint32_t vi = base + u * kBlock + threadIdx.x;
+                if (vi < nv) v[u] = src4[vi];
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const uint32_t vi = base + u * kBlock + threadIdx.x;
+                if (vi >= nv) continue;
+                const uint32_t j = vi * kPerVec;
+                const uint32_t c = div_by_s(j, s, g.div_magic);
+                uint32_t r = j - c * s;
+                uint32_t at = r * pitch + c;  // tile slot of element j
+                W w[kPerVec];
+                memcpy(w, &v[u], 16);
+#pragma unroll
+                for (uint32_t k = 0; k < kPerVec; ++k) {
+                    tile[at] = w[k];
+                    if (++r == s) {  // next column, row 0
+                        r = 0;
+                        at = at + 1 - (s - 1) * pitch;
+                    } else {
+                        at += pitch;
+                    }
+                }
+            }
+        }
+        done = nv * kPerVec;
+    }
+    for (uint32_t base = done; base < avail; base += 8 * kBlock) {  // unaligned span, ragged end
+        W v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const uint32_t j = base + u * kBlock + threadIdx.x;
+            if (j < avail) v[u] = src[j];
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const uint32_t j = base + u * kBlock + threadIdx.x;
+            if (j < avail) {
+                const uint32_t c = div_by_s(j, s, g.div_magic);
+                tile[(j - c * s) * pitch + c] = v[u];
+            }
+        }
+    }
+    __syncthreads();
+    uint32_t cur = ~0u, first = 0, len = 0, row = 0;
+    for (uint32_t k = threadIdx.x; k < span; k += kBlock) {
+        const uint32_t L = k >> g.tile_log2p, q = k & (P - 1);
+        if (L != cur) {  // warp-uniform: P >= 32
+            cur = L;
+            first = lap_start[L] + p0;
+            len = lap_len[L] > p0 ? lap_len[L] - p0 : 0;
+            row = lap_row[L];
+        }
+        if (q < len) out[static_cast<size_t>(first + q)] = tile[row + q];
+    }
+}
+
 // Grid-stride gather for any n: with i = v + k*T (T = grid threads),
 // (s*i) mod n advances by (s*T) mod n per slot, so each thread needs one
 // modular product and then conditional subtractions.
@@ -306,6 +409,11 @@ cudaError_t launch_gather_oneshot(const GatherArgs &g, int grid, cudaStream_t s)
 template <int E, int U>
 cudaError_t launch_gather_laps(const GatherArgs &g, int grid, cudaStream_t s) {
     return launch_kernel(&gather_laps_kernel<E, U>, grid, kBlock, 0, s, g);
+}
+template <int E, int U>
+cudaError_t launch_gather_tiled(const GatherArgs &g, int grid, cudaStream_t s) {
+    const size_t smem = static_cast<size_t>(g.s_mod) * g.tile_pitch * E;
+    return launch_kernel(&gather_tiled_kernel<E, U>, grid, kBlock, smem, s, g);
 }
 template <int E, int U>
 cudaError_t launch_gather_stride(const GatherArgs &g, int grid, cudaStream_t s) {

@@ -30,12 +30,16 @@ const GatherEntry kGatherStride{reinterpret_cast<const void *>(&gather_stride_ke
 constexpr int kGatherLapsUnroll = 8;
 const GatherEntry kGatherLaps{reinterpret_cast<const void *>(&gather_laps_kernel<2, kGatherLapsUnroll>),
                               &launch_gather_laps<2, kGatherLapsUnroll>, kGatherLapsUnroll};
+constexpr int kGatherTiledUnroll = 2;  // 16-byte loads in flight per thread per batch
+const GatherEntry kGatherTiled{reinterpret_cast<const void *>(&gather_tiled_kernel<2, kGatherTiledUnroll>),
+                               &launch_gather_tiled<2, kGatherTiledUnroll>, kGatherTiledUnroll};
 }  // namespace
 
 const StreamEntry *stream_table_f16() { return &kTable[0][0]; }
 
 const GatherEntry *gather_oneshot_2() { return &kGatherOneshot; }
 const GatherEntry *gather_laps_2() { return &kGatherLaps; }
+const GatherEntry *gather_tiled_2() { return &kGatherTiled; }
 const GatherEntry *gather_stride_2() { return &kGatherStride; }
 
 }  // namespace ew

@@ -30,6 +30,9 @@ const GatherEntry kGatherStride{reinterpret_cast<const void *>(&gather_stride_ke
 constexpr int kGatherLapsUnroll = 8;
 const GatherEntry kGatherLaps{reinterpret_cast<const void *>(&gather_laps_kernel<4, kGatherLapsUnroll>),
                               &launch_gather_laps<4, kGatherLapsUnroll>, kGatherLapsUnroll};
+constexpr int kGatherTiledUnroll = 2;  // 16-byte loads in flight per thread per batch
+const GatherEntry kGatherTiled{reinterpret_cast<const void *>(&gather_tiled_kernel<4, kGatherTiledUnroll>),
+                               &launch_gather_tiled<4, kGatherTiledUnroll>, kGatherTiledUnroll};
 }  // namespace
 
 const StreamEntry *stream_table_f32() { return &kTable[0][0]; }
@@ -45,6 +48,7 @@ const GatherEntry *gather_span_4(int64_t stride) {
 }
 const GatherEntry *gather_oneshot_4() { return &kGatherOneshot; }
 const GatherEntry *gather_laps_4() { return &kGatherLaps; }
+const GatherEntry *gather_tiled_4() { return &kGatherTiled; }
 const GatherEntry *gather_stride_4() { return &kGatherStride; }
 
 }  // namespace ew

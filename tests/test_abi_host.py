@@ -90,7 +90,7 @@ def test_argument_errors_are_caught_on_the_host():
     assert L.ew_set_path(9) == INVALID
     assert L.ew_set_path(-1) == INVALID
     assert L.ew_set_pointer_check(2) == INVALID
-    assert L.ew_set_schedule(4) == INVALID
+    assert L.ew_set_schedule(5) == INVALID
     assert L.ew_set_schedule(-1) == INVALID
     assert L.ew_selftest_bounded_wait(0, None) == INVALID
     assert L.ew_selftest_bounded_wait(10 ** 11, None) == INVALID
@@ -197,7 +197,7 @@ def test_programmatic_launch_switch():
 
 
 def test_schedule_roundtrip():
-    for name in ("oneshot", "persistent", "laps", "auto"):
+    for name in ("oneshot", "persistent", "laps", "tiled", "auto"):
         ew.set_schedule(name)
         assert ew.get_schedule() == name
 

@@ -249,9 +249,20 @@ LAP_BLOCK = 2048  # outputs per block of the lap-ordered gather (256 threads x 8
 
 
 def _gather_laps(n, s):
-    """Whether ew_gather_stride takes the lap-ordered kernel (schedule 'laps' or 'auto')."""
+    """Whether ew_gather_stride takes the lap-ordered kernel under schedule 'laps'."""
     sm = s % n
     return 2 <= sm <= 64 and n <= 1 << 32 and n // sm >= LAP_BLOCK
+
+
+def _gather_auto_schedule(n, s, dtype):
+    """The schedule AUTO picks: tiled from s = 32 / element size up to 64,
+    lap order below it where every lap holds a block, else index order."""
+    sm = s % n
+    if n > 1 << 32:
+        return 2
+    if 32 // ESIZE[dtype] <= sm <= 64:
+        return 4
+    return 3 if _gather_laps(n, s) else 1
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -269,6 +280,8 @@ def test_gather_schedules_agree(dtype):
                 rec = ew.last_launch()
                 if sched == "persistent":
                     assert rec["schedule"] == 2
+                elif sched == "auto":
+                    assert rec["schedule"] == _gather_auto_schedule(n, s, dtype), (n, s, rec)
                 elif sched == "oneshot" or not _gather_laps(n, s):
                     assert rec["schedule"] == 1
                 else:
@@ -423,13 +436,13 @@ def test_gather_small(dtype):
 
 @pytest.mark.parametrize("dtype", ["f32", "f16"])
 def test_gather_lap_order(dtype):
-    """The lap-ordered gather (the default for strides 2..64 once every lap
-    holds a block of outputs): sizes at, just below and just above the
+    """The lap-ordered gather (schedule 'laps'; AUTO's choice below s = 32 / E)
+    for strides 2..64 once every lap holds a block of outputs: sizes at, just below and just above the
     threshold n = 2048 s, laps of unequal length (s not dividing n), laps that
     read the same sources (s | n) and laps on distinct residues (s coprime to
     n), stride 65 and strides above n, misaligned input and output."""
     L = ew.lib()
-    ew.set_schedule("auto")
+    ew.set_schedule("laps")
     cases = []
     for s in (2, 3, 4, 5, 7, 8, 16, 31, 33, 64, 65):
         for n in (LAP_BLOCK * s - 1, LAP_BLOCK * s, LAP_BLOCK * s + 1, 3 * LAP_BLOCK * s + 5, 200_003):
@@ -665,9 +678,34 @@ def test_gather_beyond_2p32_elements_f16():
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+def test_gather_tiled(dtype):
+    """The tiled (transposing) gather for strides 2..64: strides that divide n
+    (laps share one residue row), that are coprime to n (every row used once),
+    even strides whose padded rows still share banks, ragged last blocks and
+    n just above s.  Stride 65 and strides above n fall back to index order."""
+    L = ew.lib()
+    ew.set_schedule("tiled")
+    for s in (2, 3, 4, 5, 6, 7, 8, 12, 16, 31, 33, 64, 65, (1 << 40) + 6):
+        for n, in_off in ((s % (1 << 20) + 1, 0), (1000, 1), (8191, 0), (70001, 1), (300_007, 0),
+                          (1 << 18, 1), ((1 << 18) + 3, 0)):
+            x = inputs.random_bits(n, dtype, 7100 + n + s % 1000)
+            bi = GuardedBuffer(n, dtype, in_off).fill(x)  # offset 0: 16-byte loads
+            bo = GuardedBuffer(n, dtype, 3)
+            assert L.ew_gather_stride(DT_CODE[dtype], bi.view.data_ptr(), bo.view.data_ptr(),
+                                      n, s, _stream()) == 0
+            rec = ew.last_launch()
+            assert rec["schedule"] == (4 if 2 <= s % n <= 64 else 1), (n, s, rec)
+            torch.cuda.synchronize()
+            assert_bits_equal(bo.host(), oracle.gather_stride(x, s), dtype, False,
+                              "tiled gather n=%d s=%d" % (n, s))
+            assert bi.guards_intact() and bo.guards_intact()
+
+
+@pytest.mark.parametrize("schedule", ["laps", "tiled"])
 @pytest.mark.parametrize("n,s", [(1 << 32, 2), ((1 << 32) - 1, 3), (1 << 32, 64), ((1 << 32) - 7, 5)])
-def test_gather_lap_order_at_2p32_int32(n, s):
-    """The lap-ordered gather's 32-bit index arithmetic at its limit n <= 2^32:
+def test_gather_lap_order_at_2p32_int32(n, s, schedule):
+    """The lap-ordered and tiled gathers' 32-bit index arithmetic at n <= 2^32:
     the input holds its own index (int32, i.e. modulo 2^32), so every output
     names the source it was read from.  All n outputs are compared with
     (s*i) mod n computed in int64 by torch, chunk by chunk, and 2,000
@@ -681,9 +719,10 @@ def test_gather_lap_order_at_2p32_int32(n, s):
         tin[lo:hi] = ((v + (1 << 31)) % (1 << 32) - (1 << 31)).to(torch.int32)
         del v
     tout = torch.empty_like(tin)
+    ew.set_schedule(schedule)
     assert ew.lib().ew_gather_stride(3, tin.data_ptr(), tout.data_ptr(), n, s, _stream()) == 0
     rec = ew.last_launch()
-    assert rec["schedule"] == 3, rec
+    assert rec["schedule"] == (3 if schedule == "laps" else 4), rec
     torch.cuda.synchronize()
     for lo in range(0, n, chunk):
         hi = min(n, lo + chunk)
