@@ -16,14 +16,19 @@ A and B i.i.d. uniform[-1, 1) from a seeded generator.  A step is one call of
               device copies, cudaMemcpyAsync out; serial, and chunked on three
               streams) are reported beside it.
 * cpu_baseline  the CPU oracle, single-threaded, on the same inputs (rank 0,
-              one GPU only); its output is also compared with the GPU's.
-* aux         the other measured workloads (bf16/fp16 add at 2^28 aligned and
-              offset by one element, SAXPY 32M, ReLU 2^28 out of place and in
-              place, fused add+ReLU against the unfused pair, copy and stride-2
-              gather at 2^26, fp32 add at 2^20+3, the headline through the
-              persistent schedule and the bulk-copy path, and the library
-              device-to-device copy): GB/s, fraction of the measured peak and
-              of the copy ceiling measured in the same run.
+              one GPU only); its output is also compared with the GPU's.  An
+              all-cores figure (one slice per host core) is reported beside it.
+* aux         the other measured workloads (bf16/fp16 add at 2^28 aligned,
+              offset by one element and with pointers of different parity,
+              SAXPY 32M, ReLU 2^28 out of place and in place, fused add+ReLU
+              against the unfused pair, copy and gathers at strides 2, 4 and
+              16 at 2^26 in each block order, fp32 add at 2^20+3, the headline
+              through the persistent schedule and the bulk-copy path, and the
+              library device-to-device copy): GB/s, fraction of the measured
+              peak, of 8 TB/s and of the copy ceiling measured in the same
+              run, mean, median and minimum per launch.  SAXPY 32M and the
+              2^26 copy and gather are also timed as 50 launches captured in
+              one CUDA graph, which separates the host launch gaps.
 
 ``--impl reference`` times the CPU oracle instead (the reference arm), on a
 bounded sample of the same workload per step.
@@ -353,6 +358,34 @@ def time_launches(torch, stream, fn, steps, warmup):
     return total, sum(per) / steps
 
 
+def oracle_all_cores(oracle, metrics, a_h, b_h, want, min_s=5.0):
+    """The same oracle add split into one contiguous slice per host core, run
+    on that many threads (the oracle's C loop releases the GIL); a reported
+    figure beside the single-core baseline."""
+    from concurrent.futures import ThreadPoolExecutor
+    n = a_h.size
+    cores = os.cpu_count() or 1
+    bounds = [(n * k // cores, n * (k + 1) // cores) for k in range(cores)]
+
+    def part(b):
+        return oracle.add("f32", a_h[b[0]:b[1]], b_h[b[0]:b[1]])
+
+    with ThreadPoolExecutor(cores) as pool:
+        t0 = time.perf_counter()
+        reps = 0
+        while True:
+            parts = list(pool.map(part, bounds))
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= min_s:
+                break
+    same = all(np.array_equal(p_.view(np.uint32), want[b[0]:b[1]].view(np.uint32))
+               for p_, b in zip(parts, bounds))
+    return {"value": metrics.gbps(12 * n * reps, el), "unit": "GB/s", "cores": cores,
+            "sample": "%d full passes over the N=2^28 inputs on %d threads (%.1f s)" % (reps, cores, el),
+            "matches_single_core": same}
+
+
 def aux_measurements(torch, ew, inputs, metrics, stream, peak, dev):
     """The other workloads: (name -> GB/s, fraction of peak, kernel ms)."""
     out = {}
@@ -372,11 +405,48 @@ def aux_measurements(torch, ew, inputs, metrics, stream, peak, dev):
             if st != 0:
                 raise ew.EwError(st, name)
         total, kern = time_launches(torch, stream, fn, steps, 3)
+        per = sorted(time_launches.last_per_launch)
         nbytes = metrics.algorithmic_bytes(op, dtype, n)
-        out[name] = {"gbps": metrics.gbps(nbytes, kern), "frac": metrics.gbps(nbytes, kern) / peak,
-                     "kernel_ms": kern * 1e3, "step_ms": total / steps * 1e3,
+        g = metrics.gbps(nbytes, kern)
+        out[name] = {"gbps": g, "frac": g / peak, "frac_of_nominal_8tbs": g / 8000.0,
+                     "kernel_ms": kern * 1e3, "kernel_ms_median": per[len(per) // 2] * 1e3,
+                     "kernel_ms_min": per[0] * 1e3, "step_ms": total / steps * 1e3,
                      "gelem_per_s": n / kern / 1e9,
                      "bytes_per_launch": nbytes, "launch": ew.last_launch()}
+
+    def record_graph(name, op, dtype, n, call, k=50, reps=5):
+        """K launches captured in one CUDA graph and replayed: the per-launch
+        time without host launch gaps (median of `reps` replays)."""
+        st = call()  # fills the per-device caches outside the capture
+        if st != 0:
+            raise ew.EwError(st, name)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for _ in range(k):
+                st = call()
+        if st != 0:
+            raise ew.EwError(st, name + " (captured)")
+        times = []
+        with torch.cuda.stream(stream):  # replay() launches on the current stream
+            graph.replay()
+            torch.cuda.synchronize()
+            for _ in range(reps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                graph.replay()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                times.append(e0.elapsed_time(e1) / 1e3 / k)
+        per = sorted(times)[len(times) // 2]
+        nbytes = metrics.algorithmic_bytes(op, dtype, n)
+        g = metrics.gbps(nbytes, per)
+        out[name] = {"gbps": g, "frac": g / peak, "frac_of_nominal_8tbs": g / 8000.0,
+                     "kernel_ms": per * 1e3, "launches_per_graph": k, "replays": reps,
+                     "bytes_per_launch": nbytes,
+                     "note": "%d launches captured in one CUDA graph; per-launch time of the "
+                             "median replay" % k}
+        del graph
 
     n28 = 1 << 28
     for dtype, code in (("bf16", 2), ("f16", 1)):
@@ -409,6 +479,8 @@ def aux_measurements(torch, ew, inputs, metrics, stream, peak, dev):
     ry, py = dev_of(y, "f32")
     record("saxpy_f32_32M_inplace", "saxpy", "f32", n32m,
            lambda: L.ew_saxpy(0, 2.5, px, py, n32m, s), steps=200)
+    record_graph("saxpy_f32_32M_inplace_graph", "saxpy", "f32", n32m,
+                 lambda: L.ew_saxpy(0, 2.5, px, py, n32m, s))
     del rx, ry
     # SAXPY at larger N, where the fixed cost of a launch is amortised
     x = inputs.normal(n28, inputs.seed_for("saxpy_f32", 2))
@@ -462,6 +534,9 @@ def aux_measurements(torch, ew, inputs, metrics, stream, peak, dev):
     rx, px = dev_of(x, "f32")
     ry, py = dev_of(np.zeros_like(x), "f32")
     record("copy_f32_2p26", "copy", "f32", n26, lambda: L.ew_copy(0, px, py, n26, s), steps=200)
+    record_graph("copy_f32_2p26_graph", "copy", "f32", n26, lambda: L.ew_copy(0, px, py, n26, s))
+    record_graph("gather2_f32_2p26_graph", "gather", "f32", n26,
+                 lambda: L.ew_gather_stride(0, px, py, n26, 2, s))
     record("gather2_f32_2p26", "gather", "f32", n26,
            lambda: L.ew_gather_stride(0, px, py, n26, 2, s), steps=100)
     record("gather4_f32_2p26", "gather", "f32", n26,
@@ -757,7 +832,8 @@ def run_ours(args):
         line["cpu_baseline"] = {"value": cpu_gbps, "unit": "GB/s", "cores": 1, "kind": "oracle",
                                 "sample": "%d full passes over the N=2^28 inputs (%.1f s)" % (reps, el),
                                 "cpu": host_cpu_model(),
-                                "gpu_output_bit_exact_vs_oracle": parity}
+                                "gpu_output_bit_exact_vs_oracle": parity,
+                                "all_cores": oracle_all_cores(oracle, metrics, a_h, b_h, want)}
         line["parity"] = "bit-exact over all 2^28 outputs" if parity else "MISMATCH"
     if not args.no_aux and world == 1:
         line["aux"] = aux_measurements(torch, ew, inputs, metrics, stream, peak, dev)
