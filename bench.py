@@ -21,7 +21,7 @@ A and B i.i.d. uniform[-1, 1) from a seeded generator.  A step is one call of
 * aux         the other measured workloads (bf16/fp16 add at 2^28 aligned,
               offset by one element and with pointers of different parity,
               SAXPY 32M, ReLU 2^28 out of place and in place, fused add+ReLU
-              against the unfused pair, copy and gathers at strides 2, 4 and
+              and SAXPY+ReLU against the unfused pairs, copy and gathers at strides 2, 4 and
               16 at 2^26 in each block order, fp32 add at 2^20+3, the headline
               through the persistent schedule and the bulk-copy path, and the
               library device-to-device copy): GB/s, fraction of the measured
@@ -600,6 +600,21 @@ def aux_measurements(torch, ew, inputs, metrics, stream, peak, dev):
         "gbps": metrics.gbps(nb, kern), "frac": metrics.gbps(nb, kern) / peak, "kernel_ms": kern * 1e3,
         "bytes_per_launch": nb, "note": "two launches per step (add, then ReLU in place); GB/s counts the "
                                         "fused operation's 12 bytes per element"}
+    # SAXPY + ReLU fused in one pass (y = relu(2.5 x + y) in place, on A and C),
+    # against ew_saxpy then ew_relu in place
+    record("saxpy_relu_f32_2p28_fused", "saxpy_relu", "f32", n28,
+           lambda: L.ew_saxpy_relu(0, 2.5, pa, pc, n28, s))
+
+    def saxpy_unfused():
+        for st in (L.ew_saxpy(0, 2.5, pa, pc, n28, s), L.ew_relu(0, pc, pc, n28, s)):
+            if st != 0:
+                raise ew.EwError(st, "saxpy then relu")
+    total, kern = time_launches(torch, stream, saxpy_unfused, 50, 3)
+    nb = metrics.algorithmic_bytes("saxpy_relu", "f32", n28)
+    out["saxpy_then_relu_f32_2p28_unfused"] = {
+        "gbps": metrics.gbps(nb, kern), "frac": metrics.gbps(nb, kern) / peak, "kernel_ms": kern * 1e3,
+        "bytes_per_launch": nb, "note": "two launches per step (SAXPY, then ReLU in place); GB/s counts "
+                                        "the fused operation's 12 bytes per element"}
     for label, path, sched in (("persistent", "auto", "persistent"), ("tma", "tma", "auto")):
         ew.set_path(path)
         ew.set_schedule(sched)

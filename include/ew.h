@@ -15,6 +15,8 @@
  *                     CUDA-MODE lecture notes (cyqw.cn/news/898472), §5.2 example 1.
  *   ew_add_relu       C[i] = max(A[i] + B[i], 0) in one pass
  *                     CUDA-MODE lecture notes, §5.3 (kernel fusion).
+ *   ew_saxpy_relu     y[i] = max(alpha * x[i] + y[i], 0), in place, in one pass
+ *                     CUDA-MODE lecture notes, §5.3 (kernel fusion).
  *   ew_select_even_odd y[i] = x[i] even ? 2 x[i] : x[i] + 1 on 32-bit integers
  *                     CUDA-MODE lecture notes, §6.1-6.2 (control divergence).
  *   ew_copy           out[i] = in[i]
@@ -32,6 +34,7 @@
  *                alpha is binary32 and is never rounded to the 16-bit format.
  *   relu         x > 0 -> x;  x <= 0 (including -0) -> +0;  NaN -> x unchanged.
  *   add_relu     relu applied to the rounded sum of add.
+ *   saxpy_relu   relu applied to the rounded result of saxpy.
  *   select       two's complement int32, wrapping modulo 2^32.
  *   copy/gather  raw element bits.
  *
@@ -182,6 +185,12 @@ EW_API ew_status ew_relu(ew_dtype dtype, const void *x, void *y, int64_t n, ew_s
 EW_API ew_status ew_add_relu(ew_dtype dtype, const void *a, const void *b, void *c, int64_t n,
                              ew_stream_t stream);
 
+/* y = max(alpha * x + y, 0) in place: the result rounded as in ew_saxpy, then
+ * ReLU as in ew_relu, in one pass over memory (CUDA-MODE lecture notes §5.3,
+ * kernel fusion).  Arguments and aliasing as in ew_saxpy. */
+EW_API ew_status ew_saxpy_relu(ew_dtype dtype, float alpha, const void *x, void *y, int64_t n,
+                               ew_stream_t stream);
+
 /* y = x even ? 2x : x + 1, on EW_I32 only, wrapping modulo 2^32: the
  * control-divergence example of CUDA-MODE lecture notes §6.1-6.2 (an if/else
  * on x % 2 and its branch-free rewrite compute the same thing), computed
@@ -239,7 +248,7 @@ EW_API int ew_get_programmatic_launch(void);
  * environment variable EW_CHECK_POINTERS=1 enables it at start-up. */
 EW_API ew_status ew_set_pointer_check(int enable);
 
-/* How an ew_add / ew_saxpy / ew_relu / ew_add_relu / ew_select_even_odd /
+/* How an ew_add / ew_saxpy / ew_relu / ew_add_relu / ew_saxpy_relu / ew_select_even_odd /
  * ew_copy call with these pointers is split under the current ew_set_path
  * selection (host arithmetic only; needs no GPU).  ptrs: the call's input
  * pointers, then its output pointer last; nptrs in [1, 4].  When the pointers

@@ -44,7 +44,7 @@ STATUS_NAMES = {0: "EW_OK", 1: "EW_ERR_INVALID_VALUE", 2: "EW_ERR_NULL_POINTER",
                 5: "EW_ERR_NOT_DEVICE_POINTER", 6: "EW_ERR_CUDA", 7: "EW_ERR_TIMEOUT"}
 
 # Every function declared in include/ew.h.
-EXPORTS = ("ew_add", "ew_saxpy", "ew_relu", "ew_add_relu", "ew_select_even_odd", "ew_copy",
+EXPORTS = ("ew_add", "ew_saxpy", "ew_relu", "ew_add_relu", "ew_saxpy_relu", "ew_select_even_odd", "ew_copy",
            "ew_gather_stride", "ew_set_path", "ew_set_programmatic_launch",
            "ew_get_programmatic_launch",
            "ew_get_path", "ew_set_schedule", "ew_get_schedule", "ew_set_pointer_check",
@@ -92,12 +92,13 @@ def lib():
     i32, i64, f32, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
     L.ew_add.argtypes = [ctypes.c_int, vp, vp, vp, i64, vp]
     L.ew_saxpy.argtypes = [ctypes.c_int, f32, vp, vp, i64, vp]
+    L.ew_saxpy_relu.argtypes = [ctypes.c_int, f32, vp, vp, i64, vp]
     L.ew_relu.argtypes = [ctypes.c_int, vp, vp, i64, vp]
     L.ew_add_relu.argtypes = [ctypes.c_int, vp, vp, vp, i64, vp]
     L.ew_select_even_odd.argtypes = [ctypes.c_int, vp, vp, i64, vp]
     L.ew_copy.argtypes = [ctypes.c_int, vp, vp, i64, vp]
     L.ew_gather_stride.argtypes = [ctypes.c_int, vp, vp, i64, i64, vp]
-    for name in ("ew_add", "ew_saxpy", "ew_relu", "ew_add_relu", "ew_select_even_odd", "ew_copy",
+    for name in ("ew_add", "ew_saxpy", "ew_relu", "ew_add_relu", "ew_saxpy_relu", "ew_select_even_odd", "ew_copy",
                  "ew_gather_stride",
                  "ew_set_path", "ew_set_schedule", "ew_set_pointer_check", "ew_plan_query",
                  "ew_last_launch", "ew_device_error", "ew_selftest_bounded_wait"):
@@ -182,6 +183,14 @@ def ew_saxpy(alpha, x, y, stream=None):
     dt, n = _check_tensors(x, y)
     check(lib().ew_saxpy(dt, float(alpha), x.data_ptr(), y.data_ptr(), n, _stream(stream, x.device)),
           "ew_saxpy")
+    return y
+
+
+def ew_saxpy_relu(alpha, x, y, stream=None):
+    """y = max(alpha * x + y, 0) in place, in one pass (the fma rounded first); returns y."""
+    dt, n = _check_tensors(x, y)
+    check(lib().ew_saxpy_relu(dt, float(alpha), x.data_ptr(), y.data_ptr(), n, _stream(stream, x.device)),
+          "ew_saxpy_relu")
     return y
 
 
@@ -299,7 +308,8 @@ def device_error(stream=None):
     return st, code.value
 
 
-__all__ = ["ew_add", "ew_saxpy", "ew_relu", "ew_add_relu", "ew_select_even_odd", "ew_copy", "ew_gather_stride", "set_path",
+__all__ = ["ew_add", "ew_saxpy", "ew_relu", "ew_add_relu", "ew_saxpy_relu", "ew_select_even_odd", "ew_copy",
+           "ew_gather_stride", "set_path",
            "get_path", "set_schedule", "get_schedule", "set_programmatic_launch",
            "get_programmatic_launch", "set_pointer_check", "plan_query",
            "last_launch", "device_error", "selftest_bounded_wait", "lib", "EwError", "EXPORTS"]

@@ -451,6 +451,16 @@ ew_status ew_saxpy(ew_dtype dt, float alpha, const void *x, void *y, int64_t n, 
     return run_stream(OP_SAXPY, dt, x, y, y, n, alpha, reinterpret_cast<cudaStream_t>(s));
 }
 
+ew_status ew_saxpy_relu(ew_dtype dt, float alpha, const void *x, void *y, int64_t n, ew_stream_t s) {
+    t_last = ew_launch_record{};
+    if (!float_dtype(dt)) return EW_ERR_UNSUPPORTED_DTYPE;
+    const void *p[2] = {x, y};
+    ew_status st = check_common(dt, n, p, 2);
+    if (st != EW_OK || n == 0) return st;
+    if ((st = check_alias(x, y, n * elem_size(dt))) != EW_OK) return st;
+    return run_stream(OP_SAXPY_RELU, dt, x, y, y, n, alpha, reinterpret_cast<cudaStream_t>(s));
+}
+
 ew_status ew_relu(ew_dtype dt, const void *x, void *y, int64_t n, ew_stream_t s) {
     t_last = ew_launch_record{};
     if (!float_dtype(dt)) return EW_ERR_UNSUPPORTED_DTYPE;

@@ -278,6 +278,24 @@ struct OpAddReluBF16 {
     }
 };
 
+// Fused SAXPY + ReLU: y = max(fmaf(alpha, x, y), 0) with the fma rounded
+// first, i.e. exactly relu(saxpy(x, y)) in one pass (12 bytes per binary32
+// element instead of 12 + 8).
+template <class Saxpy, class Relu>
+struct OpSaxpyReluOf {
+    static constexpr int kIn = 2, kElem = Saxpy::kElem;
+    float alpha;
+    __device__ __forceinline__ uint32_t word(uint32_t x, uint32_t y) const {
+        return Relu{}.word(Saxpy{alpha}.word(x, y), 0u);
+    }
+    __device__ __forceinline__ uint16_t half(uint16_t x, uint16_t y) const {
+        return Relu{}.half(Saxpy{alpha}.half(x, y), 0);
+    }
+};
+using OpSaxpyReluF32 = OpSaxpyReluOf<OpSaxpyF32, OpReluF32>;
+using OpSaxpyReluF16 = OpSaxpyReluOf<OpSaxpyF16, OpReluF16>;
+using OpSaxpyReluBF16 = OpSaxpyReluOf<OpSaxpyBF16, OpReluBF16>;
+
 // Even/odd select on 32-bit two's complement integers: y = x even ? 2x : x + 1
 // (CUDA-MODE lecture notes §6: the divergent if/else and its branch-free
 // rewrite compute the same thing).  Written without a branch: x + (odd ? 1 : x),

@@ -38,7 +38,8 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), unsigned grid, unsigned bloc
 
 // Operator ids of the streaming (contiguous) kernels.
 enum OpId : int {
-    OP_ADD = 0, OP_SAXPY = 1, OP_RELU = 2, OP_COPY = 3, OP_ADD_RELU = 4, OP_SELECT = 5, OP_COUNT = 6
+    OP_ADD = 0, OP_SAXPY = 1, OP_RELU = 2, OP_COPY = 3, OP_ADD_RELU = 4, OP_SELECT = 5, OP_SAXPY_RELU = 6,
+    OP_COUNT = 7
 };
 // Element-size classes of the kernel tables: the 4-byte table serves binary32
 // and int32, the 16-bit tables binary16 and bfloat16 (ids match ew_dtype for

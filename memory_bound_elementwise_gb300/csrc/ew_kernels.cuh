@@ -30,6 +30,11 @@ template <class Op> __device__ __forceinline__ Op make_op(float) { return Op{}; 
 template <> __device__ __forceinline__ OpSaxpyF32 make_op<OpSaxpyF32>(float a) { return OpSaxpyF32{a}; }
 template <> __device__ __forceinline__ OpSaxpyF16 make_op<OpSaxpyF16>(float a) { return OpSaxpyF16{a}; }
 template <> __device__ __forceinline__ OpSaxpyBF16 make_op<OpSaxpyBF16>(float a) { return OpSaxpyBF16{a}; }
+template <> __device__ __forceinline__ OpSaxpyReluF32 make_op<OpSaxpyReluF32>(float a) { return OpSaxpyReluF32{a}; }
+template <> __device__ __forceinline__ OpSaxpyReluF16 make_op<OpSaxpyReluF16>(float a) { return OpSaxpyReluF16{a}; }
+template <> __device__ __forceinline__ OpSaxpyReluBF16 make_op<OpSaxpyReluBF16>(float a) {
+    return OpSaxpyReluBF16{a};
+}
 
 template <class Op, int VB, int U>
 __global__ void __launch_bounds__(kBlock) stream_kernel(const StreamArgs a) {

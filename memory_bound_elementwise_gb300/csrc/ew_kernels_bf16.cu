@@ -19,6 +19,8 @@ const StreamEntry kTable[OP_COUNT][5] = {
     {kNoEntry, kNoEntry, kNoEntry, kNoEntry, kNoEntry},
     {eb<OpAddReluBF16>(0), eb<OpAddReluBF16>(1), eb<OpAddReluBF16>(2), eb<OpAddReluBF16>(3), eb<OpAddReluBF16>(4)},
     {kNoEntry, kNoEntry, kNoEntry, kNoEntry, kNoEntry},
+    {eb<OpSaxpyReluBF16>(0), eb<OpSaxpyReluBF16>(1), eb<OpSaxpyReluBF16>(2), eb<OpSaxpyReluBF16>(3),
+     eb<OpSaxpyReluBF16>(4)},
 };
 }  // namespace
 

@@ -19,6 +19,8 @@ const StreamEntry kTable[OP_COUNT][5] = {
     {e16<OpCopy<2>>(0), e16<OpCopy<2>>(1), e16<OpCopy<2>>(2), e16<OpCopy<2>>(3), e16<OpCopy<2>>(4)},
     {e16<OpAddReluF16>(0), e16<OpAddReluF16>(1), e16<OpAddReluF16>(2), e16<OpAddReluF16>(3), e16<OpAddReluF16>(4)},
     {kNoEntry, kNoEntry, kNoEntry, kNoEntry, kNoEntry},
+    {e16<OpSaxpyReluF16>(0), e16<OpSaxpyReluF16>(1), e16<OpSaxpyReluF16>(2), e16<OpSaxpyReluF16>(3),
+     e16<OpSaxpyReluF16>(4)},
 };
 
 constexpr int kGatherOneshotUnroll = 4;

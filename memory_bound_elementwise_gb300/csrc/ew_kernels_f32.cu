@@ -19,6 +19,7 @@ const StreamEntry kTable[OP_COUNT][5] = {
     {e32<OpAddReluF32>(0), e32<OpAddReluF32>(1), e32<OpAddReluF32>(2), e32<OpAddReluF32>(3), kNoEntry},
     {e32<OpSelectEvenOddI32>(0), e32<OpSelectEvenOddI32>(1), e32<OpSelectEvenOddI32>(2),
      e32<OpSelectEvenOddI32>(3), kNoEntry},
+    {e32<OpSaxpyReluF32>(0), e32<OpSaxpyReluF32>(1), e32<OpSaxpyReluF32>(2), e32<OpSaxpyReluF32>(3), kNoEntry},
 };
 
 constexpr int kGatherOneshotUnroll = 4;

@@ -289,6 +289,8 @@ const TmaEntry kTmaRealign[OP_COUNT][DT_COUNT] = {
     {tma_realign_entry_of<OpAddReluF32>(), tma_realign_entry_of<OpAddReluF16>(),
      tma_realign_entry_of<OpAddReluBF16>()},
     {tma_realign_entry_of<OpSelectEvenOddI32>(), TmaEntry{nullptr, nullptr, 0}, TmaEntry{nullptr, nullptr, 0}},
+    {tma_realign_entry_of<OpSaxpyReluF32>(), tma_realign_entry_of<OpSaxpyReluF16>(),
+     tma_realign_entry_of<OpSaxpyReluBF16>()},
 };
 
 template <class Op>
@@ -310,6 +312,7 @@ const TmaEntry kTma[OP_COUNT][DT_COUNT] = {
     {tma_entry_of<OpCopy<4>>(), tma_entry_of<OpCopy<2>>(), tma_entry_of<OpCopy<2>>()},
     {tma_entry_of<OpAddReluF32>(), tma_entry_of<OpAddReluF16>(), tma_entry_of<OpAddReluBF16>()},
     {tma_entry_of<OpSelectEvenOddI32>(), TmaEntry{nullptr, nullptr, 0}, TmaEntry{nullptr, nullptr, 0}},
+    {tma_entry_of<OpSaxpyReluF32>(), tma_entry_of<OpSaxpyReluF16>(), tma_entry_of<OpSaxpyReluBF16>()},
 };
 
 // Arms an mbarrier for 16 bytes that no copy will deliver: the bounded wait

@@ -12,6 +12,7 @@ Bytes are the ones the operation must move at least once, counted per element:
 * copy    out = in         read in, write out        -> 2
 * add_relu C = max(A + B, 0), fused: 3, against 3 + 2 for the two passes
   (CUDA-MODE lecture notes §5.3, kernel fusion)
+* saxpy_relu y = max(a*x + y, 0), fused: 3, against 3 + 2 for the two passes
 * select  y = x even ? 2x : x + 1 on int32 -> 2 (CUDA-MODE lecture notes §6)
 * gather  out[i] = in[(s*i) mod n]: one element read and one written per
   output -> 2 (logical bytes; the sectors actually fetched are larger and are
@@ -25,6 +26,7 @@ ELEM_SIZE = {"f32": 4, "f16": 2, "bf16": 2, "i32": 4}
 TRANSFERS_PER_ELEMENT = {
     "add": 3,
     "add_relu": 3,
+    "saxpy_relu": 3,
     "saxpy": 3,
     "relu": 2,
     "copy": 2,

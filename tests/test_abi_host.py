@@ -52,6 +52,7 @@ def test_zero_length_is_a_no_op(dt):
     assert L.ew_saxpy(dt, 2.5, None, None, 0, None) == OK
     assert L.ew_relu(dt, None, None, 0, None) == OK
     assert L.ew_add_relu(dt, None, None, None, 0, None) == OK
+    assert L.ew_saxpy_relu(dt, 2.5, None, None, 0, None) == OK
     assert L.ew_select_even_odd(3, None, None, 0, None) == OK
     assert L.ew_copy(dt, None, None, 0, None) == OK
     assert L.ew_gather_stride(dt, None, None, 0, 2, None) == OK
@@ -71,6 +72,10 @@ def test_argument_errors_are_caught_on_the_host():
     assert L.ew_add_relu(0, P, P + 4096, None, 10, None) == NULLP
     assert L.ew_add_relu(4, P, P + 4096, P + 8192, 10, None) == DTYPE
     assert L.ew_add_relu(0, P, P + 4096, P + 4, 10, None) == OVERLAP
+    assert L.ew_saxpy_relu(0, 2.5, P, None, 10, None) == NULLP
+    assert L.ew_saxpy_relu(3, 2.5, P, P + 4096, 10, None) == DTYPE
+    assert L.ew_saxpy_relu(0, 2.5, P, P + 4, 10, None) == OVERLAP
+    assert L.ew_saxpy_relu(1, 2.5, P + 1, P + 4096, 10, None) == INVALID
     # int32 is taken by the select, copy and gather only
     assert L.ew_add(3, P, P + 4096, P + 8192, 10, None) == DTYPE
     assert L.ew_saxpy(3, 1.0, P, P + 4096, 10, None) == DTYPE

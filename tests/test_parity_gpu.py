@@ -53,6 +53,8 @@ def run_op(op, dtype, bufs, n, alpha=2.5):
         st = L.ew_relu(dt, p[0], p[1], n, _stream())
     elif op == "add_relu":
         st = L.ew_add_relu(dt, p[0], p[1], p[2], n, _stream())
+    elif op == "saxpy_relu":
+        st = L.ew_saxpy_relu(dt, alpha, p[0], p[1], n, _stream())
     elif op == "copy":
         st = L.ew_copy(dt, p[0], p[1], n, _stream())
     else:
@@ -69,6 +71,8 @@ def expected(op, dtype, x, y, alpha=2.5):
         return oracle.relu(dtype, x)
     if op == "add_relu":  # the unfused definition: round the sum, then ReLU
         return oracle.relu(dtype, oracle.add(dtype, x, y))
+    if op == "saxpy_relu":  # round the fused multiply-add, then ReLU
+        return oracle.relu(dtype, oracle.saxpy(dtype, alpha, x, y))
     return oracle.copy(x)
 
 
@@ -83,8 +87,8 @@ def make_inputs(dtype, n, seed, specials=True):
 
 def check_case(op, dtype, n, offs, seed, path="auto", schedule="auto"):
     x, y = make_inputs(dtype, n, seed)
-    nin = {"add": 2, "add_relu": 2, "saxpy": 2, "relu": 1, "copy": 1}[op]
-    if op == "saxpy":
+    nin = {"add": 2, "add_relu": 2, "saxpy": 2, "saxpy_relu": 2, "relu": 1, "copy": 1}[op]
+    if op in ("saxpy", "saxpy_relu"):
         bx = GuardedBuffer(n, dtype, offs[0]).fill(x)
         by = GuardedBuffer(n, dtype, offs[1]).fill(y)
         bufs, outb = [bx, by], by
@@ -103,7 +107,7 @@ def check_case(op, dtype, n, offs, seed, path="auto", schedule="auto"):
     rec = ew.last_launch()
     torch.cuda.synchronize()
     want = expected(op, dtype, x, y)
-    assert_bits_equal(outb.host(), want, dtype, nan_as_class=op in ("add", "saxpy", "add_relu"),
+    assert_bits_equal(outb.host(), want, dtype, nan_as_class=op in ("add", "saxpy", "add_relu", "saxpy_relu"),
                       what="%s %s n=%d offs=%s path=%s" % (op, dtype, n, offs, path))
     for b in bufs:
         assert b.guards_intact(), "guard zone written: %s %s n=%d offs=%s" % (op, dtype, n, offs)
@@ -111,7 +115,7 @@ def check_case(op, dtype, n, offs, seed, path="auto", schedule="auto"):
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
-@pytest.mark.parametrize("op", ["add", "saxpy", "relu", "copy", "add_relu"])
+@pytest.mark.parametrize("op", ["add", "saxpy", "relu", "copy", "add_relu", "saxpy_relu"])
 def test_small_sizes_every_offset(op, dtype):
     per = 32 // ESIZE[dtype]
     for n in SMALL_N:
@@ -123,7 +127,7 @@ def test_small_sizes_every_offset(op, dtype):
 @pytest.mark.parametrize("schedule", ["oneshot", "persistent", "laps"])
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("dtype", DTYPES)
-@pytest.mark.parametrize("op", ["add", "saxpy", "relu", "copy", "add_relu"])
+@pytest.mark.parametrize("op", ["add", "saxpy", "relu", "copy", "add_relu", "saxpy_relu"])
 def test_forced_paths(op, dtype, path, schedule):
     for n in (1, 33, 1000, 70001, 600_001):
         for off in (0, 1, 3):
@@ -142,7 +146,7 @@ def test_forced_paths(op, dtype, path, schedule):
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
-@pytest.mark.parametrize("op", ["add", "saxpy", "relu", "copy", "add_relu"])
+@pytest.mark.parametrize("op", ["add", "saxpy", "relu", "copy", "add_relu", "saxpy_relu"])
 def test_tma_tile_boundaries(op, dtype):
     """Sizes around the 8 KiB bulk-copy tile and the 2-tile CTA, at offsets that
     keep or break 16-byte alignment (the latter falls back to vector loads)."""
@@ -162,7 +166,7 @@ REALIGN_OFFSETS = {2: [[1, 0, 3], [0, 1, 0], [1, 1, 0], [3, 6, 7], [7, 0, 5], [0
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
-@pytest.mark.parametrize("op", ["add", "saxpy", "relu", "copy", "add_relu"])
+@pytest.mark.parametrize("op", ["add", "saxpy", "relu", "copy", "add_relu", "saxpy_relu"])
 def test_tma_realign_mixed_offsets(op, dtype):
     """EW_PATH_TMA with pointers that disagree modulo 16 bytes runs the
     realigning bulk-copy kernel: 16-byte aligned output tiles, each input
@@ -182,14 +186,14 @@ def test_tma_realign_mixed_offsets(op, dtype):
             assert rec["path"] == 4
             assert rec["head"] + rec["nvec"] * per_tile + rec["tail"] == n
             if len({(o * e) % 16 for o in offs}) > 1:  # offsets disagree modulo 16 bytes
-                staged = 2 if op in ("add", "add_relu", "saxpy") else 1  # inputs staged per tile
+                staged = 2 if op in ("add", "add_relu", "saxpy", "saxpy_relu") else 1  # inputs staged per tile
                 assert rec["smem"] == 2 * (staged * (8192 + 16) + 8192) + 16, rec
                 assert rec["head"] * e >= 16 or rec["nvec"] == 0
                 assert rec["nvec"] == 0 or rec["tail"] * e >= 16
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("op", ["add", "saxpy", "relu", "copy", "add_relu"])
+@pytest.mark.parametrize("op", ["add", "saxpy", "relu", "copy", "add_relu", "saxpy_relu"])
 def test_auto_realigns_16bit_parity_mismatch(op, dtype):
     """Under EW_PATH_AUTO, 16-bit pointers of different parity take the
     realigning bulk-copy kernel from n = 2^22 (2-byte accesses below)."""
@@ -319,6 +323,42 @@ def test_saxpy_special_alphas(dtype):
         assert_bits_equal(by.host(), oracle.saxpy(dtype, alpha, x, y), dtype, True,
                           "saxpy alpha=%r" % alpha)
         assert by.guards_intact()
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_saxpy_relu_special_alphas_and_aliasing(dtype):
+    """Fused SAXPY + ReLU: alpha = +-0, +-inf, NaN, a subnormal, the largest
+    binary32 and 1/3 against the oracle's saxpy then relu; x == y in place;
+    and a 2^24-element case spanning many blocks."""
+    L = ew.lib()
+    n = 4099
+    alphas = [0.0, -0.0, float("inf"), float("-inf"), float("nan"),
+              float(np.float32(1e-40)), float(np.finfo(np.float32).max), float(np.float32(1 / 3))]
+    for k, alpha in enumerate(alphas):
+        x, y = make_inputs(dtype, n, 4700 + k)
+        bx = GuardedBuffer(n, dtype, 1).fill(x)
+        by = GuardedBuffer(n, dtype, 1).fill(y)
+        assert L.ew_saxpy_relu(DT_CODE[dtype], alpha, bx.view.data_ptr(), by.view.data_ptr(), n,
+                               _stream()) == 0
+        torch.cuda.synchronize()
+        want = oracle.relu(dtype, oracle.saxpy(dtype, alpha, x, y))
+        assert_bits_equal(by.host(), want, dtype, True, "saxpy_relu alpha=%r" % alpha)
+        assert by.guards_intact()
+    x, _ = make_inputs(dtype, n, 4750)
+    bx = GuardedBuffer(n, dtype, 0).fill(x)
+    assert L.ew_saxpy_relu(DT_CODE[dtype], -1.5, bx.view.data_ptr(), bx.view.data_ptr(), n, _stream()) == 0
+    torch.cuda.synchronize()
+    assert_bits_equal(bx.host(), oracle.relu(dtype, oracle.saxpy(dtype, -1.5, x, x)), dtype, True,
+                      "saxpy_relu x == y")
+    m = 1 << 24
+    x = inputs.as_dtype(inputs.normal(m, 4760), dtype)
+    y = inputs.as_dtype(inputs.normal(m, 4761), dtype)
+    tx = torch.from_numpy(x.view(np.int32 if dtype == "f32" else np.int16)).cuda()
+    ty = torch.from_numpy(y.view(np.int32 if dtype == "f32" else np.int16)).cuda()
+    assert L.ew_saxpy_relu(DT_CODE[dtype], 2.5, tx.data_ptr(), ty.data_ptr(), m, _stream()) == 0
+    torch.cuda.synchronize()
+    got = ty.cpu().numpy().view(np.float32 if dtype == "f32" else np.uint16)
+    assert_bits_equal(got, oracle.relu(dtype, oracle.saxpy(dtype, 2.5, x, y)), dtype, True, "saxpy_relu 2^24")
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
