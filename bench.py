@@ -21,8 +21,9 @@ A and B i.i.d. uniform[-1, 1) from a seeded generator.  A step is one call of
 * aux         the other measured workloads (bf16/fp16 add at 2^28 aligned,
               offset by one element and with pointers of different parity,
               SAXPY 32M, ReLU 2^28 out of place and in place, fused add+ReLU
-              and SAXPY+ReLU against the unfused pairs, copy and gathers at strides 2, 4 and
-              16 at 2^26 in each block order, fp32 add at 2^20+3, the headline
+              and SAXPY+ReLU against the unfused pairs, copy and gathers at
+              strides 2, 4 and 16 at 2^26 in each block order, fp32 add at
+              2^20+3, the headline
               through the persistent schedule and the bulk-copy path, and the
               library device-to-device copy): GB/s, fraction of the measured
               peak, of 8 TB/s and of the copy ceiling measured in the same
@@ -93,6 +94,7 @@ PROFILE_CASES = {
     "gather2_span_f32": ("gather_span", "f32", 0),
     "add_bf16_mixed": ("add", "bf16", (1, 0, 3)),
     "gather16_f32": ("gather16", "f32", 0),
+    "saxpy_relu_f32": ("saxpy_relu", "f32", 0),
 }
 
 
@@ -133,7 +135,8 @@ def run_profile_case(args):
             "relu_inplace": lambda: L.ew_relu(code, px, px, n, s),
             "select": lambda: L.ew_select_even_odd(3, px, pz, n, s),
             "gather_span": lambda: L.ew_gather_stride(code, px, pz, n, 2, s),
-            "gather16": lambda: L.ew_gather_stride(code, px, pz, n, 16, s)}[op]
+            "gather16": lambda: L.ew_gather_stride(code, px, pz, n, 16, s),
+            "saxpy_relu": lambda: L.ew_saxpy_relu(code, 2.5, px, py, n, s)}[op]
     if op == "gather_span":
         ew.set_path("v256")
     for _ in range(args.warmup + args.steps):
