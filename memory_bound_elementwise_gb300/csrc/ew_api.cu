@@ -421,6 +421,153 @@ ew_status check_alias(const void *in, const void *out, int64_t bytes) {
     return overlaps(in, out, bytes) ? EW_ERR_OVERLAP : EW_OK;
 }
 
+// ---------------------------------------------------------------- gather planning
+
+// One gather launch: kernel, arguments, grid and what the launch record reports.
+struct GatherLaunch {
+    const GatherEntry *entry = nullptr;
+    GatherArgs args{};
+    int grid = 0;
+    int32_t path = EW_PATH_SCALAR, vec_bytes = 0, smem = 0, schedule = EW_SCHED_ONESHOT;
+    int64_t head = 0, nvec = 0, tail = 0;
+};
+
+enum class GatherKind { SPAN, TILED, LAPS, ONESHOT, STRIDE };
+
+constexpr uint64_t kOneshotMaxN = uint64_t(1) << 32;  // the 32-bit index kernels
+
+GatherArgs gather_args(const void *in, void *out, uint64_t n, uint64_t s_mod) {
+    GatherArgs a{};
+    a.in = in;
+    a.out = out;
+    a.n = n;
+    a.s_mod = s_mod;
+    return a;
+}
+
+// The lap geometry shared by the lap-ordered and tiled kernels:
+// n = lap_q * s + lap_m, and division by s through floor(2^32 / s) + 1.
+void set_lap_geometry(GatherArgs *a, uint64_t n, uint64_t s_mod) {
+    a->lap_q = static_cast<uint32_t>(n / s_mod);
+    a->lap_m = static_cast<uint32_t>(n % s_mod);
+    a->div_magic = static_cast<uint32_t>((uint64_t(1) << 32) / s_mod + 1);
+}
+
+// Which gather kernel runs, from the path and schedule selections:
+//   span     EW_PATH_V256 chosen explicitly: 4-byte elements, s = 2 or 4;
+//   tiled    EW_SCHED_TILED, or AUTO from s = 32 / E (every lane of a strided
+//            warp load is then its own 32-byte sector), for 2 <= s <= 64;
+//   laps     AUTO below that, or EW_SCHED_LAPS, once every lap holds a block;
+//   oneshot  index order, one block per chunk (n <= 2^32);
+//   stride   index order, grid-stride (EW_SCHED_PERSISTENT, or n > 2^32).
+GatherKind choose_gather(int e, uint64_t n, uint64_t s_mod) {
+    const int path = g_path.load(std::memory_order_relaxed);
+    const int sched = g_schedule.load(std::memory_order_relaxed);
+    const bool small_n = n <= kOneshotMaxN;
+    if (path == EW_PATH_V256 && e == 4 && (s_mod == 2 || s_mod == 4) && small_n) return GatherKind::SPAN;
+    if (sched == EW_SCHED_PERSISTENT || !small_n) return GatherKind::STRIDE;
+    const bool small_stride = s_mod >= 2 && s_mod <= kMaxLaps;
+    const bool tiled = sched == EW_SCHED_TILED || (sched == EW_SCHED_AUTO && s_mod >= static_cast<uint64_t>(32 / e));
+    if (small_stride && tiled) return GatherKind::TILED;
+    const GatherEntry *laps = e == 4 ? gather_laps_4() : gather_laps_2();
+    const uint64_t lap_block = static_cast<uint64_t>(kBlock) * laps->unroll;
+    if (sched != EW_SCHED_ONESHOT && small_stride && n / s_mod >= lap_block) return GatherKind::LAPS;
+    return GatherKind::ONESHOT;
+}
+
+// Span variant: each thread loads the contiguous 8s-element source span of 8
+// outputs with 256-bit loads; a scalar head reaches 32-byte output alignment.
+GatherLaunch plan_gather_span(const void *in, void *out, uint64_t n, uint64_t s_mod) {
+    GatherLaunch gl;
+    gl.entry = gather_span_4(static_cast<int64_t>(s_mod));
+    gl.args = gather_args(in, out, n, s_mod);
+    gl.args.barrett_m = ~uint64_t(0) / n;
+    const uintptr_t o = reinterpret_cast<uintptr_t>(out);
+    gl.args.head = std::min<int64_t>(static_cast<int64_t>(((32 - o % 32) % 32) / 4), static_cast<int64_t>(n));
+    gl.args.nvec = (static_cast<int64_t>(n) - gl.args.head) / 8;
+    gl.args.tail0 = gl.args.head + 8 * gl.args.nvec;
+    const int64_t per_block = static_cast<int64_t>(kBlock) * gl.entry->unroll;
+    gl.grid = clamp_grid((gl.args.nvec + per_block - 1) / per_block);
+    gl.path = EW_PATH_V256;
+    gl.vec_bytes = 32;
+    gl.head = gl.args.head;
+    gl.nvec = gl.args.nvec;
+    gl.tail = static_cast<int64_t>(n) - gl.args.tail0;
+    return gl;
+}
+
+// Tiled kernel: P (a power of two) positions of every lap per block, the
+// 32 KiB input span they draw from staged in shared memory, rows padded.
+GatherLaunch plan_gather_tiled(int e, const void *in, void *out, uint64_t n, uint64_t s_mod) {
+    GatherLaunch gl;
+    gl.entry = e == 4 ? gather_tiled_4() : gather_tiled_2();
+    gl.args = gather_args(in, out, n, s_mod);
+    const uint32_t per_block = (kTiledSpanBytes / e) / static_cast<uint32_t>(s_mod);
+    uint32_t log2p = 0;
+    while ((2u << log2p) <= per_block) ++log2p;  // largest power of two <= per_block
+    gl.args.tile_p = 1u << log2p;
+    gl.args.tile_log2p = log2p;
+    gl.args.tile_pitch = gl.args.tile_p + tiled_pad_words(static_cast<uint32_t>(s_mod), e) * (4 / e);
+    set_lap_geometry(&gl.args, n, s_mod);
+    const uint64_t lap_len = (n + s_mod - 1) / s_mod;
+    gl.grid = clamp_grid(static_cast<int64_t>((lap_len + gl.args.tile_p - 1) / gl.args.tile_p));
+    gl.vec_bytes = e;
+    gl.smem = static_cast<int32_t>(s_mod * gl.args.tile_pitch * e);
+    gl.schedule = EW_SCHED_TILED;
+    gl.nvec = static_cast<int64_t>(n);
+    return gl;
+}
+
+// Lap order: block b takes chunk b / s of lap b mod s.
+GatherLaunch plan_gather_laps(int e, const void *in, void *out, uint64_t n, uint64_t s_mod) {
+    GatherLaunch gl;
+    gl.entry = e == 4 ? gather_laps_4() : gather_laps_2();
+    gl.args = gather_args(in, out, n, s_mod);
+    set_lap_geometry(&gl.args, n, s_mod);
+    const uint64_t lap_block = static_cast<uint64_t>(kBlock) * gl.entry->unroll;
+    const uint64_t lap_len = (n + s_mod - 1) / s_mod;  // the longest lap
+    gl.grid = clamp_grid(static_cast<int64_t>(s_mod * ((lap_len + lap_block - 1) / lap_block)));
+    gl.vec_bytes = e;
+    gl.schedule = EW_SCHED_LAPS;
+    gl.nvec = static_cast<int64_t>(n);
+    return gl;
+}
+
+// Index order, one block per chunk: (s * i) mod n by Barrett reduction, then
+// (s * kBlock) mod n per slot.
+GatherLaunch plan_gather_oneshot(int e, const void *in, void *out, uint64_t n, uint64_t s_mod) {
+    GatherLaunch gl;
+    gl.entry = e == 4 ? gather_oneshot_4() : gather_oneshot_2();
+    gl.args = gather_args(in, out, n, s_mod);
+    const int64_t per_block = static_cast<int64_t>(kBlock) * gl.entry->unroll;
+    gl.grid = clamp_grid((static_cast<int64_t>(n) + per_block - 1) / per_block);
+    gl.args.step_mod = (s_mod * static_cast<uint64_t>(kBlock)) % n;  // s_mod < n <= 2^32
+    gl.args.barrett_m = ~uint64_t(0) / n;
+    gl.vec_bytes = e;
+    gl.nvec = static_cast<int64_t>(n);
+    return gl;
+}
+
+// Index order, grid-stride over SMs x resident blocks: one modular product
+// per thread, then (s * T) mod n per slot.
+cudaError_t plan_gather_stride(int e, int dev, int sms, const void *in, void *out, uint64_t n, uint64_t s_mod,
+                               GatherLaunch *gl) {
+    gl->entry = e == 4 ? gather_stride_4() : gather_stride_2();
+    gl->args = gather_args(in, out, n, s_mod);
+    int occ = 1;
+    const cudaError_t ce = blocks_per_sm(dev, gl->entry->kernel, kBlock, 0, &occ);
+    if (ce != cudaSuccess) return ce;
+    const int64_t per_block = static_cast<int64_t>(kBlock) * gl->entry->unroll;
+    gl->grid = clamp_grid(std::min<int64_t>((static_cast<int64_t>(n) + per_block - 1) / per_block,
+                                            static_cast<int64_t>(sms) * occ));
+    const uint64_t nthr = static_cast<uint64_t>(gl->grid) * kBlock;
+    gl->args.step_mod = static_cast<uint64_t>((static_cast<unsigned __int128>(s_mod) * nthr) % n);
+    gl->vec_bytes = e;
+    gl->schedule = EW_SCHED_PERSISTENT;
+    gl->nvec = static_cast<int64_t>(n);
+    return cudaSuccess;
+}
+
 }  // namespace
 
 bool ew::programmatic_launch() { return g_programmatic.load(std::memory_order_relaxed) != 0; }
@@ -519,108 +666,31 @@ ew_status ew_gather_stride(ew_dtype dt, const void *in, void *out, int64_t n, in
     int dev = 0, sms = 0;
     cudaError_t ce = device_info(&dev, &sms);
     if (ce != cudaSuccess) return cuda_fail(ce);
+    const int e = elem_size(dt);
     const uint64_t un = static_cast<uint64_t>(n);
     const uint64_t s_mod = static_cast<uint64_t>(stride) % un;
-    const int sched = g_schedule.load(std::memory_order_relaxed);
-    // span variant (EW_PATH_V256 only): 4-byte elements, stride 2 or 4, n <= 2^32
-    if (resolved_path() == EW_PATH_V256 && g_path.load(std::memory_order_relaxed) != EW_PATH_AUTO &&
-        elem_size(dt) == 4 && (s_mod == 2 || s_mod == 4) && un <= (uint64_t(1) << 32)) {
-        const GatherEntry *g = gather_span_4(static_cast<int64_t>(s_mod));
-        GatherArgs ga{in, out, un, s_mod, 0, ~uint64_t(0) / un, 0, 0, 0, 0, 0, 0, 0, 0, 0};
-        const uintptr_t o = reinterpret_cast<uintptr_t>(out);
-        ga.head = std::min<int64_t>(static_cast<int64_t>(((32 - o % 32) % 32) / 4), n);
-        ga.nvec = (n - ga.head) / 8;
-        ga.tail0 = ga.head + 8 * ga.nvec;
-        const int64_t per_block = static_cast<int64_t>(kBlock) * g->unroll;
-        const int grid = clamp_grid((ga.nvec + per_block - 1) / per_block);
-        ce = g->launch(ga, grid, reinterpret_cast<cudaStream_t>(s));
-        if (ce != cudaSuccess) return cuda_fail(ce);
-        t_last.launches = 1;
-        t_last.path = EW_PATH_V256;
-        t_last.vec_bytes = 32;
-        t_last.grid = grid;
-        t_last.block = kBlock;
-        t_last.schedule = EW_SCHED_ONESHOT;
-        t_last.head = ga.head;
-        t_last.nvec = ga.nvec;
-        t_last.tail = n - ga.tail0;
-        return EW_OK;
+    GatherLaunch gl;
+    switch (choose_gather(e, un, s_mod)) {
+        case GatherKind::SPAN: gl = plan_gather_span(in, out, un, s_mod); break;
+        case GatherKind::TILED: gl = plan_gather_tiled(e, in, out, un, s_mod); break;
+        case GatherKind::LAPS: gl = plan_gather_laps(e, in, out, un, s_mod); break;
+        case GatherKind::ONESHOT: gl = plan_gather_oneshot(e, in, out, un, s_mod); break;
+        case GatherKind::STRIDE:
+            if ((ce = plan_gather_stride(e, dev, sms, in, out, un, s_mod, &gl)) != cudaSuccess) return cuda_fail(ce);
+            break;
     }
-    const bool oneshot = sched != EW_SCHED_PERSISTENT && un <= (uint64_t(1) << 32);
-    const bool small_stride = s_mod >= 2 && s_mod <= kMaxLaps;
-    // AUTO: lap order while a warp's strided load still shares 32-byte
-    // sectors (s < 32 / E); from there on every lane's load is its own sector,
-    // L2 traffic bounds lap order, and the tiled kernel takes over
-    const bool tiled = sched == EW_SCHED_TILED ||
-                       (sched == EW_SCHED_AUTO && s_mod >= static_cast<uint64_t>(32 / elem_size(dt)));
-    if (oneshot && small_stride && tiled) {
-        const int e = elem_size(dt);
-        const GatherEntry *gt = e == 4 ? gather_tiled_4() : gather_tiled_2();
-        GatherArgs ga{in, out, un, s_mod, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
-        const uint32_t per_block = (kTiledSpanBytes / e) / static_cast<uint32_t>(s_mod);
-        uint32_t log2p = 0;
-        while ((2u << log2p) <= per_block) ++log2p;  // largest power of two <= per_block
-        ga.tile_p = 1u << log2p;
-        ga.tile_log2p = log2p;
-        ga.tile_pitch = ga.tile_p + tiled_pad_words(static_cast<uint32_t>(s_mod), e) * (4 / e);
-        ga.lap_q = static_cast<uint32_t>(un / s_mod);
-        ga.lap_m = static_cast<uint32_t>(un % s_mod);
-        ga.div_magic = static_cast<uint32_t>((uint64_t(1) << 32) / s_mod + 1);
-        const uint64_t lap_len = (un + s_mod - 1) / s_mod;
-        const int grid = clamp_grid(static_cast<int64_t>((lap_len + ga.tile_p - 1) / ga.tile_p));
-        ce = gt->launch(ga, grid, reinterpret_cast<cudaStream_t>(s));
-        if (ce != cudaSuccess) return cuda_fail(ce);
-        t_last.launches = 1;
-        t_last.path = EW_PATH_SCALAR;
-        t_last.vec_bytes = e;
-        t_last.grid = grid;
-        t_last.block = kBlock;
-        t_last.smem = static_cast<int32_t>(s_mod * ga.tile_pitch * e);
-        t_last.schedule = EW_SCHED_TILED;
-        t_last.nvec = n;
-        return EW_OK;
-    }
-    const bool lap_order = oneshot && sched != EW_SCHED_ONESHOT;
-    GatherArgs ga{in, out, un, s_mod, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
-    const GatherEntry *g;
-    int grid;
-    const bool four = elem_size(dt) == 4;
-    const GatherEntry *laps = four ? gather_laps_4() : gather_laps_2();
-    const uint64_t lap_block = static_cast<uint64_t>(kBlock) * laps->unroll;
-    const bool lapped = lap_order && s_mod >= 2 && s_mod <= kMaxLaps && un / s_mod >= lap_block;
-    if (lapped) {
-        // lap order: block b takes chunk b / s of lap b mod s
-        g = laps;
-        const uint64_t lap_len = (un + s_mod - 1) / s_mod;  // the longest lap
-        grid = clamp_grid(static_cast<int64_t>(s_mod * ((lap_len + lap_block - 1) / lap_block)));
-        ga.lap_q = static_cast<uint32_t>(un / s_mod);
-        ga.lap_m = static_cast<uint32_t>(un % s_mod);
-        ga.div_magic = static_cast<uint32_t>((uint64_t(1) << 32) / s_mod + 1);
-    } else if (oneshot) {
-        g = four ? gather_oneshot_4() : gather_oneshot_2();
-        const int64_t per_block = static_cast<int64_t>(kBlock) * g->unroll;
-        grid = clamp_grid((n + per_block - 1) / per_block);
-        ga.step_mod = (s_mod * static_cast<uint64_t>(kBlock)) % un;  // s_mod < 2^32
-        ga.barrett_m = ~uint64_t(0) / un;
-    } else {
-        g = four ? gather_stride_4() : gather_stride_2();
-        int occ = 1;
-        ce = blocks_per_sm(dev, g->kernel, kBlock, 0, &occ);
-        if (ce != cudaSuccess) return cuda_fail(ce);
-        const int64_t per_block = static_cast<int64_t>(kBlock) * g->unroll;
-        grid = clamp_grid(std::min<int64_t>((n + per_block - 1) / per_block, int64_t(sms) * occ));
-        const uint64_t nthr = static_cast<uint64_t>(grid) * kBlock;
-        ga.step_mod = static_cast<uint64_t>((static_cast<unsigned __int128>(s_mod) * nthr) % un);
-    }
-    ce = g->launch(ga, grid, reinterpret_cast<cudaStream_t>(s));
+    ce = gl.entry->launch(gl.args, gl.grid, reinterpret_cast<cudaStream_t>(s));
     if (ce != cudaSuccess) return cuda_fail(ce);
     t_last.launches = 1;
-    t_last.path = EW_PATH_SCALAR;
-    t_last.vec_bytes = elem_size(dt);
-    t_last.grid = grid;
+    t_last.path = gl.path;
+    t_last.vec_bytes = gl.vec_bytes;
+    t_last.grid = gl.grid;
     t_last.block = kBlock;
-    t_last.schedule = lapped ? EW_SCHED_LAPS : oneshot ? EW_SCHED_ONESHOT : EW_SCHED_PERSISTENT;
-    t_last.nvec = n;
+    t_last.smem = gl.smem;
+    t_last.schedule = gl.schedule;
+    t_last.head = gl.head;
+    t_last.nvec = gl.nvec;
+    t_last.tail = gl.tail;
     return EW_OK;
 }
 
