@@ -148,11 +148,11 @@ typedef enum {
  *                     all s laps draw from (32 KiB) once, coalesced, into
  *                     shared memory with one row per residue mod s, then
  *                     writes each lap's outputs as one coalesced run.
- * EW_SCHED_AUTO       for the gather: EW_SCHED_LAPS while s < 32 / (element
- *                     size), where a warp's strided load still shares 32-byte
- *                     sectors; EW_SCHED_TILED from there up to s = 64.  For
- *                     the other operators, EW_SCHED_ONESHOT.  A gather with
- *                     n > 2^32 always runs persistent. */
+ * EW_SCHED_AUTO       for the gather: EW_SCHED_LAPS for s < 8, EW_SCHED_TILED
+ *                     for 8 <= s <= 64 (the measured crossover: from s = 8 a
+ *                     lap-ordered fp32 warp load spends one 32-byte sector per
+ *                     lane).  For the other operators, EW_SCHED_ONESHOT.  A
+ *                     gather with n > 2^32 always runs persistent. */
 typedef enum {
     EW_SCHED_AUTO = 0,
     EW_SCHED_ONESHOT = 1,

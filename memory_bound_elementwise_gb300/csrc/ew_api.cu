@@ -436,6 +436,13 @@ enum class GatherKind { SPAN, TILED, LAPS, ONESHOT, STRIDE };
 
 constexpr uint64_t kOneshotMaxN = uint64_t(1) << 32;  // the 32-bit index kernels
 
+// AUTO's crossover from lap order to the tiled kernel.  Lap order issues one
+// load per output: from s = 8 each fp32 lane's load is its own 32-byte sector
+// (L2-to-SM traffic bounds it), and 16-bit lanes move 2 bytes per load.  The
+// tiled kernel reads 16 bytes per load at any s; measured on GB300 it wins
+// from s = 8 for both element sizes (from s = 5 for 16-bit ones, narrowly).
+constexpr uint64_t kTiledMinStride = 8;
+
 GatherArgs gather_args(const void *in, void *out, uint64_t n, uint64_t s_mod) {
     GatherArgs a{};
     a.in = in;
@@ -455,8 +462,7 @@ void set_lap_geometry(GatherArgs *a, uint64_t n, uint64_t s_mod) {
 
 // Which gather kernel runs, from the path and schedule selections:
 //   span     EW_PATH_V256 chosen explicitly: 4-byte elements, s = 2 or 4;
-//   tiled    EW_SCHED_TILED, or AUTO from s = 32 / E (every lane of a strided
-//            warp load is then its own 32-byte sector), for 2 <= s <= 64;
+//   tiled    EW_SCHED_TILED, or AUTO from s = kTiledMinStride, for s <= 64;
 //   laps     AUTO below that, or EW_SCHED_LAPS, once every lap holds a block;
 //   oneshot  index order, one block per chunk (n <= 2^32);
 //   stride   index order, grid-stride (EW_SCHED_PERSISTENT, or n > 2^32).
@@ -467,7 +473,7 @@ GatherKind choose_gather(int e, uint64_t n, uint64_t s_mod) {
     if (path == EW_PATH_V256 && e == 4 && (s_mod == 2 || s_mod == 4) && small_n) return GatherKind::SPAN;
     if (sched == EW_SCHED_PERSISTENT || !small_n) return GatherKind::STRIDE;
     const bool small_stride = s_mod >= 2 && s_mod <= kMaxLaps;
-    const bool tiled = sched == EW_SCHED_TILED || (sched == EW_SCHED_AUTO && s_mod >= static_cast<uint64_t>(32 / e));
+    const bool tiled = sched == EW_SCHED_TILED || (sched == EW_SCHED_AUTO && s_mod >= kTiledMinStride);
     if (small_stride && tiled) return GatherKind::TILED;
     const GatherEntry *laps = e == 4 ? gather_laps_4() : gather_laps_2();
     const uint64_t lap_block = static_cast<uint64_t>(kBlock) * laps->unroll;

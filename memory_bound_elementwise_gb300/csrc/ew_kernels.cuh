@@ -294,16 +294,26 @@ __global__ void __launch_bounds__(kBlock) gather_tiled_kernel(const GatherArgs g
         }
     }
     __syncthreads();
-    uint32_t cur = ~0u, first = 0, len = 0, row = 0;
-    for (uint32_t k = threadIdx.x; k < span; k += kBlock) {
-        const uint32_t L = k >> g.tile_log2p, q = k & (P - 1);
-        if (L != cur) {  // warp-uniform: P >= 32
-            cur = L;
-            first = lap_start[L] + p0;
-            len = lap_len[L] > p0 ? lap_len[L] - p0 : 0;
-            row = lap_row[L];
+    if (P >= 2 * kBlock) {  // lap by lap: the block walks each lap's run
+        for (uint32_t L = 0; L < s; ++L) {
+            const uint32_t len = lap_len[L] > p0 ? min(lap_len[L] - p0, P) : 0;
+            W *dst = out + lap_start[L] + p0;
+            const W *row = tile + lap_row[L];
+#pragma unroll 4
+            for (uint32_t q = threadIdx.x; q < len; q += kBlock) dst[q] = row[q];
         }
-        if (q < len) out[static_cast<size_t>(first + q)] = tile[row + q];
+    } else {  // fewer positions than threads: kBlock / P laps side by side
+        uint32_t cur = ~0u, first = 0, len = 0, row = 0;
+        for (uint32_t k = threadIdx.x; k < span; k += kBlock) {
+            const uint32_t L = k >> g.tile_log2p, q = k & (P - 1);
+            if (L != cur) {  // warp-uniform: P >= 32
+                cur = L;
+                first = lap_start[L] + p0;
+                len = lap_len[L] > p0 ? lap_len[L] - p0 : 0;
+                row = lap_row[L];
+            }
+            if (q < len) out[static_cast<size_t>(first + q)] = tile[row + q];
+        }
     }
 }
 

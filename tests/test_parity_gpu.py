@@ -259,12 +259,12 @@ def _gather_laps(n, s):
 
 
 def _gather_auto_schedule(n, s, dtype):
-    """The schedule AUTO picks: tiled from s = 32 / element size up to 64,
-    lap order below it where every lap holds a block, else index order."""
+    """The schedule AUTO picks: tiled from s = 8 up to 64, lap order below it
+    where every lap holds a block, else index order."""
     sm = s % n
     if n > 1 << 32:
         return 2
-    if 32 // ESIZE[dtype] <= sm <= 64:
+    if 8 <= sm <= 64:
         return 4
     return 3 if _gather_laps(n, s) else 1
 
@@ -476,7 +476,7 @@ def test_gather_small(dtype):
 
 @pytest.mark.parametrize("dtype", ["f32", "f16"])
 def test_gather_lap_order(dtype):
-    """The lap-ordered gather (schedule 'laps'; AUTO's choice below s = 32 / E)
+    """The lap-ordered gather (schedule 'laps'; AUTO's choice below s = 8)
     for strides 2..64 once every lap holds a block of outputs: sizes at, just below and just above the
     threshold n = 2048 s, laps of unequal length (s not dividing n), laps that
     read the same sources (s | n) and laps on distinct residues (s coprime to
