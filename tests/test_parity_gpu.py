@@ -742,6 +742,27 @@ def test_gather_tiled(dtype):
             assert bi.guards_intact() and bo.guards_intact()
 
 
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16", "i32"])
+def test_gather_auto_crossover(dtype):
+    """AUTO's choice around its crossovers: lap order below s = 8, the tiled
+    kernel from 8 to 64 (wide tiles store lap by lap, narrow ones side by
+    side), index order from 65; each against the oracle."""
+    L = ew.lib()
+    ew.set_schedule("auto")
+    n = 300_007
+    x = inputs.random_bits(n, "f32" if dtype == "i32" else dtype, 7300 + len(dtype))
+    for s in (6, 7, 8, 9, 16, 24, 32, 48, 64, 65):
+        bi = GuardedBuffer(n, dtype, 0).fill(x)
+        bo = GuardedBuffer(n, dtype, 2)
+        assert L.ew_gather_stride(DT_CODE[dtype], bi.view.data_ptr(), bo.view.data_ptr(), n, s, _stream()) == 0
+        rec = ew.last_launch()
+        assert rec["schedule"] == _gather_auto_schedule(n, s, dtype if dtype != "i32" else "f32"), (s, rec)
+        torch.cuda.synchronize()
+        assert_bits_equal(bo.host(), oracle.gather_stride(x, s), "f32" if dtype == "i32" else dtype, False,
+                          "auto gather %s s=%d" % (dtype, s))
+        assert bi.guards_intact() and bo.guards_intact()
+
+
 @pytest.mark.parametrize("schedule", ["laps", "tiled"])
 @pytest.mark.parametrize("n,s", [(1 << 32, 2), ((1 << 32) - 1, 3), (1 << 32, 64), ((1 << 32) - 7, 5)])
 def test_gather_lap_order_at_2p32_int32(n, s, schedule):
