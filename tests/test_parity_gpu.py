@@ -6,7 +6,9 @@ alignment offset; output buffers carry guard zones that must stay untouched.
 The full-size cases are the measured workloads: fp32 add at 2^20+3 and 2^28,
 fp32 SAXPY at 32M in place, bf16/fp16 add at 2^28 (aligned and offset by one
 element), fp32 ReLU at 2^28 (out of place and in place), fp32 copy and
-stride-2 gather at 2^26.
+stride-2 gather at 2^26; and the bench's further workloads: bf16 add at
+2^28 with pointers of different parity, fused SAXPY + ReLU at 2^28 and the
+stride-16 gather at 2^26.
 The bar is bit-exact; NaN results of arithmetic compare as "both NaN".
 """
 import numpy as np
@@ -625,6 +627,47 @@ def test_config_add_16bit_2p28(dtype, offset):
     rec = _full("add", dtype, 1 << 28, inputs.seed_for("add_16"), inputs.seed_for("add_16", 1),
                 offset=offset, dist="normal")
     assert rec["head"] == (15 if offset else 0)
+
+
+def test_bf16_add_2p28_pointers_of_different_parity():
+    """The bench's mixed-parity workload at full size: bf16 add of 2^28
+    elements with A, B and C at +1, +0 and +3 elements, which AUTO sends to the
+    realigning bulk copy; every output against the oracle."""
+    n = 1 << 28
+    x = inputs.as_dtype(inputs.normal(n, inputs.seed_for("add_16")), "bf16")
+    y = inputs.as_dtype(inputs.normal(n, inputs.seed_for("add_16", 1)), "bf16")
+    ba, bb, bc = GuardedBuffer(n, "bf16", 1).fill(x), GuardedBuffer(n, "bf16", 0).fill(y), GuardedBuffer(n, "bf16", 3)
+    run_op("add", "bf16", [ba, bb, bc], n)
+    rec = ew.last_launch()
+    assert rec["path"] == 4 and rec["head"] + rec["nvec"] * 4096 + rec["tail"] == n, rec
+    torch.cuda.synchronize()
+    assert_bits_equal(bc.host(), oracle.add("bf16", x, y), "bf16", True, "bf16 add 2^28 mixed parity")
+    assert ba.guards_intact() and bb.guards_intact() and bc.guards_intact()
+
+
+def test_saxpy_relu_f32_2p28():
+    """The bench's fused SAXPY + ReLU workload at full size (alpha = 2.5)."""
+    n = 1 << 28
+    x = inputs.normal(n, inputs.seed_for("saxpy_f32", 2))
+    y = inputs.normal(n, inputs.seed_for("saxpy_f32", 3))
+    bx, by = GuardedBuffer(n, "f32").fill(x), GuardedBuffer(n, "f32").fill(y)
+    run_op("saxpy_relu", "f32", [bx, by], n)
+    torch.cuda.synchronize()
+    assert_bits_equal(by.host(), oracle.relu("f32", oracle.saxpy("f32", 2.5, x, y)), "f32", True,
+                      "saxpy_relu 2^28")
+    assert by.guards_intact()
+
+
+def test_gather_stride16_f32_2p26():
+    """The bench's stride-16 gather at full size, through AUTO's tiled kernel."""
+    n = 1 << 26
+    x = inputs.uniform(n, inputs.seed_for("copy_f32"), 0.0, 1.0)
+    bi, bo = GuardedBuffer(n, "f32").fill(x), GuardedBuffer(n, "f32")
+    assert ew.lib().ew_gather_stride(0, bi.view.data_ptr(), bo.view.data_ptr(), n, 16, _stream()) == 0
+    assert ew.last_launch()["schedule"] == 4
+    torch.cuda.synchronize()
+    assert_bits_equal(bo.host(), oracle.gather_stride(x, 16), "f32", False, "gather 16 2^26")
+    assert bo.guards_intact() and bi.guards_intact()
 
 
 @pytest.mark.parametrize("inplace", [False, True])
