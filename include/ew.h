@@ -47,14 +47,16 @@
  *              allocates no memory and keeps no reference after a call returns.
  *              Each pointer must be aligned to the element size (4 bytes for
  *              EW_F32 and EW_I32, 2 for EW_F16/EW_BF16), else
- *              EW_ERR_INVALID_VALUE.  Any
- *              such alignment is accepted; the widest vector width that all the
- *              pointers of a call share is used (see ew_plan_query).
+ *              EW_ERR_INVALID_VALUE.  Any such alignment is accepted; the
+ *              widest vector width that all the pointers of a call share is
+ *              used, or, for 16-bit pointers of different parity from
+ *              n = 2^22 on device memory, the realigning bulk copy (see
+ *              EW_PATH_TMA and ew_plan_query).
  *   Layout     n contiguous elements, index 0 first.
  *   n          element count.  n == 0 returns EW_OK and launches nothing;
  *              n < 0 is EW_ERR_INVALID_VALUE.
  *   Aliasing   an output may be *identical* to an input (in-place add, saxpy
- *              with x == y, relu, copy).  Any other overlap of an output's byte
+ *              and saxpy_relu with x == y, relu, copy).  Any other overlap of an output's byte
  *              range with an input's is EW_ERR_OVERLAP.  ew_gather_stride
  *              accepts no overlap at all.
  *   Streams    every call enqueues at most one kernel on `stream` (NULL = the
