@@ -846,6 +846,42 @@ def test_gather_lap_order_at_2p32_int32(n, s, schedule):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("schedule,s", [("laps", 2), ("laps", 5), ("tiled", 3), ("tiled", 16), ("tiled", 64)])
+def test_gather_at_2p32_16bit_low_index_bits(schedule, s):
+    """The 2-byte lap-ordered and tiled gathers at n = 2^32: element j holds the
+    low 16 bits of j, so every output must equal the low 16 bits of
+    (s*i) mod n; all 2^32 outputs are compared chunk by chunk (int64 on the
+    device), and lap boundaries and random positions against the oracle's
+    128-bit index map."""
+    n = 1 << 32
+    chunk = 1 << 28
+    tin = torch.empty(n, dtype=torch.int16, device="cuda")
+    for lo in range(0, n, chunk):
+        v = torch.arange(lo, lo + chunk, dtype=torch.int64, device="cuda")
+        tin[lo:lo + chunk] = ((v & 0xFFFF) - ((v & 0x8000) << 1)).to(torch.int16)
+        del v
+    tout = torch.empty_like(tin)
+    ew.set_schedule(schedule)
+    assert ew.lib().ew_gather_stride(1, tin.data_ptr(), tout.data_ptr(), n, s, _stream()) == 0
+    assert ew.last_launch()["schedule"] == (3 if schedule == "laps" else 4)
+    torch.cuda.synchronize()
+    for lo in range(0, n, chunk):
+        want = (torch.arange(lo, lo + chunk, dtype=torch.int64, device="cuda") * s % n) & 0xFFFF
+        got = tout[lo:lo + chunk].to(torch.int64) & 0xFFFF
+        assert torch.equal(got, want), "chunk at %d" % lo
+        del want, got
+    g = inputs.rng(8400 + s)
+    bounds = [-(-lap * n // s) for lap in range(s + 1)]
+    idx = sorted({int(i) for b in bounds for i in (b - 1, b, b + 1) if 0 <= i < n}
+                 | set(range(0, 100)) | set(range(n - 100, n))
+                 | {int(i) for i in g.integers(0, n, size=1000, dtype=np.int64)})
+    got = tout[torch.tensor(idx, dtype=torch.int64, device="cuda")].cpu().numpy().view(np.uint16)
+    want = np.array([oracle.gather_index(i, s, n) & 0xFFFF for i in idx], dtype=np.uint16)
+    assert np.array_equal(got, want)
+    del tin, tout
+    torch.cuda.empty_cache()
+
+
 def _random_i32(n, seed):
     g = inputs.rng(seed)
     x = g.integers(-2 ** 31, 2 ** 31, size=n, dtype=np.int64).astype(np.int32)
