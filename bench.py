@@ -19,7 +19,8 @@ A and B i.i.d. uniform[-1, 1) from a seeded generator.  A step is one call of
               one GPU only); its output is also compared with the GPU's.  An
               all-cores figure (one slice per host core) is reported beside it.
 * aux         the other measured workloads (bf16/fp16 add at 2^28 aligned,
-              offset by one element and with pointers of different parity,
+              offset by one element and with pointers of different parity;
+              bf16/fp16 SAXPY, ReLU and both fused chains at 2^28;
               SAXPY 32M, ReLU 2^28 out of place and in place, fused add+ReLU
               and SAXPY+ReLU against the unfused pairs, copy and gathers at
               strides 2, 4 and 16 at 2^26 in each block order, fp32 add at
@@ -462,6 +463,18 @@ def aux_measurements(torch, ew, inputs, metrics, stream, peak, dev):
             record("add_%s_2p28_off%d" % (dtype, off), "add", dtype, n28,
                    lambda: L.ew_add(code, pa, pb, pc, n28, s))
             del ra, rb, rc
+        # the other operators on the same 16-bit arrays: SAXPY in place (on B),
+        # ReLU out of place, and the two fused chains
+        ra, pa = dev_of(xa, dtype, 0)
+        rb, pb = dev_of(xb, dtype, 0)
+        rc, pc = dev_of(np.zeros_like(xa), dtype, 0)
+        record("saxpy_%s_2p28_inplace" % dtype, "saxpy", dtype, n28, lambda: L.ew_saxpy(code, 2.5, pa, pb, n28, s))
+        record("relu_%s_2p28" % dtype, "relu", dtype, n28, lambda: L.ew_relu(code, pa, pc, n28, s))
+        record("add_relu_%s_2p28_fused" % dtype, "add_relu", dtype, n28,
+               lambda: L.ew_add_relu(code, pa, pb, pc, n28, s))
+        record("saxpy_relu_%s_2p28_fused" % dtype, "saxpy_relu", dtype, n28,
+               lambda: L.ew_saxpy_relu(code, 2.5, pa, pc, n28, s))
+        del ra, rb, rc
         if dtype == "bf16":
             # pointers of different parity (A +1, B +0, C +3 elements): the
             # realigning bulk-copy kernel (default) against 2-byte accesses
