@@ -1,7 +1,9 @@
-"""Every pair of 16-bit operands through the GPU's packed add and its SAXPY
-(alpha = 2.5, the pages' coefficient): 2^32 pairs per format and operator, in
-16 launches of 2^28, compared with the oracle bit for bit; NaN results compare
-as "both NaN".  About 35 s per operator on a GB300 with a 16-core host.
+"""Every pair of 16-bit operands through the GPU's packed add, its SAXPY
+(alpha = 2.5, the pages' coefficient) and the fused SAXPY + ReLU: 2^32 pairs
+per format and operator, in 16 launches of 2^28, compared with the oracle bit
+for bit (for the fused operator: the oracle's saxpy, then its relu); NaN
+results compare as "both NaN".  About 35 s per operator on a GB300 with a
+16-core host.
 
 The oracle runs in a pool of worker processes started with "spawn" (never
 forked from a process that has touched the GPU).
@@ -35,10 +37,12 @@ def _oracle_slice(args):
     b = np.repeat(bvals, allp.size)
     if op == "add":
         return oracle.add(dtype, a, b)
+    if op == "saxpy_relu":
+        return oracle.relu(dtype, oracle.saxpy(dtype, ALPHA, a, b))
     return oracle.saxpy(dtype, ALPHA, a, b)  # x = every pattern, y = B
 
 
-@pytest.mark.parametrize("op", ["add", "saxpy"])
+@pytest.mark.parametrize("op", ["add", "saxpy", "saxpy_relu"])
 @pytest.mark.parametrize("dtype,code", [("f16", 1), ("bf16", 2)])
 def test_all_operand_pairs(op, dtype, code):
     workers = min(16, os.cpu_count() or 4)
@@ -55,9 +59,12 @@ def test_all_operand_pairs(op, dtype, code):
             b = bvals.repeat_interleave(1 << 16)
             if op == "add":
                 assert L.ew_add(code, a.data_ptr(), b.data_ptr(), c.data_ptr(), PER, s) == 0
-            else:
+            elif op == "saxpy":
                 c.copy_(b)
                 assert L.ew_saxpy(code, ALPHA, a.data_ptr(), c.data_ptr(), PER, s) == 0
+            else:
+                c.copy_(b)
+                assert L.ew_saxpy_relu(code, ALPHA, a.data_ptr(), c.data_ptr(), PER, s) == 0
             step = B_PER_CHUNK // workers
             parts = pool.map(_oracle_slice, [(op, dtype, b_lo + k * step, b_lo + (k + 1) * step)
                                              for k in range(workers)])
