@@ -1,11 +1,16 @@
 """Benchmark: achieved HBM bandwidth of the elementwise kernels on GB300.
 
-Headline (one JSON line on stdout): fp32 add C = A + B at N = 2^28 per GPU,
-A and B i.i.d. uniform[-1, 1) from a seeded generator.  A step is one call of
-``ew_add`` over the whole array (dispatch, vector body, scalar head/tail).
+Output: two JSON lines on stdout.  The first, ``{"aux_of": METRIC, ...}``,
+holds every other measured workload; the LAST line is the compact headline
+(well under 4 KB), so a reader that keeps only the tail of stdout still has it.
+
+Headline: fp32 add C = A + B at N = 2^28 per GPU, A and B i.i.d.
+uniform[-1, 1) from a seeded generator.  A step is one call of ``ew_add`` over
+the whole array (dispatch, vector body, scalar head/tail).
 
 * value       algorithmic bytes (12 per element: read A, read B, write C) of
               all steps on all ranks / max over ranks of the timed region.
+              Withheld (null) when the output differs from the CPU oracle.
 * roofline    the same bytes per launch / the mean kernel duration (CUDA events
               around every launch on the launching stream), against the measured
               copy bandwidth of this GPU model.
@@ -14,26 +19,35 @@ A and B i.i.d. uniform[-1, 1) from a seeded generator.  A step is one call of
               A and B host->device and C device->host inside the kernel, over
               the CPU-GPU link.  Staged variants (cudaMemcpyAsync in, kernel on
               device copies, cudaMemcpyAsync out; serial, and chunked on three
-              streams) are reported beside it.
+              streams) are reported in the aux line.
 * cpu_baseline  the CPU oracle, single-threaded, on the same inputs (rank 0,
               one GPU only); its output is also compared with the GPU's.  An
               all-cores figure (one slice per host core) is reported beside it.
-* aux         the other measured workloads (bf16/fp16 add at 2^28 aligned,
-              offset by one element and with pointers of different parity;
-              bf16/fp16 SAXPY, ReLU and both fused chains at 2^28;
-              SAXPY 32M, ReLU 2^28 out of place and in place, fused add+ReLU
-              and SAXPY+ReLU against the unfused pairs, copy and gathers at
-              strides 2, 4 and 16 at 2^26 in each block order, fp32 add at
-              2^20+3, the headline
-              through the persistent schedule and the bulk-copy path, and the
-              library device-to-device copy): GB/s, fraction of the measured
-              peak, of 8 TB/s and of the copy ceiling measured in the same
-              run, mean, median and minimum per launch.  SAXPY 32M and the
-              2^26 copy and gather are also timed as 50 launches captured in
-              one CUDA graph, which separates the host launch gaps.
+* clocks      SM clock and clock-event reasons read through NVML while the
+              timed launches execute (the nvidia-smi stream over the whole run
+              as a fallback).
+* aux line    the other workloads (bf16/fp16 add at 2^28 aligned, offset by one
+              element and with pointers of different parity; bf16/fp16 SAXPY,
+              ReLU and both fused chains at 2^28; SAXPY 32M, 2^26 and 2^28;
+              ReLU 2^28 out of place and in place; fused add+ReLU and
+              SAXPY+ReLU against the unfused pairs; copy and gathers at strides
+              2, 4 and 16 at 2^26 in each block order; the even/odd select;
+              fp32 add at 2^20+3; the headline through the persistent schedule
+              and the bulk-copy path; chains of short SAXPY calls; the library
+              device-to-device copy).  Every entry's output is compared with
+              the CPU oracle after its timed launches (in full up to 2^26
+              elements, else its first and last 2^20 elements and four seeded
+              2^20-element windows); an entry that differs reports
+              "parity": "MISMATCH" and no speed.  Entries whose bytes fit in L2
+              are labelled "l2_resident" and carry no fraction of HBM peak.
+
+The CPU oracle is imported only by the cpu_baseline leg, the parity checks
+beside it and the reference arm; nothing on the timed path calls it.
 
 ``--impl reference`` times the CPU oracle instead (the reference arm), on a
 bounded sample of the same workload per step.
+``--ab widths`` times 16-byte against 32-byte accesses (add, SAXPY, ReLU, copy
+in fp32 and bf16 at 2^26 and 2^28), interleaved launch by launch.
 Multi-GPU (torchrun): every rank runs its own 2^28-element slice of a
 world x 2^28 problem (weak scaling, no collective on the data path).
 """
@@ -63,9 +77,15 @@ N_HEADLINE = 1 << 28
 PAGE_BASELINE = {"value": 1576.5, "unit": "GB/s", "hardware": "RTX 5090 (GDDR7)",
                  "kernel": "V1 FP32 scalar add, N = 268.4M"}
 FALLBACK_HBM_GBS = 6800.0
+HEADLINE_MAX_BYTES = 4096
+# outputs up to this many elements are compared in full; larger ones on windows
+PARITY_FULL_MAX = 1 << 26
+PARITY_WINDOW = 1 << 20
+ESIZE = {"f32": 4, "f16": 2, "bf16": 2, "i32": 4}
+DT_CODE = {"f32": 0, "f16": 1, "bf16": 2, "i32": 3}
 
 
-def parse():
+def parse(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=2000)
@@ -73,17 +93,22 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--n", type=int, default=N_HEADLINE, help="elements per GPU (headline: 2^28)")
     p.add_argument("--no-aux", action="store_true", help="skip the other workloads")
-    p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    p.add_argument("--no-cpu", action="store_true",
+                   help="skip the CPU oracle baseline (the headline is then checked on windows)")
     p.add_argument("--path", default="auto", help="kernel variant: auto, scalar, v128, v256, tma")
-    p.add_argument("--schedule", default="auto", help="block schedule: auto, oneshot, persistent, laps")
+    p.add_argument("--schedule", default="auto", help="block schedule: auto, oneshot, persistent, laps, tiled")
     p.add_argument("--profile-case", default=None, choices=sorted(PROFILE_CASES),
                    help="run only warmup+steps launches of one workload at --n (for ncu captures)")
-    return p.parse_args()
+    p.add_argument("--stride", type=int, default=None, help="gather stride for the gather profile cases")
+    p.add_argument("--ab", default=None, choices=["widths", "gather"],
+                   help="A/B timing instead of the benchmark: access widths, or gather schedules by stride")
+    return p.parse_args(argv)
 
 
 # op, dtype, element offset of every pointer (or of A, B, C)
 PROFILE_CASES = {
     "add_f32": ("add", "f32", 0),
+    "add_bf16": ("add", "bf16", 0),
     "add_bf16_off1": ("add", "bf16", 1),
     "saxpy_f32": ("saxpy", "f32", 0),
     "relu_f32": ("relu", "f32", 0),
@@ -95,6 +120,7 @@ PROFILE_CASES = {
     "gather2_span_f32": ("gather_span", "f32", 0),
     "add_bf16_mixed": ("add", "bf16", (1, 0, 3)),
     "gather16_f32": ("gather16", "f32", 0),
+    "gather16_bf16": ("gather16", "bf16", 0),
     "saxpy_relu_f32": ("saxpy_relu", "f32", 0),
 }
 
@@ -110,7 +136,7 @@ def run_profile_case(args):
     ew.set_path(args.path)
     ew.set_schedule(args.schedule)
     n = args.n
-    e = 4 if dtype == "f32" else 2
+    e = ESIZE[dtype]
     dev = torch.device("cuda", 0)
 
     offs = off if isinstance(off, tuple) else (off, off, off)  # A (x), B (y), C (z)
@@ -126,17 +152,18 @@ def run_profile_case(args):
     rz, pz = buf(np.zeros_like(x), offs[2])
     L = ew.lib()
     s = torch.cuda.current_stream().cuda_stream
-    code = {"f32": 0, "f16": 1, "bf16": 2}[dtype]
+    code = DT_CODE[dtype]
+    stride = args.stride if args.stride else (16 if op == "gather16" else 2)
     call = {"add": lambda: L.ew_add(code, px, py, pz, n, s),
             "saxpy": lambda: L.ew_saxpy(code, 2.5, px, py, n, s),
             "relu": lambda: L.ew_relu(code, px, pz, n, s),
             "copy": lambda: L.ew_copy(code, px, pz, n, s),
-            "gather": lambda: L.ew_gather_stride(code, px, pz, n, 2, s),
+            "gather": lambda: L.ew_gather_stride(code, px, pz, n, stride, s),
             "add_relu": lambda: L.ew_add_relu(code, px, py, pz, n, s),
             "relu_inplace": lambda: L.ew_relu(code, px, px, n, s),
             "select": lambda: L.ew_select_even_odd(3, px, pz, n, s),
-            "gather_span": lambda: L.ew_gather_stride(code, px, pz, n, 2, s),
-            "gather16": lambda: L.ew_gather_stride(code, px, pz, n, 16, s),
+            "gather_span": lambda: L.ew_gather_stride(code, px, pz, n, stride, s),
+            "gather16": lambda: L.ew_gather_stride(code, px, pz, n, stride, s),
             "saxpy_relu": lambda: L.ew_saxpy_relu(code, 2.5, px, py, n, s)}[op]
     if op == "gather_span":
         ew.set_path("v256")
@@ -145,8 +172,8 @@ def run_profile_case(args):
         if st != 0:
             raise ew.EwError(st, args.profile_case)
     torch.cuda.synchronize()
-    print(json.dumps({"profile_case": args.profile_case, "n": n, "launches": args.warmup + args.steps,
-                      "launch": ew.last_launch()}))
+    print(json.dumps({"profile_case": args.profile_case, "n": n, "stride": stride if "gather" in op else None,
+                      "launches": args.warmup + args.steps, "launch": ew.last_launch()}))
 
 
 # ---------------------------------------------------------------- helpers
@@ -163,14 +190,14 @@ def measured_peak():
     try:
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs: %s)" % d.get("how", "")[:60]
+        return float(d["hbm_gbs"]), "measured hbm_gbs (copy, read+write bytes)"
     except Exception:
-        return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
+        return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no measured peaks file)"
 
 
-def profiled_traffic(kernel_key):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources; else None."""
+def profiled_entry(key):
+    """An entry of the committed ncu summary (profiles/traffic.json) if it was
+    taken on the current kernel sources; else (None, reason)."""
     from memory_bound_elementwise_gb300 import _build
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
@@ -178,16 +205,37 @@ def profiled_traffic(kernel_key):
             d = json.load(f)
     except Exception:
         return None, "no profiles/traffic.json"
-    ent = d.get(kernel_key)
+    ent = d.get(key)
     if not ent:
         return None, "kernel not profiled"
     if ent.get("source_digest") != _build.source_digest():
         return None, "kernel sources changed since the ncu capture"
-    return ent.get("dram_bytes_per_launch"), ent.get("note", "")
+    return ent, ent.get("note", "")
+
+
+def profiled_traffic(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    ent, note = profiled_entry(kernel_key)
+    if ent is None:
+        return None, note
+    return ent.get("dram_bytes_per_launch"), note
+
+
+def profiled_sectors():
+    """Global-load sectors per request of the stride-2 gather and of the
+    contiguous copy, from the committed ncu summary; None when the kernel
+    sources changed since it was taken."""
+    ent, note = profiled_entry("sectors_per_request")
+    if ent is None:
+        return {"gather": None, "copy": None, "note": note}
+    return {"gather": ent.get("gather2_f32"), "copy": ent.get("copy_f32"),
+            "metric": ent.get("metric"), "note": note}
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples every 100 ms while running."""
+    """nvidia-smi clock/throttle samples every 100 ms while running (the whole
+    run; the timed region itself is sampled through NVML, see NvmlClocks)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -245,6 +293,67 @@ class ClockSampler:
                 "window": "timed region" if inside else "whole run (timed region shorter than the sampling interval)"}
 
 
+# NVML clock-event reason bits (nvml.h, nvmlClocksEventReason*)
+NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
+def summarize_nvml_samples(samples, max_mhz):
+    """samples: [(sm_mhz, reason_bits)] taken while the timed launches ran."""
+    if not samples:
+        return None
+    reasons = sorted({name for _, bits in samples for bit, name in NVML_REASONS.items() if bits & bit})
+    return {"sm_mhz": statistics.median(m for m, _ in samples), "sm_max_mhz": max_mhz,
+            "sm_mhz_min": min(m for m, _ in samples), "reasons": reasons, "samples": len(samples),
+            "window": "timed region", "source": "NVML, polled while the timed launches executed"}
+
+
+class NvmlClocks:
+    """SM clock and clock-event reasons through NVML (the driver's
+    libnvidia-ml.so.1, by ctypes), read only.  Polled by the host while the
+    GPU executes the timed launches, so every sample lies inside the timed
+    region however short it is."""
+    NVML_CLOCK_SM = 1
+
+    def __init__(self, pci_bus_id=None, index=0, lib=None):
+        self.ok = False
+        self.samples = []
+        self.max_mhz = None
+        try:
+            self.L = lib if lib is not None else ctypes.CDLL("libnvidia-ml.so.1")
+            if self.L.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            rc = -1
+            if pci_bus_id:
+                rc = self.L.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(self.h))
+            if rc != 0:
+                rc = self.L.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h))
+            if rc != 0:
+                return
+            self._reasons = getattr(self.L, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(self.L, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            mx = ctypes.c_uint()
+            if self.L.nvmlDeviceGetMaxClockInfo(self.h, self.NVML_CLOCK_SM, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def sample(self):
+        if not self.ok:
+            return
+        mhz, bits = ctypes.c_uint(), ctypes.c_ulonglong()
+        if self.L.nvmlDeviceGetClockInfo(self.h, self.NVML_CLOCK_SM, ctypes.byref(mhz)) != 0:
+            return
+        if self._reasons(self.h, ctypes.byref(bits)) != 0:
+            return
+        self.samples.append((float(mhz.value), int(bits.value)))
+
+    def summary(self):
+        return summarize_nvml_samples(self.samples, self.max_mhz)
+
+
 def host_cpu_model():
     """CPU model of the host (x86 /proc/cpuinfo, else lscpu, else the machine)."""
     import platform
@@ -280,6 +389,14 @@ def device_facts(torch, dev):
     except Exception:
         facts["driver"] = None
     return facts
+
+
+def pci_bus_id(torch, dev):
+    props = torch.cuda.get_device_properties(dev)
+    try:
+        return "%08x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+    except AttributeError:
+        return None
 
 
 # ---------------------------------------------------------------- reference arm
@@ -328,7 +445,7 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-# ---------------------------------------------------------------- our arm
+# ---------------------------------------------------------------- timing
 
 class Timer:
     def __init__(self, torch, stream):
@@ -340,9 +457,11 @@ class Timer:
         return e
 
 
-def time_launches(torch, stream, fn, steps, warmup):
+def time_launches(torch, stream, fn, steps, warmup, poll=None):
     """Run fn() warmup times, then `steps` times with an event pair around each
-    launch and one around all; returns (total_s, mean_kernel_s)."""
+    launch and one around all; returns (total_s, mean_kernel_s).  With `poll`,
+    the host calls it repeatedly while the timed launches execute (after the
+    first event has completed and until the last one has)."""
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
@@ -355,11 +474,660 @@ def time_launches(torch, stream, fn, steps, warmup):
         e1 = t.event()
         pairs.append((e0, e1))
     end = t.event()
+    if poll is not None:
+        while not end.query():
+            if start.query():
+                poll()
+            time.sleep(0.0005)
     torch.cuda.synchronize()
     total = start.elapsed_time(end) / 1e3
     per = [a.elapsed_time(b) / 1e3 for a, b in pairs]
     time_launches.last_per_launch = per
     return total, sum(per) / steps
+
+
+# ---------------------------------------------------------------- parity (CPU oracle)
+
+def parity_windows(n, seed, full_max=PARITY_FULL_MAX, w=PARITY_WINDOW):
+    """Index ranges [lo, hi) compared with the oracle: everything up to
+    full_max elements; else the first and last w elements and four seeded
+    windows of w."""
+    if n <= full_max:
+        return [(0, n)]
+    g = np.random.default_rng(seed)
+    starts = {0, n - w} | {int(v) for v in g.integers(0, n - w, size=4)}
+    return sorted((s, s + w) for s in starts)
+
+
+def first_mismatch(got, want, dtype, nan_class):
+    """Index of the first element whose bits differ (NaN matches NaN when
+    nan_class), or None."""
+    bits = np.uint32 if ESIZE[dtype] == 4 else np.uint16
+    g = np.ascontiguousarray(got).view(bits)
+    w = np.ascontiguousarray(want).view(bits)
+    if g.shape != w.shape:
+        return 0
+    diff = g != w
+    if nan_class and dtype != "i32":
+        if dtype == "f32":
+            gn, wn = (g & 0x7FFFFFFF) > 0x7F800000, (w & 0x7FFFFFFF) > 0x7F800000
+        else:
+            inf = 0x7C00 if dtype == "f16" else 0x7F80
+            gn, wn = (g & 0x7FFF) > inf, (w & 0x7FFF) > inf
+        diff &= ~(gn & wn)
+    bad = np.nonzero(diff)[0]
+    return int(bad[0]) if bad.size else None
+
+
+class DevBuf:
+    """n elements of `dtype` on the device, `offset` elements past a 256-byte
+    boundary, filled from a host array."""
+
+    def __init__(self, torch, dev, arr, dtype, offset=0):
+        self.torch, self.dtype, self.e, self.off = torch, dtype, ESIZE[dtype], offset
+        self.n = arr.size
+        self.raw = torch.empty(self.n * self.e + 256, dtype=torch.uint8, device=dev)
+        self.ptr = self.raw.data_ptr() + offset * self.e
+        self.fill(arr)
+
+    def fill(self, arr):
+        b = np.ascontiguousarray(arr).view(np.uint8)
+        self.raw[self.off * self.e: self.off * self.e + b.size].copy_(self.torch.from_numpy(b))
+
+    def read(self, lo, hi):
+        host = {"f32": np.float32, "i32": np.int32}.get(self.dtype, np.uint16)
+        seg = self.raw[(self.off + lo) * self.e:(self.off + hi) * self.e]
+        return seg.cpu().numpy().view(host)
+
+
+class Parity:
+    """Compares a workload's device output with the CPU oracle on the same
+    inputs.  `want(lo, hi)` returns the oracle's result for outputs [lo, hi)."""
+
+    def __init__(self, enabled):
+        self.enabled = enabled
+        self.oracle = None
+        if enabled:
+            import oracle
+            self.oracle = oracle
+
+    def check(self, name, out, want, n, nan_class=True, full_max=PARITY_FULL_MAX):
+        if not self.enabled:
+            return {"parity": "unchecked"}
+        self.torch_sync(out)
+        seed = sum(name.encode()) * 7919
+        checked = 0
+        for lo, hi in parity_windows(n, seed, full_max):
+            bad = first_mismatch(out.read(lo, hi), want(lo, hi), out.dtype, nan_class)
+            if bad is not None:
+                return {"parity": "MISMATCH", "first_bad_index": lo + bad}
+            checked += hi - lo
+        return {"parity": True, "parity_elements": checked}
+
+    @staticmethod
+    def torch_sync(out):
+        out.torch.cuda.synchronize()
+
+
+# ---------------------------------------------------------------- aux workloads
+
+class Aux:
+    """The other workloads of the aux line: timing, then a parity check."""
+
+    def __init__(self, torch, ew, inputs, metrics, stream, peak, dev, parity, l2_bytes):
+        self.torch, self.ew, self.inputs, self.metrics = torch, ew, inputs, metrics
+        self.stream, self.peak, self.dev, self.parity = stream, peak, dev, parity
+        self.l2_bytes = l2_bytes or 0
+        self.L = ew.lib()
+        self.s = stream.cuda_stream
+        self.out = {}
+
+    def buf(self, arr, dtype, offset=0):
+        return DevBuf(self.torch, self.dev, arr, dtype, offset)
+
+    def _speed(self, nbytes, kern_s, footprint=None):
+        g = self.metrics.gbps(nbytes, kern_s)
+        ent = {"gbps": g, "kernel_ms": kern_s * 1e3, "bytes_per_launch": nbytes}
+        if (footprint if footprint is not None else nbytes) <= self.l2_bytes:
+            ent["l2_resident"] = True  # working set fits in L2: not an HBM figure
+        else:
+            ent["frac"] = g / self.peak
+            ent["frac_of_nominal_8tbs"] = g / 8000.0
+        return ent
+
+    def _finish(self, name, ent, check):
+        """check: (out DevBuf, want(lo, hi), n[, rerun][, kwargs]) or None.
+        rerun: resets in-place operands and launches once more before reading."""
+        if check is None:
+            ent["parity"] = "not applicable"
+        else:
+            out_buf, want, n = check[0], check[1], check[2]
+            rerun = check[3] if len(check) > 3 else None
+            kw = check[4] if len(check) > 4 else {}
+            if rerun is not None and self.parity.enabled:
+                rerun()
+            res = self.parity.check(name, out_buf, want, n, **kw)
+            if res["parity"] == "MISMATCH":
+                ent = {"parity": "MISMATCH", "first_bad_index": res["first_bad_index"],
+                       "note": "output differs from the CPU oracle: no speed reported"}
+            else:
+                ent.update(res)
+        self.out[name] = ent
+
+    def _call_ok(self, call, name):
+        st = call()
+        if st != 0:
+            raise self.ew.EwError(st, name)
+
+    def record(self, name, op, dtype, n, call, check, steps=50, footprint=None):
+        total, kern = time_launches(self.torch, self.stream, lambda: self._call_ok(call, name), steps, 3)
+        per = sorted(time_launches.last_per_launch)
+        nbytes = self.metrics.algorithmic_bytes(op, dtype, n)
+        ent = self._speed(nbytes, kern, footprint)
+        ent.update({"kernel_ms_median": per[len(per) // 2] * 1e3, "kernel_ms_min": per[0] * 1e3,
+                    "step_ms": total / steps * 1e3, "gelem_per_s": n / kern / 1e9,
+                    "launch": self.ew.last_launch()})
+        self._finish(name, ent, check)
+
+    def record_graph(self, name, op, dtype, n, call, check, k=50, reps=5):
+        """K launches captured in one CUDA graph and replayed: the per-launch
+        time without host launch gaps (median of `reps` replays).  The parity
+        rerun replays the graph once more (k launches)."""
+        torch, stream = self.torch, self.stream
+        self._call_ok(call, name)  # fills the per-device caches outside the capture
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for _ in range(k):
+                st = call()
+        if st != 0:
+            raise self.ew.EwError(st, name + " (captured)")
+        times = []
+        with torch.cuda.stream(stream):  # replay() launches on the current stream
+            graph.replay()
+            torch.cuda.synchronize()
+            for _ in range(reps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                graph.replay()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                times.append(e0.elapsed_time(e1) / 1e3 / k)
+        per = sorted(times)[len(times) // 2]
+        ent = self._speed(self.metrics.algorithmic_bytes(op, dtype, n), per)
+        ent.update({"launches_per_graph": k, "replays": reps,
+                    "note": "%d launches in one CUDA graph; per-launch time of the median replay" % k})
+        if check is not None:
+            reset = check[3] if len(check) > 3 else None
+
+            def rerun():
+                if reset is not None:
+                    reset()
+                with torch.cuda.stream(stream):
+                    graph.replay()
+                torch.cuda.synchronize()
+            check = (check[0], check[1], check[2], rerun) + tuple(check[4:])
+        self._finish(name, ent, check)
+        del graph
+
+    def record_fn(self, name, nbytes, fn, check, steps=50, note=None, footprint=None):
+        """A step of several calls (e.g. an unfused pair), timed as one."""
+        total, kern = time_launches(self.torch, self.stream, fn, steps, 3)
+        ent = self._speed(nbytes, kern, footprint)
+        if note:
+            ent["note"] = note
+        self._finish(name, ent, check)
+
+    # -------------------------------------------------------------- workloads
+
+    def run(self):
+        orc = self.parity.oracle
+        L, s = self.L, self.s
+        inputs = self.inputs
+        ew = self.ew
+        n28, n26 = 1 << 28, 1 << 26
+
+        # -- 16-bit add, SAXPY, ReLU and fused chains at 2^28
+        for dtype in ("bf16", "f16"):
+            code = DT_CODE[dtype]
+            xa = inputs.as_dtype(inputs.normal(n28, inputs.seed_for("add_16")), dtype)
+            xb = inputs.as_dtype(inputs.normal(n28, inputs.seed_for("add_16", 1)), dtype)
+
+            def want_add(lo, hi, xa=xa, xb=xb, dtype=dtype):
+                return orc.add(dtype, xa[lo:hi], xb[lo:hi])
+            for off in (0, 1):
+                A, B, C = self.buf(xa, dtype, off), self.buf(xb, dtype, off), self.buf(np.zeros_like(xa), dtype, off)
+                self.record("add_%s_2p28_off%d" % (dtype, off), "add", dtype, n28,
+                            lambda: L.ew_add(code, A.ptr, B.ptr, C.ptr, n28, s), (C, want_add, n28))
+                del A, B, C
+            A, B, C = self.buf(xa, dtype), self.buf(xb, dtype), self.buf(np.zeros_like(xa), dtype)
+            self.record("saxpy_%s_2p28_inplace" % dtype, "saxpy", dtype, n28,
+                        lambda: L.ew_saxpy(code, 2.5, A.ptr, B.ptr, n28, s),
+                        (B, lambda lo, hi: orc.saxpy(dtype, 2.5, xa[lo:hi], xb[lo:hi]), n28,
+                         lambda: (B.fill(xb), self._call_ok(lambda: L.ew_saxpy(code, 2.5, A.ptr, B.ptr, n28, s),
+                                                            "saxpy"))))
+            B.fill(xb)
+            self.record("relu_%s_2p28" % dtype, "relu", dtype, n28, lambda: L.ew_relu(code, A.ptr, C.ptr, n28, s),
+                        (C, lambda lo, hi: orc.relu(dtype, xa[lo:hi]), n28), )
+            self.record("add_relu_%s_2p28_fused" % dtype, "add_relu", dtype, n28,
+                        lambda: L.ew_add_relu(code, A.ptr, B.ptr, C.ptr, n28, s),
+                        (C, lambda lo, hi: orc.relu(dtype, orc.add(dtype, xa[lo:hi], xb[lo:hi])), n28))
+            self.record("saxpy_relu_%s_2p28_fused" % dtype, "saxpy_relu", dtype, n28,
+                        lambda: L.ew_saxpy_relu(code, 2.5, A.ptr, C.ptr, n28, s),
+                        (C, lambda lo, hi: orc.relu(dtype, orc.saxpy(dtype, 2.5, xa[lo:hi], xb[lo:hi])), n28,
+                         lambda: (C.fill(xb), self._call_ok(
+                             lambda: L.ew_saxpy_relu(code, 2.5, A.ptr, C.ptr, n28, s), "saxpy_relu"))))
+            del A, B, C
+            if dtype == "bf16":
+                # pointers of different parity (A +1, B +0, C +3 elements): the
+                # realigning bulk-copy kernel (default) against 2-byte accesses
+                A, B, C = self.buf(xa, dtype, 1), self.buf(xb, dtype, 0), self.buf(np.zeros_like(xa), dtype, 3)
+                self.record("add_bf16_2p28_mixed_parity", "add", dtype, n28,
+                            lambda: L.ew_add(code, A.ptr, B.ptr, C.ptr, n28, s), (C, want_add, n28))
+                C.fill(np.zeros_like(xa))
+                ew.set_path("v256")
+                self.record("add_bf16_2p28_mixed_parity_2byte", "add", dtype, n28,
+                            lambda: L.ew_add(code, A.ptr, B.ptr, C.ptr, n28, s), (C, want_add, n28))
+                ew.set_path("auto")
+                del A, B, C
+            del xa, xb
+
+        # -- fp32 SAXPY: 32M (the pages' size), then 2^26 and 2^28
+        n32m = 32 << 20
+        x = inputs.normal(n32m, inputs.seed_for("saxpy_f32"))
+        y = inputs.normal(n32m, inputs.seed_for("saxpy_f32", 1))
+        X, Y = self.buf(x, "f32"), self.buf(y, "f32")
+
+        def saxpy32():
+            return L.ew_saxpy(0, 2.5, X.ptr, Y.ptr, n32m, s)
+        self.record("saxpy_f32_32M_inplace", "saxpy", "f32", n32m, saxpy32,
+                    (Y, lambda lo, hi: orc.saxpy("f32", 2.5, x[lo:hi], y[lo:hi]), n32m,
+                     lambda: (Y.fill(y), self._call_ok(saxpy32, "saxpy"))), steps=200)
+        Y.fill(y)
+
+        def want_saxpy_k(lo, hi, k=50):
+            r = y[lo:hi]
+            for _ in range(k):
+                r = orc.saxpy("f32", 2.5, x[lo:hi], r)
+            return r
+        self.record_graph("saxpy_f32_32M_inplace_graph", "saxpy", "f32", n32m, saxpy32,
+                          (Y, want_saxpy_k, n32m, lambda: Y.fill(y), {"full_max": 0}))
+        del X, Y
+        x = inputs.normal(n28, inputs.seed_for("saxpy_f32", 2))
+        y = inputs.normal(n28, inputs.seed_for("saxpy_f32", 3))
+        X, Y = self.buf(x, "f32"), self.buf(y, "f32")
+        for lg in (26, 28):
+            m = 1 << lg
+
+            def call(m=m):
+                return L.ew_saxpy(0, 2.5, X.ptr, Y.ptr, m, s)
+            self.record("saxpy_f32_2p%d_inplace" % lg, "saxpy", "f32", m, call,
+                        (Y, lambda lo, hi: orc.saxpy("f32", 2.5, x[lo:hi], y[lo:hi]), m,
+                         lambda call=call: (Y.fill(y), self._call_ok(call, "saxpy"))),
+                        steps=100 if lg == 26 else 50)
+        del X, Y, x, y
+
+        # -- fp32 ReLU at 2^28: out of place, in place on fresh data, in place again
+        x = inputs.inject_signed_zeros(inputs.normal(n28, inputs.seed_for("relu_f32")))
+        X, Y = self.buf(x, "f32"), self.buf(np.zeros_like(x), "f32")
+        want_relu = lambda lo, hi: orc.relu("f32", x[lo:hi])  # noqa: E731
+        self.record("relu_f32_2p28", "relu", "f32", n28, lambda: L.ew_relu(0, X.ptr, Y.ptr, n28, s),
+                    (Y, want_relu, n28))
+        # in place on fresh data: refill from the pristine copy before each
+        # launch (outside the event pair), so every timed launch sees ~50% negatives
+        kern_ms = []
+        for _ in range(13):
+            with self.torch.cuda.stream(self.stream):
+                Y.raw.copy_(X.raw, non_blocking=True)
+            e0, e1 = self.torch.cuda.Event(enable_timing=True), self.torch.cuda.Event(enable_timing=True)
+            e0.record(self.stream)
+            st = L.ew_relu(0, Y.ptr, Y.ptr, n28, s)
+            e1.record(self.stream)
+            if st != 0:
+                raise ew.EwError(st, "relu in place")
+            self.torch.cuda.synchronize()
+            kern_ms.append(e0.elapsed_time(e1))
+        kern = sum(kern_ms[3:]) / len(kern_ms[3:]) / 1e3
+        ent = self._speed(self.metrics.algorithmic_bytes("relu", "f32", n28), kern)
+        ent["launch"] = ew.last_launch()
+        self._finish("relu_f32_2p28_inplace_fresh", ent, (Y, want_relu, n28))
+        # in place again on the now non-negative data: nothing changes, so no
+        # vector is stored (the page's case B: 4 bytes per element, read only)
+        self.record_fn("relu_f32_2p28_inplace_nonnegative", 4 * n28,
+                       lambda: self._call_ok(lambda: L.ew_relu(0, Y.ptr, Y.ptr, n28, s), "relu in place"),
+                       (Y, want_relu, n28), note="read-only bytes: unchanged vectors are not stored")
+        del X, Y, x
+
+        # -- copy and gathers at 2^26
+        x = inputs.uniform(n26, inputs.seed_for("copy_f32"), 0.0, 1.0)
+        X, Y = self.buf(x, "f32"), self.buf(np.zeros_like(x), "f32")
+        gathered = {}
+
+        def want_gather(stride):
+            if stride not in gathered:
+                gathered[stride] = orc.gather_stride(x, stride)
+            g = gathered[stride]
+            return lambda lo, hi: g[lo:hi]
+        want_copy = lambda lo, hi: x[lo:hi]  # noqa: E731
+
+        def clear():
+            Y.raw.zero_()
+        copy_call = lambda: L.ew_copy(0, X.ptr, Y.ptr, n26, s)  # noqa: E731
+        self.record("copy_f32_2p26", "copy", "f32", n26, copy_call, (Y, want_copy, n26), steps=200)
+        clear()
+        self.record_graph("copy_f32_2p26_graph", "copy", "f32", n26, copy_call, (Y, want_copy, n26, clear))
+        clear()
+        g2 = lambda: L.ew_gather_stride(0, X.ptr, Y.ptr, n26, 2, s)  # noqa: E731
+        self.record_graph("gather2_f32_2p26_graph", "gather", "f32", n26, g2, (Y, want_gather(2), n26, clear))
+        variants = [("gather2_f32_2p26", 2, "auto", "auto"), ("gather4_f32_2p26", 4, "auto", "auto"),
+                    ("gather8_f32_2p26", 8, "auto", "auto"), ("gather16_f32_2p26", 16, "auto", "auto"),
+                    ("gather64_f32_2p26", 64, "auto", "auto"),
+                    ("gather16_f32_2p26_lap_order", 16, "auto", "laps"),
+                    ("gather2_f32_2p26_index_order", 2, "auto", "oneshot"),
+                    ("gather4_f32_2p26_index_order", 4, "auto", "oneshot"),
+                    ("gather16_f32_2p26_index_order", 16, "auto", "oneshot"),
+                    ("gather2_f32_2p26_span", 2, "v256", "auto")]
+        for name, stride, path, sched in variants:
+            ew.set_path(path)
+            ew.set_schedule(sched)
+            clear()
+            self.record(name, "gather", "f32", n26,
+                        lambda stride=stride: L.ew_gather_stride(0, X.ptr, Y.ptr, n26, stride, s),
+                        (Y, want_gather(stride), n26), steps=100)
+        ew.set_path("auto")
+        ew.set_schedule("auto")
+        del X, Y
+        gathered.clear()
+        # 16-bit gathers (the tiled kernel's 2-byte instantiation from stride 8)
+        xh = inputs.as_dtype(inputs.uniform(n26, inputs.seed_for("copy_f32", 3), 0.0, 1.0), "bf16")
+        X, Y = self.buf(xh, "bf16"), self.buf(np.zeros_like(xh), "bf16")
+        for stride in (2, 16, 64):
+            want = orc.gather_stride(xh, stride)
+            Y.raw.zero_()
+            self.record("gather%d_bf16_2p26" % stride, "gather", "bf16", n26,
+                        lambda stride=stride: L.ew_gather_stride(2, X.ptr, Y.ptr, n26, stride, s),
+                        (Y, lambda lo, hi, want=want: want[lo:hi], n26), steps=100)
+        del X, Y, xh
+
+        # -- the branch-free even/odd select on int32 (CUDA-MODE lecture notes §6)
+        xi = inputs.rng(inputs.seed_for("copy_f32", 7)).integers(-2 ** 31, 2 ** 31, size=n28,
+                                                                 dtype=np.int64).astype(np.int32)
+        X, Y = self.buf(xi, "i32"), self.buf(np.zeros_like(xi), "i32")
+        self.record("select_even_odd_i32_2p28", "select", "i32", n28,
+                    lambda: L.ew_select_even_odd(3, X.ptr, Y.ptr, n28, s),
+                    (Y, lambda lo, hi: orc.select_even_odd(xi[lo:hi]), n28))
+        del X, Y, xi
+
+        # -- fp32 add at 2^20 + 3 (L2-resident, launch-bound)
+        n1 = (1 << 20) + 3
+        a = inputs.uniform(n1, inputs.seed_for("add_f32_small"))
+        b = inputs.uniform(n1, inputs.seed_for("add_f32_small", 1))
+        A, B, C = self.buf(a, "f32"), self.buf(b, "f32"), self.buf(np.zeros_like(a), "f32")
+        self.record("add_f32_2p20p3_l2_resident", "add", "f32", n1, lambda: L.ew_add(0, A.ptr, B.ptr, C.ptr, n1, s),
+                    (C, lambda lo, hi: orc.add("f32", a[lo:hi], b[lo:hi]), n1), steps=500)
+        del A, B, C
+
+        # -- the headline workload through other variants, and the fused chains
+        a = inputs.normal(n28, inputs.seed_for("add_f32"))
+        b = inputs.normal(n28, inputs.seed_for("add_f32", 1))
+        A, B, C = self.buf(a, "f32"), self.buf(b, "f32"), self.buf(np.zeros_like(a), "f32")
+        want_add_relu = lambda lo, hi: orc.relu("f32", orc.add("f32", a[lo:hi], b[lo:hi]))  # noqa: E731
+        self.record("add_relu_f32_2p28_fused", "add_relu", "f32", n28,
+                    lambda: L.ew_add_relu(0, A.ptr, B.ptr, C.ptr, n28, s), (C, want_add_relu, n28))
+        C.raw.zero_()
+
+        def unfused():
+            for st in (L.ew_add(0, A.ptr, B.ptr, C.ptr, n28, s), L.ew_relu(0, C.ptr, C.ptr, n28, s)):
+                if st != 0:
+                    raise ew.EwError(st, "add then relu")
+        self.record_fn("add_then_relu_f32_2p28_unfused", self.metrics.algorithmic_bytes("add_relu", "f32", n28),
+                       unfused, (C, want_add_relu, n28),
+                       note="two launches per step (add, then ReLU in place); GB/s counts the fused "
+                            "operation's 12 bytes per element")
+        # SAXPY + ReLU fused in one pass (y = relu(2.5 x + y) in place, x = A, y = C)
+        want_sr = lambda lo, hi: orc.relu("f32", orc.saxpy("f32", 2.5, a[lo:hi], b[lo:hi]))  # noqa: E731
+        sr = lambda: L.ew_saxpy_relu(0, 2.5, A.ptr, C.ptr, n28, s)  # noqa: E731
+        self.record("saxpy_relu_f32_2p28_fused", "saxpy_relu", "f32", n28, sr,
+                    (C, want_sr, n28, lambda: (C.fill(b), self._call_ok(sr, "saxpy_relu"))))
+
+        def saxpy_unfused():
+            for st in (L.ew_saxpy(0, 2.5, A.ptr, C.ptr, n28, s), L.ew_relu(0, C.ptr, C.ptr, n28, s)):
+                if st != 0:
+                    raise ew.EwError(st, "saxpy then relu")
+        self.record_fn("saxpy_then_relu_f32_2p28_unfused",
+                       self.metrics.algorithmic_bytes("saxpy_relu", "f32", n28), saxpy_unfused,
+                       (C, want_sr, n28, lambda: (C.fill(b), saxpy_unfused())),
+                       note="two launches per step (SAXPY, then ReLU in place); GB/s counts the fused "
+                            "operation's 12 bytes per element")
+        want_a_plus_b = lambda lo, hi: orc.add("f32", a[lo:hi], b[lo:hi])  # noqa: E731
+        for label, path, sched in (("persistent", "auto", "persistent"), ("tma", "tma", "auto")):
+            ew.set_path(path)
+            ew.set_schedule(sched)
+            C.raw.zero_()
+            self.record("add_f32_2p28_" + label, "add", "f32", n28,
+                        lambda: L.ew_add(0, A.ptr, B.ptr, C.ptr, n28, s), (C, want_a_plus_b, n28))
+        ew.set_path("tma")
+        ew.set_schedule("auto")
+        C.raw.zero_()
+        self.record("copy_f32_2p26_tma", "copy", "f32", n26, lambda: L.ew_copy(0, A.ptr, C.ptr, n26, s),
+                    (C, lambda lo, hi: a[lo:hi], n26), steps=200)
+        ew.set_path("auto")
+        del A, B, C, a, b
+
+        # -- chains of short calls launched back to back without events in
+        # between: programmatic dependent launch on (the default) against off
+        for lg in (20, 23, 25):
+            m = 1 << lg
+            cx = inputs.normal(m, inputs.seed_for("saxpy_f32", 4))
+            cy = inputs.normal(m, inputs.seed_for("saxpy_f32", 5))
+            X, Y = self.buf(cx, "f32"), self.buf(cy, "f32")
+            call = lambda m=m: L.ew_saxpy(0, 0.5, X.ptr, Y.ptr, m, s)  # noqa: E731
+            for prog in (True, False):
+                ew.set_programmatic_launch(prog)
+                for _ in range(10):
+                    call()
+                self.torch.cuda.synchronize()
+                e0, e1 = self.torch.cuda.Event(enable_timing=True), self.torch.cuda.Event(enable_timing=True)
+                e0.record(self.stream)
+                for _ in range(200):
+                    self._call_ok(call, "saxpy chain")
+                e1.record(self.stream)
+                self.torch.cuda.synchronize()
+                per = e0.elapsed_time(e1) / 1e3 / 200
+                ent = self._speed(self.metrics.algorithmic_bytes("saxpy", "f32", m), per)
+                ent["note"] = "200 launches back to back, time per launch from one event pair"
+                self._finish("saxpy_chain_f32_2p%d_%s" % (lg, "pdl" if prog else "plain"), ent,
+                             (Y, lambda lo, hi, cx=cx, cy=cy: orc.saxpy("f32", 0.5, cx[lo:hi], cy[lo:hi]), m,
+                              lambda call=call, cy=cy: (Y.fill(cy), self._call_ok(call, "saxpy chain"))))
+                Y.fill(cy)
+            ew.set_programmatic_launch(True)
+            del X, Y
+
+        # -- device-to-device copy ceiling of this GPU (cudaMemcpyAsync via
+        # torch copy_, 2 GiB, read + write bytes), timed on the same stream
+        big = self.torch.empty(1 << 31, dtype=self.torch.uint8, device=self.dev)
+        big2 = self.torch.empty_like(big)
+
+        def d2d():
+            with self.torch.cuda.stream(self.stream):
+                big2.copy_(big, non_blocking=True)
+        total, kern = time_launches(self.torch, self.stream, d2d, 20, 3)
+        g = self.metrics.gbps(2 * big.numel(), kern)
+        self.out["memcpy_d2d_2GiB"] = {"gbps": g, "frac": g / self.peak, "kernel_ms": kern * 1e3,
+                                       "parity": "not applicable (library copy)",
+                                       "note": "library device-to-device copy (torch copy_), read+write bytes"}
+        del big, big2
+        for ent in self.out.values():  # against the copy ceiling measured in this run
+            if "frac" in ent:
+                ent["frac_of_d2d"] = ent["gbps"] / g
+        if "gather2_f32_2p26" in self.out:
+            self.out["gather2_f32_2p26"]["sectors_per_request"] = profiled_sectors()
+        return self.out
+
+
+# ---------------------------------------------------------------- access-width A/B
+
+def run_ab_widths(args):
+    """16-byte against 32-byte accesses, launch by launch interleaved on the
+    same buffers: add, SAXPY, ReLU, copy in fp32 and bf16 at 2^26 and 2^28.
+    Prints one JSON line per case with the median and minimum per launch."""
+    import torch
+
+    import memory_bound_elementwise_gb300 as ew
+    from memory_bound_elementwise_gb300 import inputs, metrics
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(dev)
+    s = stream.cuda_stream
+    L = ew.lib()
+    parity = Parity(not args.no_cpu)
+    rows = []
+    reps = 200
+    for dtype in ("f32", "bf16"):
+        code = DT_CODE[dtype]
+        for lg in (26, 28):
+            n = 1 << lg
+            a = inputs.as_dtype(inputs.normal(n, inputs.seed_for("add_f32")), dtype)
+            b = inputs.as_dtype(inputs.normal(n, inputs.seed_for("add_f32", 1)), dtype)
+            A, B = DevBuf(torch, dev, a, dtype), DevBuf(torch, dev, b, dtype)
+            C = DevBuf(torch, dev, np.zeros_like(a), dtype)
+            orc = parity.oracle
+            cases = [("add", lambda: L.ew_add(code, A.ptr, B.ptr, C.ptr, n, s),
+                      lambda lo, hi: orc.add(dtype, a[lo:hi], b[lo:hi])),
+                     ("saxpy", lambda: L.ew_saxpy(code, 2.5, A.ptr, C.ptr, n, s), None),
+                     ("relu", lambda: L.ew_relu(code, A.ptr, C.ptr, n, s),
+                      lambda lo, hi: orc.relu(dtype, a[lo:hi])),
+                     ("copy", lambda: L.ew_copy(code, A.ptr, C.ptr, n, s), lambda lo, hi: a[lo:hi])]
+            for op, call, want in cases:
+                if op == "saxpy":
+                    C.fill(b)  # y = C: in place; values drift over the launches (timing only)
+                per = {"v128": [], "v256": []}
+                for _ in range(3):
+                    for path in ("v128", "v256"):
+                        ew.set_path(path)
+                        call()
+                torch.cuda.synchronize()
+                for _ in range(reps):
+                    for path in ("v128", "v256"):
+                        ew.set_path(path)
+                        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        e0.record(stream)
+                        st = call()
+                        e1.record(stream)
+                        if st != 0:
+                            raise ew.EwError(st, op)
+                        per[path].append((e0, e1))
+                torch.cuda.synchronize()
+                nbytes = metrics.algorithmic_bytes(op, dtype, n)
+                row = {"ab": "widths", "op": op, "dtype": dtype, "n": n, "launches_each": reps}
+                for path in ("v128", "v256"):
+                    t = sorted(e0.elapsed_time(e1) / 1e3 for e0, e1 in per[path])
+                    row[path] = {"median_us": t[len(t) // 2] * 1e6, "min_us": t[0] * 1e6,
+                                 "gbps_median": metrics.gbps(nbytes, t[len(t) // 2])}
+                    ew.set_path(path)
+                    if want is not None:
+                        C.raw.zero_()
+                        call()
+                        row[path].update(parity.check("%s_%s_%s" % (op, dtype, path), C, want, n))
+                    elif op == "saxpy" and parity.enabled:
+                        C.fill(b)
+                        call()
+                        row[path].update(parity.check("saxpy_%s_%s" % (dtype, path), C,
+                                                      lambda lo, hi: orc.saxpy(dtype, 2.5, a[lo:hi], b[lo:hi]), n))
+                ew.set_path("auto")
+                row["v256_over_v128"] = row["v128"]["median_us"] / row["v256"]["median_us"]
+                rows.append(row)
+                print(json.dumps(row), flush=True)
+            del A, B, C
+
+
+def run_ab_gather(args):
+    """Gather schedules (lap order, tiled, index order) at strides 2 to 64, on
+    2^26 fp32 and bf16 elements: median per launch and parity for each."""
+    import torch
+
+    import memory_bound_elementwise_gb300 as ew
+    from memory_bound_elementwise_gb300 import inputs, metrics
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(dev)
+    s = stream.cuda_stream
+    L = ew.lib()
+    parity = Parity(not args.no_cpu)
+    n = args.n if args.n != N_HEADLINE else 1 << 26
+    strides = [args.stride] if args.stride else [2, 3, 4, 5, 8, 12, 16, 32, 64]
+    for dtype in ("f32", "bf16"):
+        code = DT_CODE[dtype]
+        x = inputs.as_dtype(inputs.uniform(n, inputs.seed_for("copy_f32"), 0.0, 1.0), dtype)
+        X, Y = DevBuf(torch, dev, x, dtype), DevBuf(torch, dev, np.zeros_like(x), dtype)
+        for stride in strides:
+            want = parity.oracle.gather_stride(x, stride) if parity.enabled else None
+            row = {"ab": "gather", "dtype": dtype, "n": n, "stride": stride}
+            for sched in ("auto", "laps", "tiled"):
+                ew.set_schedule(sched)
+                call = lambda: L.ew_gather_stride(code, X.ptr, Y.ptr, n, stride, s)  # noqa: E731
+                Y.raw.zero_()
+                total, kern = time_launches(torch, stream, call, 50, 3)
+                t = sorted(time_launches.last_per_launch)
+                rec = ew.last_launch()
+                row[sched] = {"median_us": t[len(t) // 2] * 1e6,
+                              "gbps_median": metrics.gbps(metrics.algorithmic_bytes("gather", dtype, n),
+                                                          t[len(t) // 2]),
+                              "schedule_ran": ew.SCHED_NAMES.get(rec["schedule"], rec["schedule"])}
+                if want is not None:
+                    row[sched].update(parity.check("g%d%s%s" % (stride, dtype, sched), Y,
+                                                   lambda lo, hi: want[lo:hi], n))
+            ew.set_schedule("auto")
+            print(json.dumps(row), flush=True)
+        del X, Y
+
+
+# ---------------------------------------------------------------- our arm
+
+def headline_line(*, value, parity, world, steps, warmup, total_s, n, lo, hi, step_bytes, rec, facts,
+                  gpu_name, achieved, peak, peak_src, traffic, traffic_note, kern_s, per_launch,
+                  e2e, clocks, cpu_baseline):
+    """The compact headline dict (printed last, well under HEADLINE_MAX_BYTES)."""
+    ok = parity is True or parity == "unchecked"
+    line = {
+        "metric": METRIC, "value": value if ok else None, "unit": "GB/s", "n_gpus": world,
+        "steps": steps, "warmup": warmup, "ms_per_step": total_s / steps * 1e3,
+        "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": (value / PAGE_BASELINE["value"]) if ok else None,
+        "baseline": "%s GB/s, %s, %s" % (PAGE_BASELINE["value"], PAGE_BASELINE["kernel"],
+                                         PAGE_BASELINE["hardware"]),
+        "dtype": "f32",
+        "data": "synthetic: A, B i.i.d. uniform[-1,1) binary32, seeded PCG64 per rank",
+        "config": {"workload": "fp32 add C=A+B, N=2^28 per GPU", "n": n, "slice": [lo, hi],
+                   "bytes_per_step_per_gpu": step_bytes,
+                   "l2": "no flush: inputs larger than L2 (3.2 GB working set vs 129 MB L2)",
+                   "path": rec.get("path"), "vec_bytes": rec.get("vec_bytes"),
+                   "grid": rec.get("grid"), "block": rec.get("block"), "gpu": gpu_name,
+                   "sms": facts.get("sms"), "l2_bytes": facts.get("l2_bytes"),
+                   "driver": facts.get("driver")},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
+                     "traffic_note": traffic_note, "kernel_ms": kern_s * 1e3,
+                     "kernel_ms_median": per_launch[len(per_launch) // 2] * 1e3,
+                     "kernel_ms_min": per_launch[0] * 1e3, "frac_of_nominal_8tbs": achieved / 8000.0},
+        "e2e": e2e,
+        "gpu_launches": steps,
+        "clocks": clocks,
+        "parity": ("bit-exact vs the CPU oracle" if parity is True else parity),
+    }
+    if cpu_baseline is not None:
+        line["cpu_baseline"] = cpu_baseline
+    return line
+
+
+def emit(aux_line, headline, out=None):
+    """Print the aux line (if any), then the headline as the LAST line."""
+    out = out or sys.stdout
+    if aux_line is not None:
+        out.write(json.dumps(aux_line) + "\n")
+    text = json.dumps(headline, separators=(",", ":"))
+    if len(text.encode()) > HEADLINE_MAX_BYTES:
+        raise RuntimeError("headline line is %d bytes (limit %d)" % (len(text.encode()), HEADLINE_MAX_BYTES))
+    out.write(text + "\n")
+    out.flush()
 
 
 def oracle_all_cores(oracle, metrics, a_h, b_h, want, min_s=5.0):
@@ -385,308 +1153,7 @@ def oracle_all_cores(oracle, metrics, a_h, b_h, want, min_s=5.0):
                 break
     same = all(np.array_equal(p_.view(np.uint32), want[b[0]:b[1]].view(np.uint32))
                for p_, b in zip(parts, bounds))
-    return {"value": metrics.gbps(12 * n * reps, el), "unit": "GB/s", "cores": cores,
-            "sample": "%d full passes over the N=2^28 inputs on %d threads (%.1f s)" % (reps, cores, el),
-            "matches_single_core": same}
-
-
-def aux_measurements(torch, ew, inputs, metrics, stream, peak, dev):
-    """The other workloads: (name -> GB/s, fraction of peak, kernel ms)."""
-    out = {}
-    L = ew.lib()
-    s = stream.cuda_stream
-
-    def dev_of(arr, dtype, offset=0):
-        e = 4 if dtype == "f32" else 2
-        raw = torch.empty(arr.size * e + 256, dtype=torch.uint8, device=dev)
-        view = raw[offset * e: offset * e + arr.size * e]
-        view.copy_(torch.from_numpy(np.ascontiguousarray(arr).view(np.uint8)))
-        return raw, view.data_ptr()
-
-    def record(name, op, dtype, n, call, steps=50):
-        def fn():
-            st = call()
-            if st != 0:
-                raise ew.EwError(st, name)
-        total, kern = time_launches(torch, stream, fn, steps, 3)
-        per = sorted(time_launches.last_per_launch)
-        nbytes = metrics.algorithmic_bytes(op, dtype, n)
-        g = metrics.gbps(nbytes, kern)
-        out[name] = {"gbps": g, "frac": g / peak, "frac_of_nominal_8tbs": g / 8000.0,
-                     "kernel_ms": kern * 1e3, "kernel_ms_median": per[len(per) // 2] * 1e3,
-                     "kernel_ms_min": per[0] * 1e3, "step_ms": total / steps * 1e3,
-                     "gelem_per_s": n / kern / 1e9,
-                     "bytes_per_launch": nbytes, "launch": ew.last_launch()}
-
-    def record_graph(name, op, dtype, n, call, k=50, reps=5):
-        """K launches captured in one CUDA graph and replayed: the per-launch
-        time without host launch gaps (median of `reps` replays)."""
-        st = call()  # fills the per-device caches outside the capture
-        if st != 0:
-            raise ew.EwError(st, name)
-        torch.cuda.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            for _ in range(k):
-                st = call()
-        if st != 0:
-            raise ew.EwError(st, name + " (captured)")
-        times = []
-        with torch.cuda.stream(stream):  # replay() launches on the current stream
-            graph.replay()
-            torch.cuda.synchronize()
-            for _ in range(reps):
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                graph.replay()
-                e1.record(stream)
-                torch.cuda.synchronize()
-                times.append(e0.elapsed_time(e1) / 1e3 / k)
-        per = sorted(times)[len(times) // 2]
-        nbytes = metrics.algorithmic_bytes(op, dtype, n)
-        g = metrics.gbps(nbytes, per)
-        out[name] = {"gbps": g, "frac": g / peak, "frac_of_nominal_8tbs": g / 8000.0,
-                     "kernel_ms": per * 1e3, "launches_per_graph": k, "replays": reps,
-                     "bytes_per_launch": nbytes,
-                     "note": "%d launches captured in one CUDA graph; per-launch time of the "
-                             "median replay" % k}
-        del graph
-
-    n28 = 1 << 28
-    for dtype, code in (("bf16", 2), ("f16", 1)):
-        xa = inputs.as_dtype(inputs.normal(n28, inputs.seed_for("add_16")), dtype)
-        xb = inputs.as_dtype(inputs.normal(n28, inputs.seed_for("add_16", 1)), dtype)
-        for off in (0, 1):
-            ra, pa = dev_of(xa, dtype, off)
-            rb, pb = dev_of(xb, dtype, off)
-            rc, pc = dev_of(np.zeros_like(xa), dtype, off)
-            record("add_%s_2p28_off%d" % (dtype, off), "add", dtype, n28,
-                   lambda: L.ew_add(code, pa, pb, pc, n28, s))
-            del ra, rb, rc
-        # the other operators on the same 16-bit arrays: SAXPY in place (on B),
-        # ReLU out of place, and the two fused chains
-        ra, pa = dev_of(xa, dtype, 0)
-        rb, pb = dev_of(xb, dtype, 0)
-        rc, pc = dev_of(np.zeros_like(xa), dtype, 0)
-        record("saxpy_%s_2p28_inplace" % dtype, "saxpy", dtype, n28, lambda: L.ew_saxpy(code, 2.5, pa, pb, n28, s))
-        record("relu_%s_2p28" % dtype, "relu", dtype, n28, lambda: L.ew_relu(code, pa, pc, n28, s))
-        record("add_relu_%s_2p28_fused" % dtype, "add_relu", dtype, n28,
-               lambda: L.ew_add_relu(code, pa, pb, pc, n28, s))
-        record("saxpy_relu_%s_2p28_fused" % dtype, "saxpy_relu", dtype, n28,
-               lambda: L.ew_saxpy_relu(code, 2.5, pa, pc, n28, s))
-        del ra, rb, rc
-        if dtype == "bf16":
-            # pointers of different parity (A +1, B +0, C +3 elements): the
-            # realigning bulk-copy kernel (default) against 2-byte accesses
-            ra, pa = dev_of(xa, dtype, 1)
-            rb, pb = dev_of(xb, dtype, 0)
-            rc, pc = dev_of(np.zeros_like(xa), dtype, 3)
-            record("add_bf16_2p28_mixed_parity", "add", dtype, n28, lambda: L.ew_add(code, pa, pb, pc, n28, s))
-            ew.set_path("v256")
-            record("add_bf16_2p28_mixed_parity_2byte", "add", dtype, n28,
-                   lambda: L.ew_add(code, pa, pb, pc, n28, s))
-            ew.set_path("auto")
-            del ra, rb, rc
-        del xa, xb
-    n32m = 32 << 20
-    x = inputs.normal(n32m, inputs.seed_for("saxpy_f32"))
-    y = inputs.normal(n32m, inputs.seed_for("saxpy_f32", 1))
-    rx, px = dev_of(x, "f32")
-    ry, py = dev_of(y, "f32")
-    record("saxpy_f32_32M_inplace", "saxpy", "f32", n32m,
-           lambda: L.ew_saxpy(0, 2.5, px, py, n32m, s), steps=200)
-    record_graph("saxpy_f32_32M_inplace_graph", "saxpy", "f32", n32m,
-                 lambda: L.ew_saxpy(0, 2.5, px, py, n32m, s))
-    del rx, ry
-    # SAXPY at larger N, where the fixed cost of a launch is amortised
-    x = inputs.normal(n28, inputs.seed_for("saxpy_f32", 2))
-    y = inputs.normal(n28, inputs.seed_for("saxpy_f32", 3))
-    rx, px = dev_of(x, "f32")
-    ry, py = dev_of(y, "f32")
-    del x, y
-    for lg in (26, 28):
-        m = 1 << lg
-        record("saxpy_f32_2p%d_inplace" % lg, "saxpy", "f32", m,
-               lambda: L.ew_saxpy(0, 2.5, px, py, m, s), steps=100 if lg == 26 else 50)
-    del rx, ry
-    x = inputs.normal(n28, inputs.seed_for("relu_f32"))
-    inputs.inject_signed_zeros(x)
-    rx, px = dev_of(x, "f32")
-    ry, py = dev_of(np.zeros_like(x), "f32")
-    record("relu_f32_2p28", "relu", "f32", n28, lambda: L.ew_relu(0, px, py, n28, s))
-    # in place on fresh data: refill from the pristine copy before each launch
-    # (outside the event pair), so every timed launch sees ~50% negatives
-    kern_ms = []
-    for _ in range(13):
-        with torch.cuda.stream(stream):
-            ry.copy_(rx, non_blocking=True)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        st = L.ew_relu(0, py, py, n28, s)
-        e1.record(stream)
-        if st != 0:
-            raise ew.EwError(st, "relu in place")
-        torch.cuda.synchronize()
-        kern_ms.append(e0.elapsed_time(e1))
-    kern = sum(kern_ms[3:]) / len(kern_ms[3:]) / 1e3
-    nb = metrics.algorithmic_bytes("relu", "f32", n28)
-    out["relu_f32_2p28_inplace_fresh"] = {"gbps": metrics.gbps(nb, kern), "frac": metrics.gbps(nb, kern) / peak,
-                                          "kernel_ms": kern * 1e3, "bytes_per_launch": nb,
-                                          "launch": ew.last_launch()}
-    # in place again on the now non-negative data: nothing changes, so no vector
-    # is stored (page's case B: 4 bytes per element, read only)
-    def relu_again():
-        st = L.ew_relu(0, py, py, n28, s)
-        if st != 0:
-            raise ew.EwError(st, "relu in place")
-    total, kern = time_launches(torch, stream, relu_again, 50, 3)
-    nb = 4 * n28
-    out["relu_f32_2p28_inplace_nonnegative"] = {
-        "gbps": metrics.gbps(nb, kern), "frac": metrics.gbps(nb, kern) / peak, "kernel_ms": kern * 1e3,
-        "bytes_per_launch": nb, "note": "read-only bytes: unchanged vectors are not stored"}
-    del rx, ry
-    n26 = 1 << 26
-    x = inputs.uniform(n26, inputs.seed_for("copy_f32"), 0.0, 1.0)
-    rx, px = dev_of(x, "f32")
-    ry, py = dev_of(np.zeros_like(x), "f32")
-    record("copy_f32_2p26", "copy", "f32", n26, lambda: L.ew_copy(0, px, py, n26, s), steps=200)
-    record_graph("copy_f32_2p26_graph", "copy", "f32", n26, lambda: L.ew_copy(0, px, py, n26, s))
-    record_graph("gather2_f32_2p26_graph", "gather", "f32", n26,
-                 lambda: L.ew_gather_stride(0, px, py, n26, 2, s))
-    record("gather2_f32_2p26", "gather", "f32", n26,
-           lambda: L.ew_gather_stride(0, px, py, n26, 2, s), steps=100)
-    record("gather4_f32_2p26", "gather", "f32", n26,
-           lambda: L.ew_gather_stride(0, px, py, n26, 4, s), steps=100)
-    # stride 16: every lane's load is its own sector; the default is the tiled kernel
-    record("gather16_f32_2p26", "gather", "f32", n26,
-           lambda: L.ew_gather_stride(0, px, py, n26, 16, s), steps=100)
-    ew.set_schedule("laps")
-    record("gather16_f32_2p26_lap_order", "gather", "f32", n26,
-           lambda: L.ew_gather_stride(0, px, py, n26, 16, s), steps=100)
-    # index order (one block per 1024 consecutive outputs): once the input no
-    # longer fits in L2, each lap fetches it from DRAM again
-    ew.set_schedule("oneshot")
-    record("gather2_f32_2p26_index_order", "gather", "f32", n26,
-           lambda: L.ew_gather_stride(0, px, py, n26, 2, s), steps=100)
-    record("gather4_f32_2p26_index_order", "gather", "f32", n26,
-           lambda: L.ew_gather_stride(0, px, py, n26, 4, s), steps=100)
-    record("gather16_f32_2p26_index_order", "gather", "f32", n26,
-           lambda: L.ew_gather_stride(0, px, py, n26, 16, s), steps=100)
-    ew.set_schedule("auto")
-    ew.set_path("v256")  # span variant: contiguous 256-bit source spans, lane select
-    record("gather2_f32_2p26_span", "gather", "f32", n26,
-           lambda: L.ew_gather_stride(0, px, py, n26, 2, s), steps=100)
-    ew.set_path("auto")
-    del rx, ry
-    # the branch-free even/odd select on int32 (CUDA-MODE lecture notes §6)
-    xi = inputs.rng(inputs.seed_for("copy_f32", 7)).integers(-2 ** 31, 2 ** 31, size=n28,
-                                                             dtype=np.int64).astype(np.int32)
-    rx, px = dev_of(xi.view(np.float32), "f32")
-    ry, py = dev_of(np.zeros(n28, np.float32), "f32")
-    del xi
-    record("select_even_odd_i32_2p28", "select", "i32", n28,
-           lambda: L.ew_select_even_odd(3, px, py, n28, s))
-    del rx, ry
-    n1 = (1 << 20) + 3
-    a = inputs.uniform(n1, inputs.seed_for("add_f32_small"))
-    b = inputs.uniform(n1, inputs.seed_for("add_f32_small", 1))
-    ra, pa = dev_of(a, "f32")
-    rb, pb = dev_of(b, "f32")
-    rc, pc = dev_of(np.zeros_like(a), "f32")
-    record("add_f32_2p20p3_l2_resident", "add", "f32", n1, lambda: L.ew_add(0, pa, pb, pc, n1, s),
-           steps=500)
-    del ra, rb, rc
-    # the headline workload through the other variants: persistent schedule, bulk-copy path
-    a = inputs.normal(n28, inputs.seed_for("add_f32"))
-    b = inputs.normal(n28, inputs.seed_for("add_f32", 1))
-    ra, pa = dev_of(a, "f32")
-    rb, pb = dev_of(b, "f32")
-    rc, pc = dev_of(np.zeros_like(a), "f32")
-    del a, b
-    # bias add + ReLU fused in one pass, against ew_add then ew_relu in place
-    record("add_relu_f32_2p28_fused", "add_relu", "f32", n28, lambda: L.ew_add_relu(0, pa, pb, pc, n28, s))
-
-    def unfused():
-        for st in (L.ew_add(0, pa, pb, pc, n28, s), L.ew_relu(0, pc, pc, n28, s)):
-            if st != 0:
-                raise ew.EwError(st, "add then relu")
-    total, kern = time_launches(torch, stream, unfused, 50, 3)
-    nb = metrics.algorithmic_bytes("add_relu", "f32", n28)
-    out["add_then_relu_f32_2p28_unfused"] = {
-        "gbps": metrics.gbps(nb, kern), "frac": metrics.gbps(nb, kern) / peak, "kernel_ms": kern * 1e3,
-        "bytes_per_launch": nb, "note": "two launches per step (add, then ReLU in place); GB/s counts the "
-                                        "fused operation's 12 bytes per element"}
-    # SAXPY + ReLU fused in one pass (y = relu(2.5 x + y) in place, on A and C),
-    # against ew_saxpy then ew_relu in place
-    record("saxpy_relu_f32_2p28_fused", "saxpy_relu", "f32", n28,
-           lambda: L.ew_saxpy_relu(0, 2.5, pa, pc, n28, s))
-
-    def saxpy_unfused():
-        for st in (L.ew_saxpy(0, 2.5, pa, pc, n28, s), L.ew_relu(0, pc, pc, n28, s)):
-            if st != 0:
-                raise ew.EwError(st, "saxpy then relu")
-    total, kern = time_launches(torch, stream, saxpy_unfused, 50, 3)
-    nb = metrics.algorithmic_bytes("saxpy_relu", "f32", n28)
-    out["saxpy_then_relu_f32_2p28_unfused"] = {
-        "gbps": metrics.gbps(nb, kern), "frac": metrics.gbps(nb, kern) / peak, "kernel_ms": kern * 1e3,
-        "bytes_per_launch": nb, "note": "two launches per step (SAXPY, then ReLU in place); GB/s counts "
-                                        "the fused operation's 12 bytes per element"}
-    for label, path, sched in (("persistent", "auto", "persistent"), ("tma", "tma", "auto")):
-        ew.set_path(path)
-        ew.set_schedule(sched)
-        record("add_f32_2p28_" + label, "add", "f32", n28, lambda: L.ew_add(0, pa, pb, pc, n28, s))
-    ew.set_path("tma")
-    ew.set_schedule("auto")
-    record("copy_f32_2p26_tma", "copy", "f32", n26, lambda: L.ew_copy(0, pa, pb, n26, s), steps=200)
-    ew.set_path("auto")
-    del ra, rb, rc
-    # chains of short calls, launched back to back without events in between:
-    # programmatic dependent launch on (the default) against off
-    for lg in (20, 23, 25):
-        m = 1 << lg
-        cx = torch.zeros(m, device=dev)
-        cy = torch.zeros(m, device=dev)
-        px2, py2 = cx.data_ptr(), cy.data_ptr()
-        for prog in (True, False):
-            ew.set_programmatic_launch(prog)
-            for _ in range(10):
-                L.ew_saxpy(0, 0.5, px2, py2, m, s)
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(200):
-                st = L.ew_saxpy(0, 0.5, px2, py2, m, s)
-                if st != 0:
-                    raise ew.EwError(st, "saxpy chain")
-            e1.record(stream)
-            torch.cuda.synchronize()
-            per = e0.elapsed_time(e1) / 1e3 / 200
-            nb = metrics.algorithmic_bytes("saxpy", "f32", m)
-            out["saxpy_chain_f32_2p%d_%s" % (lg, "pdl" if prog else "plain")] = {
-                "gbps": metrics.gbps(nb, per), "frac": metrics.gbps(nb, per) / peak,
-                "kernel_ms": per * 1e3, "bytes_per_launch": nb,
-                "note": "200 launches back to back, time per launch from one event pair"}
-        ew.set_programmatic_launch(True)
-        del cx, cy
-    # device-to-device copy ceiling of this GPU (cudaMemcpyAsync via torch copy_, 2 GiB,
-    # read + write bytes), timed on the same stream
-    big = torch.empty(1 << 31, dtype=torch.uint8, device=dev)
-    big2 = torch.empty_like(big)
-
-    def d2d():
-        with torch.cuda.stream(stream):
-            big2.copy_(big, non_blocking=True)
-    total, kern = time_launches(torch, stream, d2d, 20, 3)
-    g = metrics.gbps(2 * big.numel(), kern)
-    out["memcpy_d2d_2GiB"] = {"gbps": g, "frac": g / peak, "kernel_ms": kern * 1e3,
-                              "note": "library device-to-device copy (torch copy_), read+write bytes"}
-    for ent in out.values():  # against the copy ceiling measured in this run
-        ent["frac_of_d2d"] = ent["gbps"] / g
-    out["gather2_f32_2p26"]["sectors_per_request"] = {
-        "gather": 8.0, "contiguous_copy_32bit_lanes": 4.0,
-        "source": "ncu l1tex__average_t_sectors_per_request_pipe_lsu_mem_global_op_ld.ratio, "
-                  "profiles/gather2_f32_2p26.md"}
-    return out
+    return {"value": metrics.gbps(12 * n * reps, el), "cores": cores, "matches_single_core": same}
 
 
 def run_ours(args):
@@ -725,6 +1192,7 @@ def run_ours(args):
     peak, peak_src = measured_peak()
     clocks = ClockSampler(local)
     clocks.start()
+    nvml = NvmlClocks(pci_bus_id(torch, dev), local)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -732,14 +1200,16 @@ def run_ours(args):
         dist.barrier()
     torch.cuda.synchronize()
     clocks.mark("start")
-    total, kern = time_launches(torch, stream, step, args.steps, 0)
+    total, kern = time_launches(torch, stream, step, args.steps, 0, poll=nvml.sample)
     per_launch = sorted(time_launches.last_per_launch)
     clocks.mark("stop")
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     rec = ew.last_launch()
-    clk = clocks.stop()
+    rec["path"] = ew.PATH_NAMES.get(rec["path"], rec["path"])
+    clk_run = clocks.stop()
+    clk = nvml.summary() or clk_run
     if world > 1:
         t = torch.tensor([total, kern], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -810,45 +1280,22 @@ def run_ours(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_total, e2e_serial_total, e2e_piped_total = float(t[0]), float(t[1]), float(t[2])
     e2e_value = metrics.gbps(step_bytes * e2e_steps * world, e2e_total)
-    e2e_serial = metrics.gbps(step_bytes * e2e_steps * world, e2e_serial_total)
-    e2e_piped = metrics.gbps(step_bytes * e2e_steps * world, e2e_piped_total)
     e2e_ok = bool(torch.equal(c_pin, c.cpu())) and piped_ok
+    e2e = {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": 8 * n, "d2h_bytes_per_step": 4 * n,
+           "steps": e2e_steps, "result_matches_device": e2e_ok,
+           "how": "ew_add on pinned host A, B, C: the kernel reads 8N bytes from and writes 4N bytes "
+                  "to host memory over the CPU-GPU link every step"}
+    e2e_staged = {"staged_pipelined_gbps": metrics.gbps(step_bytes * e2e_steps * world, e2e_piped_total),
+                  "staged_pipelined_how": "cudaMemcpyAsync H2D of A, B, ew_add on device copies, D2H of C, "
+                                          "in %d chunks overlapped on three streams" % len(spans),
+                  "staged_serial_gbps": metrics.gbps(step_bytes * e2e_steps * world, e2e_serial_total)}
 
-    line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": value / PAGE_BASELINE["value"], "baseline": PAGE_BASELINE,
-        "dtype": "f32",
-        "data": "synthetic: A, B i.i.d. uniform[-1,1) binary32, seeded PCG64 per rank",
-        "config": {"workload": "fp32 add C=A+B, N=2^28 per GPU", "n": n, "slice": [lo, hi],
-                   "bytes_per_step_per_gpu": step_bytes,
-                   "l2": "no flush: inputs larger than L2 (3.2 GB working set vs 129 MB L2)",
-                   "path": ew.PATH_NAMES.get(rec["path"], rec["path"]), "vec_bytes": rec["vec_bytes"],
-                   "grid": rec["grid"], "block": rec["block"],
-                   "gpu": torch.cuda.get_device_name(dev), **device_facts(torch, dev)},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
-                     "traffic_note": traffic_note, "kernel_ms": kern * 1e3,
-                     "kernel_ms_median": per_launch[len(per_launch) // 2] * 1e3,
-                     "kernel_ms_min": per_launch[0] * 1e3,
-                     "gelem_per_s": n / kern / 1e9,
-                     "frac_of_nominal_8tbs": achieved / 8000.0},
-        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": 8 * n,
-                "d2h_bytes_per_step": 4 * n, "steps": e2e_steps, "result_matches_device": e2e_ok,
-                "how": "ew_add called on pinned host A, B, C: the kernel reads 8N bytes from and "
-                       "writes 4N bytes to host memory over the CPU-GPU link every step",
-                "staged_pipelined_value": e2e_piped,
-                "staged_pipelined_how": "cudaMemcpyAsync H2D of A, B, ew_add on device copies, D2H of C, "
-                                        "in %d chunks overlapped on three streams" % len(spans),
-                "staged_serial_value": e2e_serial},
-        "gpu_launches": args.steps,
-        "clocks": clk,
-    }
-
+    # parity of the headline output, then the CPU baseline (rank 0, one GPU)
+    torch.cuda.synchronize()
+    c_host = c.cpu().numpy()
+    cpu_baseline, all_cores, parity = None, None, "unchecked"
     if rank == 0 and world == 1 and not args.no_cpu:
         import oracle
-        torch.cuda.synchronize()
-        c_host = c.cpu().numpy()
         t0 = time.perf_counter()
         reps = 0
         want = None
@@ -859,17 +1306,48 @@ def run_ours(args):
             if el >= 10.0 or el / reps * (reps + 1) > 30.0:
                 break
         cpu_gbps = metrics.gbps(step_bytes * reps, el)
-        parity = bool(np.array_equal(want.view(np.uint32), c_host.view(np.uint32)))
-        line["cpu_baseline"] = {"value": cpu_gbps, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                                "sample": "%d full passes over the N=2^28 inputs (%.1f s)" % (reps, el),
-                                "cpu": host_cpu_model(),
-                                "gpu_output_bit_exact_vs_oracle": parity,
-                                "all_cores": oracle_all_cores(oracle, metrics, a_h, b_h, want)}
-        line["parity"] = "bit-exact over all 2^28 outputs" if parity else "MISMATCH"
-    if not args.no_aux and world == 1:
-        line["aux"] = aux_measurements(torch, ew, inputs, metrics, stream, peak, dev)
+        parity = True if np.array_equal(want.view(np.uint32), c_host.view(np.uint32)) else "MISMATCH"
+        all_cores = oracle_all_cores(oracle, metrics, a_h, b_h, want)
+        cpu_baseline = {"value": cpu_gbps, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                        "sample": "%d full passes over the N=2^28 inputs (%.1f s)" % (reps, el),
+                        "cpu": host_cpu_model(), "all_cores_value": all_cores["value"],
+                        "all_cores_cores": all_cores["cores"]}
+        del want
+    elif not args.no_cpu:  # other ranks and multi-GPU runs: seeded windows of the output
+        chk = Parity(True)
+        pr = True
+        for w0, w1 in parity_windows(n, 1234 + rank):
+            if first_mismatch(c_host[w0:w1], chk.oracle.add("f32", a_h[w0:w1], b_h[w0:w1]), "f32", True) is not None:
+                pr = "MISMATCH"
+                break
+        parity = pr
+    if world > 1:
+        t = torch.tensor([1.0 if parity is True else 0.0], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MIN)
+        if parity is True and float(t[0]) < 1.0:
+            parity = "MISMATCH on another rank"
+
+    aux_line = None
     if rank == 0:
-        print(json.dumps(line), flush=True)
+        aux_line = {"aux_of": METRIC, "e2e_staged": e2e_staged, "clocks_whole_run": clk_run,
+                    "peak_source": peak_src, "baseline": PAGE_BASELINE,
+                    "device": {"gpu": torch.cuda.get_device_name(dev), **device_facts(torch, dev)}}
+        if all_cores is not None:
+            aux_line["cpu_all_cores"] = all_cores
+    if not args.no_aux and world == 1:
+        del a_pin, b_pin, c_pin, a_d, b_d, c_d
+        facts = device_facts(torch, dev)
+        aux = Aux(torch, ew, inputs, metrics, stream, peak, dev, Parity(not args.no_cpu), facts.get("l2_bytes"))
+        aux_line["aux"] = aux.run()
+    if rank == 0:
+        facts = device_facts(torch, dev)
+        line = headline_line(
+            value=value, parity=parity, world=world, steps=args.steps, warmup=args.warmup, total_s=total,
+            n=n, lo=lo, hi=hi, step_bytes=step_bytes, rec=rec, facts=facts,
+            gpu_name=torch.cuda.get_device_name(dev), achieved=achieved, peak=peak, peak_src=peak_src,
+            traffic=traffic, traffic_note=traffic_note, kern_s=kern, per_launch=per_launch, e2e=e2e,
+            clocks=clk, cpu_baseline=cpu_baseline)
+        emit(aux_line, line)
     if world > 1:
         dist.destroy_process_group()
 
@@ -880,6 +1358,10 @@ def main():
         run_profile_case(args)
     elif args.impl == "reference":
         run_reference(args)
+    elif args.ab == "widths":
+        run_ab_widths(args)
+    elif args.ab == "gather":
+        run_ab_gather(args)
     else:
         run_ours(args)
 

@@ -149,7 +149,11 @@ typedef enum {
  *                     reads the contiguous input span that its positions of
  *                     all s laps draw from (32 KiB) once, coalesced, into
  *                     shared memory with one row per residue mod s, then
- *                     writes each lap's outputs as one coalesced run.
+ *                     writes each lap's outputs as one coalesced run.  For
+ *                     s = 8, 16, 32 or 64 and an input aligned to 16 bytes a
+ *                     kernel specialised for that stride runs (division by
+ *                     s as shifts, a conflict-free shared-memory layout, one
+ *                     lap per warp; the launch record shows EW_PATH_V128).
  * EW_SCHED_AUTO       for the gather: EW_SCHED_LAPS for s < 8, EW_SCHED_TILED
  *                     for 8 <= s <= 64 (the measured crossover: from s = 8 a
  *                     lap-ordered fp32 warp load spends one 32-byte sector per
@@ -290,11 +294,23 @@ EW_API const char *ew_status_string(ew_status status);
 /* cudaError_t value behind the last EW_ERR_CUDA returned on this thread (0 if none). */
 EW_API int ew_last_cuda_error(void);
 
-/* Read and clear the device-side error word of the current device after
- * synchronising `stream`.  *code = 0 when no bounded wait has given up since the
- * last read; otherwise the wait site that gave up (1: a bulk-copy tile of
- * EW_PATH_TMA, 99: ew_selftest_bounded_wait).  Returns EW_ERR_TIMEOUT when
- * *code != 0, EW_ERR_CUDA when the synchronisation itself fails. */
+/* Read and clear the device-side error word of the current device, in stream
+ * order on `stream`, then synchronise `stream`.  The read and the clear are one
+ * atomic exchange on the device: a code that a kernel on another stream records
+ * meanwhile is either returned here or kept for the next call.  *code = 0 when
+ * no bounded wait has given up since the last read; otherwise the wait site
+ * that gave up:
+ *   1   a tile of a bulk-copy kernel: under EW_PATH_TMA, and under
+ *       EW_PATH_AUTO for 16-bit operands whose pointers differ in parity, from
+ *       n >= 2^22 on device memory (the realigning bulk copy).  The outputs of
+ *       the calls that ran such a kernel since the last read are undefined:
+ *       the CTA that gave up skipped its remaining tiles, and if its second
+ *       bounded wait (for loads already issued) also expired it left with
+ *       loads still in flight.  Callers of those paths that must know their
+ *       results are complete check this word after synchronising.
+ *   99  ew_selftest_bounded_wait.
+ * Returns EW_ERR_TIMEOUT when *code != 0, EW_ERR_CUDA when the exchange, the
+ * copy or the synchronisation fails. */
 EW_API ew_status ew_device_error(ew_stream_t stream, int32_t *code);
 
 /* Self-test of the bounded device waits: enqueues one block that arms an

@@ -301,7 +301,8 @@ def selftest_bounded_wait(limit_ns, stream=None):
 
 
 def device_error(stream=None):
-    """Synchronise ``stream``, then read and clear the device error word."""
+    """Read and clear the device error word (one atomic exchange ordered on
+    ``stream``), then synchronise ``stream``; returns (status, code)."""
     import torch
     code = ctypes.c_int32(0)
     st = lib().ew_device_error(_stream(stream, torch.cuda.current_device()), ctypes.byref(code))

@@ -427,7 +427,7 @@ ew_status check_alias(const void *in, const void *out, int64_t bytes) {
 struct GatherLaunch {
     const GatherEntry *entry = nullptr;
     GatherArgs args{};
-    int grid = 0;
+    int grid = 0, block = kBlock;
     int32_t path = EW_PATH_SCALAR, vec_bytes = 0, smem = 0, schedule = EW_SCHED_ONESHOT;
     int64_t head = 0, nvec = 0, tail = 0;
 };
@@ -503,9 +503,28 @@ GatherLaunch plan_gather_span(const void *in, void *out, uint64_t n, uint64_t s_
 }
 
 // Tiled kernel: P (a power of two) positions of every lap per block, the
-// 32 KiB input span they draw from staged in shared memory, rows padded.
+// 32 KiB input span they draw from staged in shared memory, rows padded.  A
+// power-of-two stride from 8 to 64 on a 16-byte aligned input takes the
+// kernel specialised for that stride (16-byte loads; the launch record shows
+// EW_PATH_V128 and vec_bytes 16), any other the general one.
 GatherLaunch plan_gather_tiled(int e, const void *in, void *out, uint64_t n, uint64_t s_mod) {
     GatherLaunch gl;
+    const GatherEntry *pow2 = e == 4 ? gather_tiled_pow2_4(s_mod) : gather_tiled_pow2_2(s_mod);
+    if (pow2 != nullptr && reinterpret_cast<uintptr_t>(in) % 16 == 0) {
+        gl.entry = pow2;
+        gl.args = gather_args(in, out, n, s_mod);
+        gl.args.tile_p = (kTiledPow2SpanBytes / e) / static_cast<uint32_t>(s_mod);
+        set_lap_geometry(&gl.args, n, s_mod);
+        const uint64_t lap_len = (n + s_mod - 1) / s_mod;
+        gl.grid = clamp_grid(static_cast<int64_t>((lap_len + gl.args.tile_p - 1) / gl.args.tile_p));
+        gl.path = EW_PATH_V128;
+        gl.vec_bytes = 16;
+        gl.smem = pow2->smem_bytes;
+        gl.block = kTiledPow2Threads;
+        gl.schedule = EW_SCHED_TILED;
+        gl.nvec = static_cast<int64_t>(n);
+        return gl;
+    }
     gl.entry = e == 4 ? gather_tiled_4() : gather_tiled_2();
     gl.args = gather_args(in, out, n, s_mod);
     const uint32_t per_block = (kTiledSpanBytes / e) / static_cast<uint32_t>(s_mod);
@@ -691,7 +710,7 @@ ew_status ew_gather_stride(ew_dtype dt, const void *in, void *out, int64_t n, in
     t_last.path = gl.path;
     t_last.vec_bytes = gl.vec_bytes;
     t_last.grid = gl.grid;
-    t_last.block = kBlock;
+    t_last.block = gl.block;
     t_last.smem = gl.smem;
     t_last.schedule = gl.schedule;
     t_last.head = gl.head;

@@ -32,8 +32,11 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), unsigned grid, unsigned bloc
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
-    return e != cudaSuccess ? e : cudaGetLastError();
+    // The launch's own status: an error recorded earlier on this thread by
+    // another runtime call is not this call's failure and is left alone.
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    if (e != cudaSuccess) (void)cudaGetLastError();  // the failure is returned; do not leave it pending too
+    return e;
 }
 
 // Operator ids of the streaming (contiguous) kernels.
@@ -102,6 +105,7 @@ struct GatherEntry {
     const void *kernel;
     GatherLaunchFn launch;
     int unroll;
+    int smem_bytes = 0;  // static shared memory per block, for the launch record
 };
 // Lap-ordered gather: 2 <= s_mod <= kMaxLaps, n <= 2^32 and n >= s_mod x the
 // outputs of one block.
@@ -113,6 +117,13 @@ const GatherEntry *gather_laps_2();
 constexpr uint32_t kTiledSpanBytes = 32768;
 const GatherEntry *gather_tiled_4();
 const GatherEntry *gather_tiled_2();
+// Tiled gather specialised for a power-of-two stride (8, 16, 32 or 64) and an
+// input aligned to 16 bytes; nullptr for other strides.  Each block of
+// kTiledPow2Threads threads stages kTiledPow2SpanBytes of input.
+constexpr int kTiledPow2SpanBytes = 16384;
+constexpr int kTiledPow2Threads = 256;
+const GatherEntry *gather_tiled_pow2_4(uint64_t stride);
+const GatherEntry *gather_tiled_pow2_2(uint64_t stride);
 const GatherEntry *gather_oneshot_4();  // binary32, n <= 2^32
 const GatherEntry *gather_stride_4();   // binary32, any n
 const GatherEntry *gather_oneshot_2();  // 16-bit types
@@ -156,7 +167,8 @@ const TmaEntry *tma_realign_entry(int op, int dtype);
 // One CTA that arms an mbarrier no copy will complete and must give up after
 // limit_ns, recording error code 99 (checks the bounded-wait path).
 cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t s);
-// Device error word written by bounded waits (read and cleared by the host).
+// Device error word written by bounded waits: read and cleared in one atomic
+// exchange on the device, ordered on stream s.
 cudaError_t read_and_clear_device_error(cudaStream_t s, int32_t *code);
 
 }  // namespace ew

@@ -317,6 +317,147 @@ __global__ void __launch_bounds__(kBlock) gather_tiled_kernel(const GatherArgs g
     }
 }
 
+// Tiled gather for a power-of-two stride S (8 <= S <= 64) known at compile
+// time, and an input aligned to 16 bytes.  Same schedule as the tiled kernel
+// above: block b owns positions [b*P, (b+1)*P) of every lap and stages the
+// 32 KiB input span they draw from.  With S a compile-time power of two every
+// division by S is a shift, and a thread's 16-byte loads all land in the
+// same rows: thread t's load i holds the span elements j = V*t + V*kBlock*i
+// (V elements per load), i.e. rows (V*t) mod S onwards and column
+// (V*t) / S + i*V*kBlock/S, so its shared-memory stores use one base address
+// and compile-time offsets.  The rows are padded (and, from row 32 on,
+// shifted) so that the 32 lanes of a warp storing element k of their loads
+// hit 32 different banks; the layout is found at compile time.  Each warp
+// then writes whole laps: lane l stores positions l, l + 32, ... of its lap's
+// run from one row, 4-byte words where the run allows (pairs of 16-bit
+// elements), in a fully unrolled loop.  The last block, whose span is cut
+// short by n, stages and stores element by element with bounds checks.
+struct TiledLayout {
+    uint32_t pad;  // elements added to every row
+    uint32_t x;    // elements added per 32 rows
+};
+
+template <int E, int S, int kSpanBytes>
+constexpr TiledLayout tiled_pow2_layout() {
+    constexpr uint32_t kPerVec = 16 / E, kP = (kSpanBytes / E) / S, kStep = E == 2 ? 2 : 1;
+    for (uint32_t pad = 0; pad < 32; pad += kStep) {
+        for (uint32_t x = 0; x < 64; x += kStep) {
+            uint32_t banks = 0, words[32] = {};
+            bool ok = true;
+            for (uint32_t t = 0; t < 32 && ok; ++t) {
+                const uint32_t j = kPerVec * t, row = j % S, col = j / S;
+                const uint32_t word = ((row * (kP + pad) + x * (row >> 5) + col) * E) / 4;
+                bool same_word = false;  // two halves of one word: one access
+                for (uint32_t q = 0; q < t; ++q) same_word = same_word || words[q] == word;
+                words[t] = word;
+                if (same_word) continue;
+                ok = (banks >> (word % 32) & 1u) == 0;
+                banks |= 1u << (word % 32);
+            }
+            if (ok) return TiledLayout{pad, x};
+        }
+    }
+    return TiledLayout{~0u, 0};
+}
+
+// Geometry of the power-of-two tiled gather: element size E, stride S, input
+// span per block, threads per block.
+template <int E, int S, int kSpanBytes = kTiledPow2SpanBytes, int kThreads = kTiledPow2Threads>
+struct TiledPow2 {
+    static_assert(S >= 8 && S <= 64 && (S & (S - 1)) == 0, "power-of-two stride from 8 to 64");
+    static constexpr uint32_t kPerVec = 16 / E;                    // elements per 16-byte load
+    static constexpr uint32_t kSpan = kSpanBytes / E;              // input elements per block
+    static constexpr uint32_t kP = kSpan / S;                      // positions per lap per block
+    static constexpr uint32_t kLog2S = S == 8 ? 3 : S == 16 ? 4 : S == 32 ? 5 : 6;
+    static constexpr uint32_t kLoads = kSpan / kPerVec / kThreads;  // 16-byte loads per thread
+    static constexpr uint32_t kColStep = kThreads * kPerVec / S;    // columns between a thread's loads
+    static constexpr uint32_t kPad = tiled_pow2_layout<E, S, kSpanBytes>().pad;
+    static constexpr uint32_t kX = tiled_pow2_layout<E, S, kSpanBytes>().x;
+    static constexpr uint32_t kPitch = kP + kPad;
+    static constexpr uint32_t kElems = S * kPitch + kX * ((S - 1) >> 5);
+    static constexpr int kSmemBytes = static_cast<int>((kElems * E + 15) / 16 * 16);
+    static_assert(kPad != ~0u, "no bank-conflict-free row layout");
+    static_assert(kLoads >= 1 && kLoads * kThreads * kPerVec == kSpan, "whole 16-byte loads per thread");
+    static_assert(kP % 32 == 0 && kThreads >= S, "whole warps per lap run; one thread per lap");
+    static_assert(E == 4 || (kPitch % 2 == 0 && kX % 2 == 0), "16-bit rows must start on whole words");
+    __host__ __device__ static constexpr uint32_t row_offset(uint32_t r) { return r * kPitch + kX * (r >> 5); }
+};
+
+template <int E, int S, int kSpanBytes, int kThreads>
+__global__ void __launch_bounds__(kThreads) gather_tiled_pow2_kernel(const GatherArgs g) {
+    enter_grid();
+    using T = TiledPow2<E, S, kSpanBytes, kThreads>;
+    using W = typename std::conditional<E == 4, uint32_t, uint16_t>::type;
+    __shared__ __align__(16) W tile[T::kElems];
+    __shared__ uint32_t lap_start[S], lap_len[S], lap_row[S];
+    W *out = static_cast<W *>(g.out);
+    const uint32_t p0 = blockIdx.x * T::kP;
+    if (threadIdx.x < S) {  // lap L: first output, length, offset of its source row
+        const uint32_t L = threadIdx.x, a0 = L * g.lap_m;
+        const uint32_t c0 = (a0 + S - 1) >> T::kLog2S;             // ceil(L*m/S)
+        const uint32_t c1 = (a0 + g.lap_m + S - 1) >> T::kLog2S;
+        lap_start[L] = L * g.lap_q + c0;
+        lap_len[L] = g.lap_q + (c1 - c0);
+        lap_row[L] = T::row_offset(c0 * S - a0);
+    }
+    const uint64_t j0 = static_cast<uint64_t>(S) * p0;  // first source of the span
+    const W *src = static_cast<const W *>(g.in) + j0;
+    const bool full = j0 + T::kSpan <= g.n;              // block-uniform
+    if (full) {
+        const char *src_bytes = reinterpret_cast<const char *>(src);
+        Vec<16> v[T::kLoads];
+#pragma unroll
+        for (uint32_t i = 0; i < T::kLoads; ++i) v[i] = ld<16>(src_bytes + (threadIdx.x + i * kThreads) * 16u);
+        const uint32_t j = T::kPerVec * threadIdx.x;
+        W *dst = tile + T::row_offset(j & (S - 1)) + (j >> T::kLog2S);
+#pragma unroll
+        for (uint32_t i = 0; i < T::kLoads; ++i) {
+#pragma unroll
+            for (uint32_t k = 0; k < T::kPerVec; ++k) {
+                const uint32_t w = v[i].w[k * E / 4];
+                dst[k * T::kPitch + i * T::kColStep] = static_cast<W>(E == 4 ? w : w >> (16u * (k & 1u)));
+            }
+        }
+    } else {
+        const uint32_t avail = static_cast<uint32_t>(g.n - j0);  // fewer than kSpan
+        for (uint32_t j = threadIdx.x; j < avail; j += kThreads)
+            tile[T::row_offset(j & (S - 1)) + (j >> T::kLog2S)] = src[j];
+    }
+    __syncthreads();
+    const uint32_t lane = threadIdx.x & 31u;
+    for (uint32_t L = threadIdx.x >> 5; L < S; L += kThreads / 32) {  // one lap per warp at a time
+        const W *row = tile + lap_row[L];
+        W *dst = out + (static_cast<size_t>(lap_start[L]) + p0);
+        if (full) {  // the whole run [0, P) of every lap lies before n
+            if (E == 4 || (reinterpret_cast<uintptr_t>(dst) & 3u) == 0) {
+                const uint32_t *row_w = reinterpret_cast<const uint32_t *>(row);
+                uint32_t *dst_w = reinterpret_cast<uint32_t *>(dst);
+#pragma unroll
+                for (uint32_t i = 0; i < T::kP * E / 4 / 32; ++i) dst_w[lane + 32 * i] = row_w[lane + 32 * i];
+            } else {
+#pragma unroll 8
+                for (uint32_t i = 0; i < T::kP / 32; ++i) dst[lane + 32 * i] = row[lane + 32 * i];
+            }
+        } else {
+            const uint32_t len = lap_len[L] > p0 ? min(lap_len[L] - p0, T::kP) : 0u;
+            for (uint32_t q = lane; q < len; q += 32) dst[q] = row[q];
+        }
+    }
+}
+
+template <int E, int S, int kSpanBytes, int kThreads>
+cudaError_t launch_gather_tiled_pow2(const GatherArgs &g, int grid, cudaStream_t s) {
+    return launch_kernel(&gather_tiled_pow2_kernel<E, S, kSpanBytes, kThreads>, grid, kThreads, 0, s, g);
+}
+
+template <int E, int S, int kSpanBytes = kTiledPow2SpanBytes, int kThreads = kTiledPow2Threads>
+constexpr GatherEntry tiled_pow2_entry() {
+    using T = TiledPow2<E, S, kSpanBytes, kThreads>;
+    return GatherEntry{reinterpret_cast<const void *>(&gather_tiled_pow2_kernel<E, S, kSpanBytes, kThreads>),
+                       &launch_gather_tiled_pow2<E, S, kSpanBytes, kThreads>, static_cast<int>(T::kLoads),
+                       T::kSmemBytes};
+}
+
 // Grid-stride gather for any n: with i = v + k*T (T = grid threads),
 // (s*i) mod n advances by (s*T) mod n per slot, so each thread needs one
 // modular product and then conditional subtractions.

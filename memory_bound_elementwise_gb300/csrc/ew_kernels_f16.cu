@@ -42,6 +42,19 @@ const StreamEntry *stream_table_f16() { return &kTable[0][0]; }
 const GatherEntry *gather_oneshot_2() { return &kGatherOneshot; }
 const GatherEntry *gather_laps_2() { return &kGatherLaps; }
 const GatherEntry *gather_tiled_2() { return &kGatherTiled; }
+
+static const GatherEntry kGatherTiledPow2[4] = {tiled_pow2_entry<2, 8>(), tiled_pow2_entry<2, 16>(),
+                                                tiled_pow2_entry<2, 32>(), tiled_pow2_entry<2, 64>()};
+
+const GatherEntry *gather_tiled_pow2_2(uint64_t stride) {
+    switch (stride) {
+        case 8: return &kGatherTiledPow2[0];
+        case 16: return &kGatherTiledPow2[1];
+        case 32: return &kGatherTiledPow2[2];
+        case 64: return &kGatherTiledPow2[3];
+        default: return nullptr;
+    }
+}
 const GatherEntry *gather_stride_2() { return &kGatherStride; }
 
 }  // namespace ew

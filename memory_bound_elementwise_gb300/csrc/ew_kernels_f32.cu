@@ -50,6 +50,19 @@ const GatherEntry *gather_span_4(int64_t stride) {
 const GatherEntry *gather_oneshot_4() { return &kGatherOneshot; }
 const GatherEntry *gather_laps_4() { return &kGatherLaps; }
 const GatherEntry *gather_tiled_4() { return &kGatherTiled; }
+
+static const GatherEntry kGatherTiledPow2[4] = {tiled_pow2_entry<4, 8>(), tiled_pow2_entry<4, 16>(),
+                                                tiled_pow2_entry<4, 32>(), tiled_pow2_entry<4, 64>()};
+
+const GatherEntry *gather_tiled_pow2_4(uint64_t stride) {
+    switch (stride) {
+        case 8: return &kGatherTiledPow2[0];
+        case 16: return &kGatherTiledPow2[1];
+        case 32: return &kGatherTiledPow2[2];
+        case 64: return &kGatherTiledPow2[3];
+        default: return nullptr;
+    }
+}
 const GatherEntry *gather_stride_4() { return &kGatherStride; }
 
 }  // namespace ew

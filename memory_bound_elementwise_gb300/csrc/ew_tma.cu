@@ -18,6 +18,7 @@
 // drains its bulk stores and returns; the host reads the code with
 // ew_device_error.
 #include <atomic>
+#include <mutex>
 #include <type_traits>
 
 #include "ew_internal.h"
@@ -26,6 +27,8 @@
 namespace ew {
 
 __device__ int32_t g_device_error = 0;
+// What the last read-and-clear took out of g_device_error (copied to the host).
+__device__ int32_t g_device_error_taken = 0;
 
 namespace {
 
@@ -158,7 +161,12 @@ __global__ void __launch_bounds__(kTmaBlock) tma_kernel(const TmaArgs a) {
     }
     if (threadIdx.x == 0) {
         bulk_store_drain();
-        if (s_failed)  // let copies still in flight land before the CTA exits
+        // After a wait gave up, let the loads still in flight land before the
+        // CTA exits.  Only if this second wait expires too (both limits, 2 s in
+        // all, with the memory system not delivering) does the CTA leave with
+        // loads possibly still writing into its shared memory; the call's
+        // outputs are then undefined, and code 1 in the error word says so.
+        if (s_failed)
             for (int r = s; r < cnt; ++r) (void)mbar_wait_bounded(&full[r], 0, a.wait_limit_ns);
     }
 }
@@ -247,7 +255,9 @@ __global__ void __launch_bounds__(kTmaBlock) tma_realign_kernel(const TmaArgs a)
     }
     if (threadIdx.x == 0) {
         bulk_store_drain();
-        if (s_failed)  // let copies still in flight land before the CTA exits
+        // as in tma_kernel: loads may still be in flight at exit only after
+        // both bounded waits expired, and code 1 then marks the outputs undefined
+        if (s_failed)
             for (int r = s; r < cnt; ++r) (void)mbar_wait_bounded(&full[r], 0, a.wait_limit_ns);
     }
 }
@@ -328,6 +338,15 @@ __global__ void wait_selftest_kernel(uint64_t limit_ns) {
     }
 }
 
+// Moves the error word out (leaving 0) in one atomic exchange, so a code that
+// a kernel on another stream records meanwhile is kept for the next read.
+__global__ void take_device_error_kernel() {
+    enter_grid();
+    g_device_error_taken = atomicExch(&g_device_error, 0);
+}
+
+std::mutex g_take_mu;  // one reader of g_device_error_taken at a time
+
 }  // namespace
 
 const TmaEntry *tma_entry(int op, int dtype) {
@@ -347,14 +366,11 @@ cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t s) {
 }
 
 cudaError_t read_and_clear_device_error(cudaStream_t s, int32_t *code) {
+    std::lock_guard<std::mutex> lk(g_take_mu);
     int32_t v = 0;
-    const int32_t zero = 0;
-    cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_device_error, sizeof(v), 0,
-                                              cudaMemcpyDeviceToHost, s);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    if (e == cudaSuccess && v != 0)
-        e = cudaMemcpyToSymbolAsync(g_device_error, &zero, sizeof(zero), 0,
-                                    cudaMemcpyHostToDevice, s);
+    cudaError_t e = launch_kernel(&take_device_error_kernel, 1, 1, 0, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyFromSymbolAsync(&v, g_device_error_taken, sizeof(v), 0, cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     *code = v;
     return e;

@@ -77,3 +77,153 @@ def test_traffic_lookup_is_tied_to_the_kernel_sources(tmp_path, monkeypatch):
     (prof / "traffic.json").write_text(json.dumps(good))
     assert bench.profiled_traffic("add_f32_v256")[0] is None
     assert bench.profiled_traffic("missing")[0] is None
+
+
+def _headline(parity=True, note_len=200):
+    per = [0.000449, 0.000448, 0.000450]
+    return bench.headline_line(
+        value=7137.7, parity=parity, world=1, steps=20, warmup=5, total_s=0.009, n=1 << 28, lo=0,
+        hi=1 << 28, step_bytes=12 << 28,
+        rec={"path": "v256", "vec_bytes": 32, "grid": 65536, "block": 256},
+        facts={"sms": 152, "l2_bytes": 135528448, "driver": "580.178.04"}, gpu_name="NVIDIA GB300",
+        achieved=7175.7, peak=6796.2, peak_src="measured hbm_gbs (copy, read+write bytes)",
+        traffic=3225885696, traffic_note="x" * note_len, kern_s=0.000449, per_launch=sorted(per),
+        e2e={"value": 301.4, "unit": "GB/s", "h2d_bytes_per_step": 8 << 28, "d2h_bytes_per_step": 4 << 28,
+             "steps": 10, "result_matches_device": True, "how": "y" * 150},
+        clocks={"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "sm_mhz_min": 2070.0, "reasons": ["sw_power_cap"],
+                "samples": 17, "window": "timed region", "source": "NVML"},
+        cpu_baseline={"value": 21.0, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                      "sample": "3 full passes over the N=2^28 inputs (11.2 s)", "cpu": "aarch64 Neoverse-V2",
+                      "all_cores_value": 135.0, "all_cores_cores": 16})
+
+
+def test_headline_is_the_last_line_and_compact():
+    import io
+    aux = {"aux_of": bench.METRIC, "aux": {"w%d" % k: {"gbps": 1.0, "note": "z" * 500} for k in range(60)}}
+    buf = io.StringIO()
+    bench.emit(aux, _headline(), out=buf)
+    lines = buf.getvalue().splitlines()
+    assert len(lines) == 2
+    assert json.loads(lines[0])["aux_of"] == bench.METRIC
+    last = lines[-1]
+    assert len(last.encode()) < 4096
+    d = json.loads(last)
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "cpu_baseline", "e2e",
+                "gpu_launches", "clocks", "parity"):
+        assert key in d, key
+    assert d["config"]["workload"] and d["value"] == 7137.7
+    for key in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
+        assert key in d["roofline"], key
+    for key in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"):
+        assert key in d["e2e"], key
+    for key in ("value", "unit", "cores", "kind", "sample"):
+        assert key in d["cpu_baseline"], key
+    assert d["e2e"]["h2d_bytes_per_step"] > 0 and d["e2e"]["d2h_bytes_per_step"] > 0
+
+
+def test_headline_refuses_to_grow_past_the_limit():
+    import io
+    with pytest.raises(RuntimeError):
+        bench.emit(None, _headline(note_len=5000), out=io.StringIO())
+
+
+def test_headline_withholds_value_on_mismatch():
+    d = _headline(parity="MISMATCH")
+    assert d["value"] is None and d["vs_baseline"] is None and d["parity"] == "MISMATCH"
+    assert _headline(parity="unchecked")["value"] == 7137.7
+
+
+def test_parity_windows_cover_head_tail_and_stay_in_range():
+    assert bench.parity_windows(1000, 1) == [(0, 1000)]
+    n = 1 << 28
+    w = bench.parity_windows(n, 7)
+    assert w[0] == (0, 1 << 20) and w[-1] == (n - (1 << 20), n)
+    assert all(0 <= lo < hi <= n and hi - lo == 1 << 20 for lo, hi in w)
+    assert len(w) >= 3
+    assert bench.parity_windows(n, 7) == w  # seeded
+    assert len(bench.parity_windows(33554432, 3, full_max=0)) >= 3
+
+
+def test_first_mismatch_bits_and_nan_class():
+    import numpy as np
+    a = np.array([1.0, -0.0, np.nan], dtype=np.float32)
+    b = a.copy()
+    assert bench.first_mismatch(a, b, "f32", False) is None
+    b[1] = 0.0  # -0 against +0 is a mismatch
+    assert bench.first_mismatch(a, b, "f32", True) == 1
+    c = a.copy()
+    c.view(np.uint32)[2] = 0x7FC00001  # another NaN: a match only as a class
+    assert bench.first_mismatch(a, c, "f32", True) is None
+    assert bench.first_mismatch(a, c, "f32", False) == 2
+    h = np.array([0x7E00, 0x3C00], dtype=np.uint16)
+    g = np.array([0x7E01, 0x3C00], dtype=np.uint16)
+    assert bench.first_mismatch(g, h, "f16", True) is None
+    assert bench.first_mismatch(np.array([1, 2], np.int32), np.array([1, 3], np.int32), "i32", True) == 1
+
+
+def test_nvml_summary_names_reasons():
+    out = bench.summarize_nvml_samples([(2070.0, 0), (2040.0, 0x4), (2070.0, 0x0)], 2070.0)
+    assert out["sm_mhz"] == 2070.0 and out["sm_mhz_min"] == 2040.0
+    assert out["reasons"] == ["sw_power_cap"] and out["window"] == "timed region"
+    hot = bench.summarize_nvml_samples([(1500.0, 0x40 | 0x8)], 2070.0)
+    assert hot["reasons"] == ["hw_slowdown", "hw_thermal_slowdown"]
+    assert bench.summarize_nvml_samples([], 2070.0) is None
+
+
+class _FakeNvml:
+    """Stands in for libnvidia-ml: writes through the byref arguments."""
+
+    def __init__(self):
+        self.mhz = iter([2070, 2055, 2070])
+        self.bits = iter([0, 0x4, 0])
+        self.bus = None
+
+    def nvmlInit_v2(self):
+        return 0
+
+    def nvmlDeviceGetHandleByPciBusId_v2(self, bus, h):
+        self.bus = bus
+        return 0
+
+    def nvmlDeviceGetHandleByIndex_v2(self, i, h):
+        return 0
+
+    def nvmlDeviceGetMaxClockInfo(self, h, kind, out):
+        out._obj.value = 2070
+        return 0
+
+    def nvmlDeviceGetClockInfo(self, h, kind, out):
+        out._obj.value = next(self.mhz)
+        return 0
+
+    def nvmlDeviceGetCurrentClocksEventReasons(self, h, out):
+        out._obj.value = next(self.bits)
+        return 0
+
+
+def test_nvml_clocks_through_a_fake_library():
+    fake = _FakeNvml()
+    clk = bench.NvmlClocks("00000000:01:00.0", 0, lib=fake)
+    assert clk.ok and fake.bus == b"00000000:01:00.0"
+    for _ in range(3):
+        clk.sample()
+    s = clk.summary()
+    assert s["samples"] == 3 and s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"]
+
+
+def test_sectors_lookup_is_tied_to_the_kernel_sources(tmp_path, monkeypatch):
+    from memory_bound_elementwise_gb300 import _build
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    ent = {"sectors_per_request": {"gather2_f32": 8.0, "copy_f32": 4.0, "metric": "m",
+                                   "source_digest": _build.source_digest()}}
+    (prof / "traffic.json").write_text(json.dumps(ent))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    got = bench.profiled_sectors()
+    assert got["gather"] == 8.0 and got["copy"] == 4.0
+    ent["sectors_per_request"]["source_digest"] = "0" * 64
+    (prof / "traffic.json").write_text(json.dumps(ent))
+    got = bench.profiled_sectors()
+    assert got["gather"] is None and got["copy"] is None

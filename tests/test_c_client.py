@@ -18,11 +18,29 @@ SRC = os.path.join(ROOT, "tests", "c", "abi_client.c")
 pytestmark = pytest.mark.skipif(not os.path.exists(ew.LIB_PATH), reason="libew.so not built")
 
 
-def _cudart_dir():
-    for d in ("/usr/local/cuda/lib64", "/usr/local/cuda/targets/sbsa-linux/lib",
-              "/usr/local/cuda/targets/x86_64-linux/lib"):
+def _cuda_lib_dirs():
+    """Library folders of the CUDA toolkit, on x86_64 and on Arm (sbsa) hosts."""
+    import glob
+    roots = [os.environ.get("CUDA_HOME"), "/usr/local/cuda"]
+    nv = shutil.which("nvcc")
+    if nv:
+        roots.append(os.path.dirname(os.path.dirname(os.path.realpath(nv))))
+    dirs = []
+    for r in roots:
+        if r:
+            dirs += [os.path.join(r, "lib64")] + sorted(glob.glob(os.path.join(r, "targets", "*", "lib")))
+    return dirs
+
+
+def _cudart_link_args():
+    """Link arguments for the CUDA runtime calls the client makes itself: the
+    toolkit's static runtime (present wherever nvcc is), else the shared one."""
+    for d in _cuda_lib_dirs():
+        if os.path.exists(os.path.join(d, "libcudart_static.a")):
+            return [os.path.join(d, "libcudart_static.a"), "-lpthread", "-ldl", "-lrt"]
+    for d in _cuda_lib_dirs():
         if os.path.exists(os.path.join(d, "libcudart.so")):
-            return d
+            return ["-L", d, "-lcudart", "-Wl,-rpath," + d]
     return None
 
 
@@ -33,15 +51,12 @@ def client(tmp_path_factory):
         pytest.skip("no C compiler")
     out = str(tmp_path_factory.mktemp("cabi") / "abi_client")
     libdir = os.path.dirname(ew.LIB_PATH)
+    cudart = _cudart_link_args()
+    if cudart is None:
+        pytest.skip("no CUDA runtime library to link the client against")
+    # the library file is libew.so: link it by path so no -l lookup rules apply
     cmd = [cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-O1", SRC, "-I", os.path.join(ROOT, "include"),
-           "-L", libdir, "-lew", "-Wl,-rpath," + libdir]
-    cudart = _cudart_dir()
-    if cudart:
-        cmd += ["-L", cudart, "-lcudart", "-Wl,-rpath," + cudart]
-    else:
-        pytest.skip("no libcudart.so to link the client against")
-    # the library file is libew.so: link it by path so no -lew lookup rules apply
-    cmd = [c for c in cmd if c != "-lew"] + [ew.LIB_PATH]
+           ew.LIB_PATH, "-Wl,-rpath," + libdir] + cudart
     subprocess.run(cmd + ["-o", out], check=True)
     return out
 

@@ -251,6 +251,19 @@ def test_bounded_wait_gives_up_and_reports():
     assert float(y.sum()) == float(sum(range(1, 500)))
 
 
+def test_device_error_read_on_another_stream():
+    """The error word is taken out by an atomic exchange ordered on the
+    reading stream: a code recorded by a kernel on stream A is returned by a
+    read on stream B once A's work is done, exactly once."""
+    a, b = torch.cuda.Stream(), torch.cuda.Stream()
+    assert ew.device_error() == (0, 0)
+    ew.selftest_bounded_wait(20_000_000, stream=a)  # 20 ms
+    a.synchronize()
+    assert ew.device_error(stream=b) == (7, 99)
+    assert ew.device_error(stream=a) == (0, 0)
+    assert ew.device_error(stream=b) == (0, 0)
+
+
 LAP_BLOCK = 2048  # outputs per block of the lap-ordered gather (256 threads x 8)
 
 
@@ -964,3 +977,56 @@ def test_gather_span_variant(dtype):
                 assert_bits_equal(bo.host(), oracle.gather_stride(x, s), "f32", False,
                                   "span gather n=%d s=%d offs=%d,%d" % (n, s, in_off, out_off))
                 assert bi.guards_intact() and bo.guards_intact()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16", "i32"])
+def test_gather_tiled_pow2(dtype):
+    """The tiled gather specialised for strides 8, 16, 32 and 64 (and strides
+    congruent to them mod n), on a 16-byte aligned input: one ragged block,
+    exactly one and several full 16 KiB spans, spans plus a ragged block, n
+    divisible by the stride (every lap on one residue row) and not (laps of
+    unequal length on distinct rows), output offsets that start laps on odd
+    and even elements (16-bit runs stored as words or as halves).  A 2-byte
+    input offset takes the general tiled kernel."""
+    L = ew.lib()
+    code = DT_CODE[dtype]
+    e = ESIZE[dtype]
+    span = 16384 // e  # input elements a block stages (16 KiB)
+    bits = "f32" if dtype == "i32" else dtype
+    for s in (8, 16, 32, 64):
+        sizes = (s + 1, 1000, span - 1, span, span + 1, 2 * span, 3 * span + 5, (1 << 20) + 3, 1 << 20)
+        for n in sizes:
+            x = inputs.random_bits(n, bits, 9900 + n + s)
+            for stride in ((s, n + s) if n < 2000 else (s,)):
+                for in_off, out_off in ((0, 0), (0, 1), (0, 3), (4 // e if e == 2 else 1, 2)):
+                    bi = GuardedBuffer(n, dtype, in_off).fill(x)
+                    bo = GuardedBuffer(n, dtype, out_off)
+                    assert L.ew_gather_stride(code, bi.view.data_ptr(), bo.view.data_ptr(), n, stride,
+                                              _stream()) == 0
+                    rec = ew.last_launch()
+                    aligned = (in_off * e) % 16 == 0
+                    assert rec["schedule"] == 4, (n, s, rec)
+                    assert rec["path"] == (2 if aligned else 1) and rec["vec_bytes"] == (16 if aligned else e), rec
+                    if aligned:
+                        assert rec["grid"] == -(-(-(-n // s)) // (span // s)), (n, s, rec)
+                    torch.cuda.synchronize()
+                    assert_bits_equal(bo.host(), oracle.gather_stride(x, stride), bits, False,
+                                      "pow2 tiled gather %s n=%d s=%d offs=%d,%d"
+                                      % (dtype, n, stride, in_off, out_off))
+                    assert bi.guards_intact() and bo.guards_intact()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("s", [16, 64])
+def test_gather_pow2_full_size_2p26(dtype, s):
+    """The bench's tiled gathers at n = 2^26, every output against the oracle."""
+    n = 1 << 26
+    x = inputs.as_dtype(inputs.uniform(n, inputs.seed_for("copy_f32", 3), 0.0, 1.0), dtype)
+    bi, bo = GuardedBuffer(n, dtype).fill(x), GuardedBuffer(n, dtype)
+    assert ew.lib().ew_gather_stride(DT_CODE[dtype], bi.view.data_ptr(), bo.view.data_ptr(), n, s,
+                                     _stream()) == 0
+    rec = ew.last_launch()
+    assert rec["schedule"] == 4 and rec["path"] == 2, rec
+    torch.cuda.synchronize()
+    assert_bits_equal(bo.host(), oracle.gather_stride(x, s), dtype, False, "gather %d 2^26 %s" % (s, dtype))
+    assert bo.guards_intact() and bi.guards_intact()
