@@ -111,7 +111,10 @@ typedef enum {
 } ew_status;
 
 /* Kernel variant for the body of a call.  EW_PATH_AUTO picks the fastest
- * measured variant that the pointers' alignment allows. */
+ * measured variant that the pointers' alignment allows: 32-byte accesses once
+ * every array of the call holds at least 1 GiB (n * element size >= 2^30),
+ * 16-byte accesses below that (the measured crossover on GB300), narrower ones
+ * when the pointers share no wider alignment. */
 typedef enum {
     EW_PATH_AUTO = 0,
     EW_PATH_SCALAR = 1, /* one element per access, grid-stride */
@@ -154,11 +157,14 @@ typedef enum {
  *                     kernel specialised for that stride runs (division by
  *                     s as shifts, a conflict-free shared-memory layout, one
  *                     lap per warp; the launch record shows EW_PATH_V128).
- * EW_SCHED_AUTO       for the gather: EW_SCHED_LAPS for s < 8, EW_SCHED_TILED
- *                     for 8 <= s <= 64 (the measured crossover: from s = 8 a
+ * EW_SCHED_AUTO       for the gather: EW_SCHED_LAPS below the crossover,
+ *                     EW_SCHED_TILED from it up to s = 64.  The measured
+ *                     crossover is s = 8 for 4-byte elements (from s = 8 a
  *                     lap-ordered fp32 warp load spends one 32-byte sector per
- *                     lane).  For the other operators, EW_SCHED_ONESHOT.  A
- *                     gather with n > 2^32 always runs persistent. */
+ *                     lane) and s = 5 for 2-byte elements (whose lap-ordered
+ *                     loads move 2 bytes each).  For the other operators,
+ *                     EW_SCHED_ONESHOT.  A gather with n > 2^32 always runs
+ *                     persistent. */
 typedef enum {
     EW_SCHED_AUTO = 0,
     EW_SCHED_ONESHOT = 1,

@@ -58,11 +58,25 @@ bool overlaps(const void *p, const void *q, int64_t len) {
 
 // ---------------------------------------------------------------- planning
 
-int path_cap_bytes(int path, int e) {
+// AUTO's access width for the vector body: 32-byte accesses once each array
+// of the call holds at least kWideMinBytes, 16-byte accesses below.  Measured
+// on GB300 through this library with both widths interleaved launch by launch
+// on the same buffers (64 bytes in flight per thread per input either way):
+// at 2^26 elements the 16-byte kernels are 3-10% faster for every operator in
+// fp32 and bf16; at 2^28 the 32-byte fp32 add is 0.6-0.75% faster (SAXPY,
+// ReLU and copy tie) while every bf16 operator is 0.5-1.3% faster with
+// 16-byte accesses.  The 16-byte kernels use fewer registers (60 against 78
+// for the fp32 add), so four blocks rather than three fit on an SM, which
+// shortens the ramp and the tail that weigh on a launch of a few hundred
+// microseconds or less.
+constexpr int64_t kWideMinBytes = int64_t(1) << 30;
+
+int path_cap_bytes(int path, int e, int64_t n) {
     switch (path) {
         case EW_PATH_SCALAR: return e;
         case EW_PATH_V128: return 16;
-        default: return 32;  // AUTO, V256, TMA
+        case EW_PATH_AUTO: return n >= kWideMinBytes / e ? 32 : 16;
+        default: return 32;  // V256, TMA
     }
 }
 
@@ -70,7 +84,7 @@ int path_cap_bytes(int path, int e) {
 // the head brings that common offset to zero.
 ew_plan make_plan(int path, int e, const uintptr_t *p, int np, int64_t n) {
     int vb = e;
-    for (int w = path_cap_bytes(path, e); w > e; w >>= 1) {
+    for (int w = path_cap_bytes(path, e, n); w > e; w >>= 1) {
         bool same = true;
         for (int k = 1; k < np; ++k) same = same && (p[k] % w == p[0] % w);
         if (same) { vb = w; break; }
@@ -87,10 +101,7 @@ ew_plan make_plan(int path, int e, const uintptr_t *p, int np, int64_t n) {
     return pl;
 }
 
-int resolved_path() {
-    const int p = g_path.load(std::memory_order_relaxed);
-    return p == EW_PATH_AUTO ? EW_PATH_V256 : p;
-}
+int selected_path() { return g_path.load(std::memory_order_relaxed); }
 // schedule of the streaming kernels (lap order exists for the gather only)
 int resolved_schedule() {
     const int s = g_schedule.load(std::memory_order_relaxed);
@@ -346,7 +357,7 @@ ew_status run_stream(int op, ew_dtype dt, const void *in0, const void *in1, void
     const int np = (in1 != nullptr) ? 3 : 2;
     uintptr_t up[3];
     for (int k = 0; k < np; ++k) up[k] = reinterpret_cast<uintptr_t>(ptrs[k]);
-    const int path = resolved_path();
+    const int path = selected_path();
     const ew_plan pl = make_plan(path, e, up, np, n);
 
     if (pointer_check_enabled()) {
@@ -439,9 +450,10 @@ constexpr uint64_t kOneshotMaxN = uint64_t(1) << 32;  // the 32-bit index kernel
 // AUTO's crossover from lap order to the tiled kernel.  Lap order issues one
 // load per output: from s = 8 each fp32 lane's load is its own 32-byte sector
 // (L2-to-SM traffic bounds it), and 16-bit lanes move 2 bytes per load.  The
-// tiled kernel reads 16 bytes per load at any s; measured on GB300 it wins
-// from s = 8 for both element sizes (from s = 5 for 16-bit ones, narrowly).
-constexpr uint64_t kTiledMinStride = 8;
+// tiled kernel reads 16 bytes per load at any s.  Measured on GB300 at 2^26
+// elements it wins from s = 8 for 4-byte elements (within 1.5% at s = 5 to 7)
+// and from s = 5 for 2-byte ones (bf16 at s = 5: 5053 against 4607 GB/s).
+uint64_t tiled_min_stride(int e) { return e == 2 ? 5 : 8; }
 
 GatherArgs gather_args(const void *in, void *out, uint64_t n, uint64_t s_mod) {
     GatherArgs a{};
@@ -462,7 +474,7 @@ void set_lap_geometry(GatherArgs *a, uint64_t n, uint64_t s_mod) {
 
 // Which gather kernel runs, from the path and schedule selections:
 //   span     EW_PATH_V256 chosen explicitly: 4-byte elements, s = 2 or 4;
-//   tiled    EW_SCHED_TILED, or AUTO from s = kTiledMinStride, for s <= 64;
+//   tiled    EW_SCHED_TILED, or AUTO from s = tiled_min_stride(e), for s <= 64;
 //   laps     AUTO below that, or EW_SCHED_LAPS, once every lap holds a block;
 //   oneshot  index order, one block per chunk (n <= 2^32);
 //   stride   index order, grid-stride (EW_SCHED_PERSISTENT, or n > 2^32).
@@ -473,7 +485,7 @@ GatherKind choose_gather(int e, uint64_t n, uint64_t s_mod) {
     if (path == EW_PATH_V256 && e == 4 && (s_mod == 2 || s_mod == 4) && small_n) return GatherKind::SPAN;
     if (sched == EW_SCHED_PERSISTENT || !small_n) return GatherKind::STRIDE;
     const bool small_stride = s_mod >= 2 && s_mod <= kMaxLaps;
-    const bool tiled = sched == EW_SCHED_TILED || (sched == EW_SCHED_AUTO && s_mod >= kTiledMinStride);
+    const bool tiled = sched == EW_SCHED_TILED || (sched == EW_SCHED_AUTO && s_mod >= tiled_min_stride(e));
     if (small_stride && tiled) return GatherKind::TILED;
     const GatherEntry *laps = e == 4 ? gather_laps_4() : gather_laps_2();
     const uint64_t lap_block = static_cast<uint64_t>(kBlock) * laps->unroll;
@@ -761,7 +773,7 @@ ew_status ew_plan_query(ew_dtype dt, const void *const *ptrs, int32_t nptrs, int
     uintptr_t up[4];
     for (int k = 0; k < nptrs; ++k) up[k] = reinterpret_cast<uintptr_t>(ptrs[k]);
     const int e = elem_size(dt);
-    const int path = resolved_path();
+    const int path = selected_path();
     ew_plan pl = make_plan(path, e, up, nptrs, n);
     if ((path == EW_PATH_TMA || auto_realign(e, pl, n)) && tma_grid_fits(n, e)) {
         TmaPlan tp;

@@ -274,12 +274,13 @@ def _gather_laps(n, s):
 
 
 def _gather_auto_schedule(n, s, dtype):
-    """The schedule AUTO picks: tiled from s = 8 up to 64, lap order below it
-    where every lap holds a block, else index order."""
+    """The schedule AUTO picks: tiled from s = 8 (4-byte elements) or s = 5
+    (2-byte elements) up to 64, lap order below it where every lap holds a
+    block, else index order."""
     sm = s % n
     if n > 1 << 32:
         return 2
-    if 8 <= sm <= 64:
+    if (5 if ESIZE[dtype] == 2 else 8) <= sm <= 64:
         return 4
     return 3 if _gather_laps(n, s) else 1
 
@@ -529,9 +530,9 @@ def test_launch_record_and_grid():
     ew.ew_add(a, b, torch.empty_like(a))
     rec = ew.last_launch()
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert rec["launches"] == 1 and rec["vec_bytes"] == 32 and rec["path"] == 3
+    assert rec["launches"] == 1 and rec["vec_bytes"] == 16 and rec["path"] == 2  # 16 MiB arrays
     assert 1 <= rec["grid"] <= sms * (2048 // rec["block"])
-    assert rec["nvec"] == n // 8 and rec["head"] == 0 and rec["tail"] == 0
+    assert rec["nvec"] == n // 4 and rec["head"] == 0 and rec["tail"] == 0
     torch.cuda.synchronize()
 
 
@@ -639,7 +640,8 @@ def test_config_saxpy_f32_32M_in_place():
 def test_config_add_16bit_2p28(dtype, offset):
     rec = _full("add", dtype, 1 << 28, inputs.seed_for("add_16"), inputs.seed_for("add_16", 1),
                 offset=offset, dist="normal")
-    assert rec["head"] == (15 if offset else 0)
+    assert rec["vec_bytes"] == 16  # 512 MiB arrays: 16-byte accesses
+    assert rec["head"] == (7 if offset else 0)
 
 
 def test_bf16_add_2p28_pointers_of_different_parity():
@@ -800,14 +802,15 @@ def test_gather_tiled(dtype):
 
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16", "i32"])
 def test_gather_auto_crossover(dtype):
-    """AUTO's choice around its crossovers: lap order below s = 8, the tiled
-    kernel from 8 to 64 (wide tiles store lap by lap, narrow ones side by
-    side), index order from 65; each against the oracle."""
+    """AUTO's choice around its crossovers: lap order below s = 8 (4-byte
+    elements) or s = 5 (2-byte elements), the tiled kernel from there to 64
+    (wide tiles store lap by lap, narrow ones side by side; powers of two take
+    the specialised kernel), index order from 65; each against the oracle."""
     L = ew.lib()
     ew.set_schedule("auto")
     n = 300_007
     x = inputs.random_bits(n, "f32" if dtype == "i32" else dtype, 7300 + len(dtype))
-    for s in (6, 7, 8, 9, 16, 24, 32, 48, 64, 65):
+    for s in (4, 5, 6, 7, 8, 9, 16, 24, 32, 48, 64, 65):
         bi = GuardedBuffer(n, dtype, 0).fill(x)
         bo = GuardedBuffer(n, dtype, 2)
         assert L.ew_gather_stride(DT_CODE[dtype], bi.view.data_ptr(), bo.view.data_ptr(), n, s, _stream()) == 0

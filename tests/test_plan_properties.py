@@ -14,12 +14,22 @@ pytestmark = pytest.mark.skipif(not os.path.exists(ew.LIB_PATH), reason="libew.s
 
 BASE = 0x7f0000000000  # fake, 4 KiB aligned; never dereferenced
 ESIZE = {0: 4, 1: 2, 2: 2}
-CAP = {"scalar": None, "v128": 16, "v256": 32, "auto": 32, "tma": 32}
+CAP = {"scalar": None, "v128": 16, "v256": 32, "tma": 32}
+
+
+def _cap(path, e, n):
+    """Widest access a path may use: AUTO takes 32 bytes from 1 GiB per array."""
+    if path == "auto":
+        return 32 if n * e >= 1 << 30 else 16
+    return CAP[path] or e
 
 
 def _property(test):
     if given is None:
-        return pytest.mark.skip(reason="hypothesis is not installed")(lambda: None)
+        @pytest.mark.skip(reason="hypothesis is not installed")
+        def skipped():
+            pass
+        return skipped
     return settings(max_examples=400, deadline=None)(given(
         dt=st.sampled_from([0, 1, 2]),
         n=st.one_of(st.integers(0, 100), st.integers(0, 1 << 40)),
@@ -45,7 +55,7 @@ def test_plan_partitions_and_aligns(dt, n, offsets, path):
                                  and len({q % 4 for q in ptrs}) > 1)
     else:
         per = vb // e
-        cap = CAP[path] or e
+        cap = _cap(path, e, n)
         assert e <= vb <= cap and (vb & (vb - 1)) == 0
     assert p["head"] + p["nvec"] * per + p["tail"] == n
     assert p["head"] >= 0 and p["tail"] >= 0 and p["nvec"] >= 0
@@ -63,6 +73,6 @@ def test_plan_partitions_and_aligns(dt, n, offsets, path):
                 assert (q + p["head"] * e) % align == 0
             assert p["tail"] < per
     # the width is the widest the pointers share
-    if p["path"] != 4 and vb < (CAP[path] or e):
+    if p["path"] != 4 and vb < _cap(path, e, n):
         w = vb * 2
         assert len({q % w for q in ptrs}) > 1
