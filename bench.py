@@ -47,7 +47,7 @@ beside it and the reference arm; nothing on the timed path calls it.
 ``--impl reference`` times the CPU oracle instead (the reference arm), on a
 bounded sample of the same workload per step.
 ``--ab widths`` times 16-byte against 32-byte accesses (add, SAXPY, ReLU, copy
-in fp32 and bf16 at 2^26 and 2^28), interleaved launch by launch.
+in fp32 and bf16 at 2^25 to 2^28), in alternating blocks of 50 launches.
 Multi-GPU (torchrun): every rank runs its own 2^28-element slice of a
 world x 2^28 problem (weak scaling, no collective on the data path).
 """
@@ -121,6 +121,7 @@ PROFILE_CASES = {
     "add_bf16_mixed": ("add", "bf16", (1, 0, 3)),
     "gather16_f32": ("gather16", "f32", 0),
     "gather16_bf16": ("gather16", "bf16", 0),
+    "gather2_bf16": ("gather", "bf16", 0),
     "saxpy_relu_f32": ("saxpy_relu", "f32", 0),
 }
 
@@ -968,9 +969,12 @@ class Aux:
 # ---------------------------------------------------------------- access-width A/B
 
 def run_ab_widths(args):
-    """16-byte against 32-byte accesses, launch by launch interleaved on the
-    same buffers: add, SAXPY, ReLU, copy in fp32 and bf16 at 2^26 and 2^28.
-    Prints one JSON line per case with the median and minimum per launch."""
+    """16-byte against 32-byte accesses: add, SAXPY, ReLU, copy in fp32 and
+    bf16 at 2^25 to 2^28.  Each width runs in blocks of 50 launches of the
+    same kernel (the way a caller repeats one operation), the blocks of the
+    two widths alternating 4 times on the same buffers; the first 5 launches
+    of every block are not counted.  Prints one JSON line per case with the
+    median and minimum per launch."""
     import torch
 
     import memory_bound_elementwise_gb300 as ew
@@ -980,11 +984,10 @@ def run_ab_widths(args):
     s = stream.cuda_stream
     L = ew.lib()
     parity = Parity(not args.no_cpu)
-    rows = []
-    reps = 200
+    block, blocks, skip = 50, 4, 5
     for dtype in ("f32", "bf16"):
         code = DT_CODE[dtype]
-        for lg in (26, 28):
+        for lg in (25, 26, 27, 28):
             n = 1 << lg
             a = inputs.as_dtype(inputs.normal(n, inputs.seed_for("add_f32")), dtype)
             b = inputs.as_dtype(inputs.normal(n, inputs.seed_for("add_f32", 1)), dtype)
@@ -1001,27 +1004,28 @@ def run_ab_widths(args):
                 if op == "saxpy":
                     C.fill(b)  # y = C: in place; values drift over the launches (timing only)
                 per = {"v128": [], "v256": []}
-                for _ in range(3):
+                for _ in range(blocks):
                     for path in ("v128", "v256"):
                         ew.set_path(path)
-                        call()
-                torch.cuda.synchronize()
-                for _ in range(reps):
-                    for path in ("v128", "v256"):
-                        ew.set_path(path)
-                        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                        e0.record(stream)
-                        st = call()
-                        e1.record(stream)
-                        if st != 0:
-                            raise ew.EwError(st, op)
-                        per[path].append((e0, e1))
-                torch.cuda.synchronize()
+                        evs = []
+                        for k in range(block):
+                            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                            e0.record(stream)
+                            st = call()
+                            e1.record(stream)
+                            if st != 0:
+                                raise ew.EwError(st, op)
+                            if k >= skip:
+                                evs.append((e0, e1))
+                        torch.cuda.synchronize()
+                        per[path] += [e0.elapsed_time(e1) / 1e3 for e0, e1 in evs]
                 nbytes = metrics.algorithmic_bytes(op, dtype, n)
-                row = {"ab": "widths", "op": op, "dtype": dtype, "n": n, "launches_each": reps}
+                row = {"ab": "widths", "op": op, "dtype": dtype, "n": n,
+                       "launches_each": blocks * (block - skip), "blocks": blocks}
                 for path in ("v128", "v256"):
-                    t = sorted(e0.elapsed_time(e1) / 1e3 for e0, e1 in per[path])
+                    t = sorted(per[path])
                     row[path] = {"median_us": t[len(t) // 2] * 1e6, "min_us": t[0] * 1e6,
+                                 "mean_us": sum(t) / len(t) * 1e6,
                                  "gbps_median": metrics.gbps(nbytes, t[len(t) // 2])}
                     ew.set_path(path)
                     if want is not None:
@@ -1035,7 +1039,6 @@ def run_ab_widths(args):
                                                       lambda lo, hi: orc.saxpy(dtype, 2.5, a[lo:hi], b[lo:hi]), n))
                 ew.set_path("auto")
                 row["v256_over_v128"] = row["v128"]["median_us"] / row["v256"]["median_us"]
-                rows.append(row)
                 print(json.dumps(row), flush=True)
             del A, B, C
 

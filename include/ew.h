@@ -111,10 +111,8 @@ typedef enum {
 } ew_status;
 
 /* Kernel variant for the body of a call.  EW_PATH_AUTO picks the fastest
- * measured variant that the pointers' alignment allows: 32-byte accesses once
- * every array of the call holds at least 1 GiB (n * element size >= 2^30),
- * 16-byte accesses below that (the measured crossover on GB300), narrower ones
- * when the pointers share no wider alignment. */
+ * measured variant that the pointers' alignment allows: the widest access
+ * width all the pointers share, up to 32 bytes. */
 typedef enum {
     EW_PATH_AUTO = 0,
     EW_PATH_SCALAR = 1, /* one element per access, grid-stride */
@@ -153,16 +151,19 @@ typedef enum {
  *                     all s laps draw from (32 KiB) once, coalesced, into
  *                     shared memory with one row per residue mod s, then
  *                     writes each lap's outputs as one coalesced run.  For
- *                     s = 8, 16, 32 or 64 and an input aligned to 16 bytes a
+ *                     s = 2, 4, ..., 64 and an input aligned to 16 bytes a
  *                     kernel specialised for that stride runs (division by
- *                     s as shifts, a conflict-free shared-memory layout, one
- *                     lap per warp; the launch record shows EW_PATH_V128).
+ *                     s as shifts, a conflict-free shared-memory layout, warps
+ *                     copying whole lap runs; the launch record shows
+ *                     EW_PATH_V128).
  * EW_SCHED_AUTO       for the gather: EW_SCHED_LAPS below the crossover,
  *                     EW_SCHED_TILED from it up to s = 64.  The measured
  *                     crossover is s = 8 for 4-byte elements (from s = 8 a
  *                     lap-ordered fp32 warp load spends one 32-byte sector per
  *                     lane) and s = 5 for 2-byte elements (whose lap-ordered
- *                     loads move 2 bytes each).  For the other operators,
+ *                     loads move 2 bytes each); 2-byte elements at s = 2 and
+ *                     4 on an input aligned to 16 bytes also take
+ *                     EW_SCHED_TILED.  For the other operators,
  *                     EW_SCHED_ONESHOT.  A gather with n > 2^32 always runs
  *                     persistent. */
 typedef enum {

@@ -58,25 +58,20 @@ bool overlaps(const void *p, const void *q, int64_t len) {
 
 // ---------------------------------------------------------------- planning
 
-// AUTO's access width for the vector body: 32-byte accesses once each array
-// of the call holds at least kWideMinBytes, 16-byte accesses below.  Measured
-// on GB300 through this library with both widths interleaved launch by launch
-// on the same buffers (64 bytes in flight per thread per input either way):
-// at 2^26 elements the 16-byte kernels are 3-10% faster for every operator in
-// fp32 and bf16; at 2^28 the 32-byte fp32 add is 0.6-0.75% faster (SAXPY,
-// ReLU and copy tie) while every bf16 operator is 0.5-1.3% faster with
-// 16-byte accesses.  The 16-byte kernels use fewer registers (60 against 78
-// for the fp32 add), so four blocks rather than three fit on an SM, which
-// shortens the ramp and the tail that weigh on a launch of a few hundred
-// microseconds or less.
-constexpr int64_t kWideMinBytes = int64_t(1) << 30;
-
-int path_cap_bytes(int path, int e, int64_t n) {
+// AUTO's access width for the vector body is 32 bytes (the widest the
+// pointers share).  Measured on GB300 through this library in alternating
+// blocks of 50 launches of one width (2^25 to 2^28 elements; add, SAXPY,
+// ReLU, copy in fp32 and bf16), 16- and 32-byte accesses with 64 bytes in
+// flight per thread per input tie within 0.6% in most cases; the 32-byte
+// kernels are 0.2-0.6% ahead for the fp32 add and SAXPY from 2^26, the
+// 16-byte ones 1.5-2% ahead for bf16 ReLU and copy at 2^26-2^27.  The 32-byte
+// kernels issue half as many memory instructions and keep the three-operand
+// fp32 operators ahead, so AUTO keeps them.
+int path_cap_bytes(int path, int e) {
     switch (path) {
         case EW_PATH_SCALAR: return e;
         case EW_PATH_V128: return 16;
-        case EW_PATH_AUTO: return n >= kWideMinBytes / e ? 32 : 16;
-        default: return 32;  // V256, TMA
+        default: return 32;  // AUTO, V256, TMA
     }
 }
 
@@ -84,7 +79,7 @@ int path_cap_bytes(int path, int e, int64_t n) {
 // the head brings that common offset to zero.
 ew_plan make_plan(int path, int e, const uintptr_t *p, int np, int64_t n) {
     int vb = e;
-    for (int w = path_cap_bytes(path, e, n); w > e; w >>= 1) {
+    for (int w = path_cap_bytes(path, e); w > e; w >>= 1) {
         bool same = true;
         for (int k = 1; k < np; ++k) same = same && (p[k] % w == p[0] % w);
         if (same) { vb = w; break; }
@@ -447,13 +442,19 @@ enum class GatherKind { SPAN, TILED, LAPS, ONESHOT, STRIDE };
 
 constexpr uint64_t kOneshotMaxN = uint64_t(1) << 32;  // the 32-bit index kernels
 
-// AUTO's crossover from lap order to the tiled kernel.  Lap order issues one
+// AUTO's crossover from lap order to the tiled kernels.  Lap order issues one
 // load per output: from s = 8 each fp32 lane's load is its own 32-byte sector
 // (L2-to-SM traffic bounds it), and 16-bit lanes move 2 bytes per load.  The
-// tiled kernel reads 16 bytes per load at any s.  Measured on GB300 at 2^26
-// elements it wins from s = 8 for 4-byte elements (within 1.5% at s = 5 to 7)
-// and from s = 5 for 2-byte ones (bf16 at s = 5: 5053 against 4607 GB/s).
-uint64_t tiled_min_stride(int e) { return e == 2 ? 5 : 8; }
+// tiled kernels read 16 bytes per load at any s.  Measured on GB300 at 2^26
+// elements they win from s = 8 for 4-byte elements (within 1.5% at s = 5 to
+// 7; lap order is 4% ahead at s = 2 and 4) and from s = 5 for 2-byte ones
+// (bf16 at s = 5: 5053 against 4607 GB/s).  For 2-byte elements at s = 2 and
+// 4 on a 16-byte aligned input the kernel specialised for the stride wins too
+// (bf16: 5971 against 5472 at s = 2, 5975 against 5253 at s = 4).
+bool auto_tiled(int e, uint64_t s_mod, bool in_aligned16) {
+    if (e == 2 && in_aligned16 && (s_mod == 2 || s_mod == 4)) return true;
+    return s_mod >= (e == 2 ? 5u : 8u);
+}
 
 GatherArgs gather_args(const void *in, void *out, uint64_t n, uint64_t s_mod) {
     GatherArgs a{};
@@ -474,18 +475,18 @@ void set_lap_geometry(GatherArgs *a, uint64_t n, uint64_t s_mod) {
 
 // Which gather kernel runs, from the path and schedule selections:
 //   span     EW_PATH_V256 chosen explicitly: 4-byte elements, s = 2 or 4;
-//   tiled    EW_SCHED_TILED, or AUTO from s = tiled_min_stride(e), for s <= 64;
+//   tiled    EW_SCHED_TILED, or AUTO where auto_tiled() says so, for s <= 64;
 //   laps     AUTO below that, or EW_SCHED_LAPS, once every lap holds a block;
 //   oneshot  index order, one block per chunk (n <= 2^32);
 //   stride   index order, grid-stride (EW_SCHED_PERSISTENT, or n > 2^32).
-GatherKind choose_gather(int e, uint64_t n, uint64_t s_mod) {
+GatherKind choose_gather(int e, uint64_t n, uint64_t s_mod, bool in_aligned16) {
     const int path = g_path.load(std::memory_order_relaxed);
     const int sched = g_schedule.load(std::memory_order_relaxed);
     const bool small_n = n <= kOneshotMaxN;
     if (path == EW_PATH_V256 && e == 4 && (s_mod == 2 || s_mod == 4) && small_n) return GatherKind::SPAN;
     if (sched == EW_SCHED_PERSISTENT || !small_n) return GatherKind::STRIDE;
     const bool small_stride = s_mod >= 2 && s_mod <= kMaxLaps;
-    const bool tiled = sched == EW_SCHED_TILED || (sched == EW_SCHED_AUTO && s_mod >= tiled_min_stride(e));
+    const bool tiled = sched == EW_SCHED_TILED || (sched == EW_SCHED_AUTO && auto_tiled(e, s_mod, in_aligned16));
     if (small_stride && tiled) return GatherKind::TILED;
     const GatherEntry *laps = e == 4 ? gather_laps_4() : gather_laps_2();
     const uint64_t lap_block = static_cast<uint64_t>(kBlock) * laps->unroll;
@@ -707,7 +708,7 @@ ew_status ew_gather_stride(ew_dtype dt, const void *in, void *out, int64_t n, in
     const uint64_t un = static_cast<uint64_t>(n);
     const uint64_t s_mod = static_cast<uint64_t>(stride) % un;
     GatherLaunch gl;
-    switch (choose_gather(e, un, s_mod)) {
+    switch (choose_gather(e, un, s_mod, reinterpret_cast<uintptr_t>(in) % 16 == 0)) {
         case GatherKind::SPAN: gl = plan_gather_span(in, out, un, s_mod); break;
         case GatherKind::TILED: gl = plan_gather_tiled(e, in, out, un, s_mod); break;
         case GatherKind::LAPS: gl = plan_gather_laps(e, in, out, un, s_mod); break;

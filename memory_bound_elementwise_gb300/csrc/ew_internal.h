@@ -117,7 +117,7 @@ const GatherEntry *gather_laps_2();
 constexpr uint32_t kTiledSpanBytes = 32768;
 const GatherEntry *gather_tiled_4();
 const GatherEntry *gather_tiled_2();
-// Tiled gather specialised for a power-of-two stride (8, 16, 32 or 64) and an
+// Tiled gather specialised for a power-of-two stride (2, 4, ..., 64) and an
 // input aligned to 16 bytes; nullptr for other strides.  Each block of
 // kTiledPow2Threads threads stages kTiledPow2SpanBytes of input.
 constexpr int kTiledPow2SpanBytes = 16384;

@@ -317,21 +317,26 @@ __global__ void __launch_bounds__(kBlock) gather_tiled_kernel(const GatherArgs g
     }
 }
 
-// Tiled gather for a power-of-two stride S (8 <= S <= 64) known at compile
+// Tiled gather for a power-of-two stride S (2 <= S <= 64) known at compile
 // time, and an input aligned to 16 bytes.  Same schedule as the tiled kernel
 // above: block b owns positions [b*P, (b+1)*P) of every lap and stages the
-// 32 KiB input span they draw from.  With S a compile-time power of two every
+// input span they draw from.  With S a compile-time power of two every
 // division by S is a shift, and a thread's 16-byte loads all land in the
-// same rows: thread t's load i holds the span elements j = V*t + V*kBlock*i
-// (V elements per load), i.e. rows (V*t) mod S onwards and column
-// (V*t) / S + i*V*kBlock/S, so its shared-memory stores use one base address
-// and compile-time offsets.  The rows are padded (and, from row 32 on,
-// shifted) so that the 32 lanes of a warp storing element k of their loads
-// hit 32 different banks; the layout is found at compile time.  Each warp
-// then writes whole laps: lane l stores positions l, l + 32, ... of its lap's
-// run from one row, 4-byte words where the run allows (pairs of 16-bit
-// elements), in a fully unrolled loop.  The last block, whose span is cut
-// short by n, stages and stores element by element with bounds checks.
+// same rows: thread t's load i holds the span elements j = V*t + V*T*i
+// (V elements per load, T threads), i.e. rows (V*t) mod S onwards and column
+// (V*t) / S + i*V*T/S, so its shared-memory stores use one base address and
+// compile-time offsets.  When S >= V each element of a load goes to its own
+// row; the rows are padded (and, from row 32 on, shifted) so that the 32
+// lanes of a warp storing element k of their loads hit 32 different banks,
+// with the layout found at compile time.  When S < V a load holds V/S
+// consecutive columns of every row, which the thread packs and stores as one
+// 4- or 8-byte access per row (lanes then write consecutive words).  The
+// store phase splits the S lap runs of the block among its warps (a warp per
+// lap, or several per lap when S is below the warp count): lane l copies
+// positions l, l + 32, ... of its share of a run from one row, 4-byte words
+// where the run allows (pairs of 16-bit elements), in a fully unrolled loop.
+// The last block, whose span is cut short by n, stages and stores element by
+// element with bounds checks.
 struct TiledLayout {
     uint32_t pad;  // elements added to every row
     uint32_t x;    // elements added per 32 rows
@@ -340,11 +345,13 @@ struct TiledLayout {
 template <int E, int S, int kSpanBytes>
 constexpr TiledLayout tiled_pow2_layout() {
     constexpr uint32_t kPerVec = 16 / E, kP = (kSpanBytes / E) / S, kStep = E == 2 ? 2 : 1;
-    for (uint32_t pad = 0; pad < 32; pad += kStep) {
+    // S < kPerVec: packed row stores, lanes on consecutive words, no padding needed
+    constexpr uint32_t kPadEnd = S < static_cast<int>(kPerVec) ? kStep : 32;
+    for (uint32_t pad = 0; pad < kPadEnd; pad += kStep) {
         for (uint32_t x = 0; x < 64; x += kStep) {
             uint32_t banks = 0, words[32] = {};
             bool ok = true;
-            for (uint32_t t = 0; t < 32 && ok; ++t) {
+            for (uint32_t t = 0; t < 32 && ok && S >= static_cast<int>(kPerVec); ++t) {
                 const uint32_t j = kPerVec * t, row = j % S, col = j / S;
                 const uint32_t word = ((row * (kP + pad) + x * (row >> 5) + col) * E) / 4;
                 bool same_word = false;  // two halves of one word: one access
@@ -360,15 +367,17 @@ constexpr TiledLayout tiled_pow2_layout() {
     return TiledLayout{~0u, 0};
 }
 
+constexpr uint32_t log2_pow2(uint32_t v) { return v <= 1 ? 0 : 1 + log2_pow2(v >> 1); }
+
 // Geometry of the power-of-two tiled gather: element size E, stride S, input
 // span per block, threads per block.
 template <int E, int S, int kSpanBytes = kTiledPow2SpanBytes, int kThreads = kTiledPow2Threads>
 struct TiledPow2 {
-    static_assert(S >= 8 && S <= 64 && (S & (S - 1)) == 0, "power-of-two stride from 8 to 64");
+    static_assert(S >= 2 && S <= 64 && (S & (S - 1)) == 0, "power-of-two stride from 2 to 64");
     static constexpr uint32_t kPerVec = 16 / E;                    // elements per 16-byte load
     static constexpr uint32_t kSpan = kSpanBytes / E;              // input elements per block
     static constexpr uint32_t kP = kSpan / S;                      // positions per lap per block
-    static constexpr uint32_t kLog2S = S == 8 ? 3 : S == 16 ? 4 : S == 32 ? 5 : 6;
+    static constexpr uint32_t kLog2S = log2_pow2(S);
     static constexpr uint32_t kLoads = kSpan / kPerVec / kThreads;  // 16-byte loads per thread
     static constexpr uint32_t kColStep = kThreads * kPerVec / S;    // columns between a thread's loads
     static constexpr uint32_t kPad = tiled_pow2_layout<E, S, kSpanBytes>().pad;
@@ -376,12 +385,24 @@ struct TiledPow2 {
     static constexpr uint32_t kPitch = kP + kPad;
     static constexpr uint32_t kElems = S * kPitch + kX * ((S - 1) >> 5);
     static constexpr int kSmemBytes = static_cast<int>((kElems * E + 15) / 16 * 16);
+    static constexpr uint32_t kWarps = kThreads / 32;
+    static constexpr uint32_t kWarpsPerLap = S >= static_cast<int>(kWarps) ? 1 : kWarps / S;
+    static constexpr uint32_t kSeg = kP / kWarpsPerLap;            // positions of a run per warp
     static_assert(kPad != ~0u, "no bank-conflict-free row layout");
     static_assert(kLoads >= 1 && kLoads * kThreads * kPerVec == kSpan, "whole 16-byte loads per thread");
-    static_assert(kP % 32 == 0 && kThreads >= S, "whole warps per lap run; one thread per lap");
+    static_assert(kThreads >= S, "one thread per lap computes its geometry");
+    static_assert(kSeg % (E == 2 ? 64 : 32) == 0, "whole warp-wide words per run share");
     static_assert(E == 4 || (kPitch % 2 == 0 && kX % 2 == 0), "16-bit rows must start on whole words");
+    static_assert(S >= static_cast<int>(kPerVec) || (kPitch * E) % 8 == 0, "packed rows start on 8 bytes");
     __host__ __device__ static constexpr uint32_t row_offset(uint32_t r) { return r * kPitch + kX * (r >> 5); }
 };
+
+// The element of row r that a 16-byte load v holds at column slot c (S < V):
+// element k = c*S + r of the load.
+template <int E, int S>
+__device__ __forceinline__ uint32_t load_elem(const Vec<16> &v, uint32_t k) {
+    return E == 4 ? v.w[k] : (v.w[k >> 1] >> (16u * (k & 1u))) & 0xffffu;
+}
 
 template <int E, int S, int kSpanBytes, int kThreads>
 __global__ void __launch_bounds__(kThreads) gather_tiled_pow2_kernel(const GatherArgs g) {
@@ -409,13 +430,35 @@ __global__ void __launch_bounds__(kThreads) gather_tiled_pow2_kernel(const Gathe
 #pragma unroll
         for (uint32_t i = 0; i < T::kLoads; ++i) v[i] = ld<16>(src_bytes + (threadIdx.x + i * kThreads) * 16u);
         const uint32_t j = T::kPerVec * threadIdx.x;
-        W *dst = tile + T::row_offset(j & (S - 1)) + (j >> T::kLog2S);
+        if constexpr (S >= static_cast<int>(T::kPerVec)) {  // element k to row (j mod S) + k
+            W *dst = tile + T::row_offset(j & (S - 1)) + (j >> T::kLog2S);
 #pragma unroll
-        for (uint32_t i = 0; i < T::kLoads; ++i) {
+            for (uint32_t i = 0; i < T::kLoads; ++i) {
 #pragma unroll
-            for (uint32_t k = 0; k < T::kPerVec; ++k) {
-                const uint32_t w = v[i].w[k * E / 4];
-                dst[k * T::kPitch + i * T::kColStep] = static_cast<W>(E == 4 ? w : w >> (16u * (k & 1u)));
+                for (uint32_t k = 0; k < T::kPerVec; ++k) {
+                    const uint32_t w = v[i].w[k * E / 4];
+                    dst[k * T::kPitch + i * T::kColStep] = static_cast<W>(E == 4 ? w : w >> (16u * (k & 1u)));
+                }
+            }
+        } else {  // j mod S = 0: element k to row k mod S, column j/S + k/S; V/S columns per row
+            constexpr uint32_t kPerRow = T::kPerVec / S;  // 2 or 4 elements: 4 or 8 bytes
+            W *dst = tile + (j >> T::kLog2S);
+#pragma unroll
+            for (uint32_t i = 0; i < T::kLoads; ++i) {
+#pragma unroll
+                for (uint32_t r = 0; r < static_cast<uint32_t>(S); ++r) {
+                    W *at = dst + T::row_offset(r) + i * T::kColStep;
+                    uint32_t e[kPerRow];
+#pragma unroll
+                    for (uint32_t c = 0; c < kPerRow; ++c) e[c] = load_elem<E, S>(v[i], c * S + r);
+                    if constexpr (E == 4) {
+                        *reinterpret_cast<uint2 *>(at) = make_uint2(e[0], e[1]);
+                    } else if constexpr (kPerRow == 2) {
+                        *reinterpret_cast<uint32_t *>(at) = e[0] | (e[1] << 16);
+                    } else {
+                        *reinterpret_cast<uint2 *>(at) = make_uint2(e[0] | (e[1] << 16), e[2] | (e[3] << 16));
+                    }
+                }
             }
         }
     } else {
@@ -425,22 +468,25 @@ __global__ void __launch_bounds__(kThreads) gather_tiled_pow2_kernel(const Gathe
     }
     __syncthreads();
     const uint32_t lane = threadIdx.x & 31u;
-    for (uint32_t L = threadIdx.x >> 5; L < S; L += kThreads / 32) {  // one lap per warp at a time
-        const W *row = tile + lap_row[L];
-        W *dst = out + (static_cast<size_t>(lap_start[L]) + p0);
+    // work item = (lap, share of its run); one per warp at a time
+    for (uint32_t item = threadIdx.x >> 5; item < S * T::kWarpsPerLap; item += T::kWarps) {
+        const uint32_t L = item / T::kWarpsPerLap, q0 = (item % T::kWarpsPerLap) * T::kSeg;
+        const W *row = tile + lap_row[L] + q0;
+        W *dst = out + (static_cast<size_t>(lap_start[L]) + p0 + q0);
         if (full) {  // the whole run [0, P) of every lap lies before n
             if (E == 4 || (reinterpret_cast<uintptr_t>(dst) & 3u) == 0) {
                 const uint32_t *row_w = reinterpret_cast<const uint32_t *>(row);
                 uint32_t *dst_w = reinterpret_cast<uint32_t *>(dst);
 #pragma unroll
-                for (uint32_t i = 0; i < T::kP * E / 4 / 32; ++i) dst_w[lane + 32 * i] = row_w[lane + 32 * i];
+                for (uint32_t i = 0; i < T::kSeg * E / 4 / 32; ++i) dst_w[lane + 32 * i] = row_w[lane + 32 * i];
             } else {
 #pragma unroll 8
-                for (uint32_t i = 0; i < T::kP / 32; ++i) dst[lane + 32 * i] = row[lane + 32 * i];
+                for (uint32_t i = 0; i < T::kSeg / 32; ++i) dst[lane + 32 * i] = row[lane + 32 * i];
             }
         } else {
             const uint32_t len = lap_len[L] > p0 ? min(lap_len[L] - p0, T::kP) : 0u;
-            for (uint32_t q = lane; q < len; q += 32) dst[q] = row[q];
+            const uint32_t end = len > q0 ? min(len - q0, T::kSeg) : 0u;
+            for (uint32_t q = lane; q < end; q += 32) dst[q] = row[q];
         }
     }
 }

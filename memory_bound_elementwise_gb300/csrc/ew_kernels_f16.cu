@@ -43,15 +43,18 @@ const GatherEntry *gather_oneshot_2() { return &kGatherOneshot; }
 const GatherEntry *gather_laps_2() { return &kGatherLaps; }
 const GatherEntry *gather_tiled_2() { return &kGatherTiled; }
 
-static const GatherEntry kGatherTiledPow2[4] = {tiled_pow2_entry<2, 8>(), tiled_pow2_entry<2, 16>(),
+static const GatherEntry kGatherTiledPow2[6] = {tiled_pow2_entry<2, 2>(), tiled_pow2_entry<2, 4>(),
+                                                tiled_pow2_entry<2, 8>(), tiled_pow2_entry<2, 16>(),
                                                 tiled_pow2_entry<2, 32>(), tiled_pow2_entry<2, 64>()};
 
 const GatherEntry *gather_tiled_pow2_2(uint64_t stride) {
     switch (stride) {
-        case 8: return &kGatherTiledPow2[0];
-        case 16: return &kGatherTiledPow2[1];
-        case 32: return &kGatherTiledPow2[2];
-        case 64: return &kGatherTiledPow2[3];
+        case 2: return &kGatherTiledPow2[0];
+        case 4: return &kGatherTiledPow2[1];
+        case 8: return &kGatherTiledPow2[2];
+        case 16: return &kGatherTiledPow2[3];
+        case 32: return &kGatherTiledPow2[4];
+        case 64: return &kGatherTiledPow2[5];
         default: return nullptr;
     }
 }

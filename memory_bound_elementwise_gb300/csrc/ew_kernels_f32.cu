@@ -51,15 +51,18 @@ const GatherEntry *gather_oneshot_4() { return &kGatherOneshot; }
 const GatherEntry *gather_laps_4() { return &kGatherLaps; }
 const GatherEntry *gather_tiled_4() { return &kGatherTiled; }
 
-static const GatherEntry kGatherTiledPow2[4] = {tiled_pow2_entry<4, 8>(), tiled_pow2_entry<4, 16>(),
+static const GatherEntry kGatherTiledPow2[6] = {tiled_pow2_entry<4, 2>(), tiled_pow2_entry<4, 4>(),
+                                                tiled_pow2_entry<4, 8>(), tiled_pow2_entry<4, 16>(),
                                                 tiled_pow2_entry<4, 32>(), tiled_pow2_entry<4, 64>()};
 
 const GatherEntry *gather_tiled_pow2_4(uint64_t stride) {
     switch (stride) {
-        case 8: return &kGatherTiledPow2[0];
-        case 16: return &kGatherTiledPow2[1];
-        case 32: return &kGatherTiledPow2[2];
-        case 64: return &kGatherTiledPow2[3];
+        case 2: return &kGatherTiledPow2[0];
+        case 4: return &kGatherTiledPow2[1];
+        case 8: return &kGatherTiledPow2[2];
+        case 16: return &kGatherTiledPow2[3];
+        case 32: return &kGatherTiledPow2[4];
+        case 64: return &kGatherTiledPow2[5];
         default: return nullptr;
     }
 }

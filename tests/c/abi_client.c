@@ -35,13 +35,13 @@ static int host_mode(void) {
 
     const void *ptrs[3] = {q + 2, q + 2 + 4096, q + 2 + 8192};
     ew_plan pl;
-    EXPECT(ew_plan_query(EW_BF16, ptrs, 3, 1000, &pl) == EW_OK);  /* AUTO: 16-byte body */
-    EXPECT(pl.vec_bytes == 16 && pl.head == 7);
-    EXPECT(pl.head + pl.nvec * 8 + pl.tail == 1000);
-    EXPECT(ew_set_path(EW_PATH_V256) == EW_OK);
     EXPECT(ew_plan_query(EW_BF16, ptrs, 3, 1000, &pl) == EW_OK);
     EXPECT(pl.vec_bytes == 32 && pl.head == 15);
     EXPECT(pl.head + pl.nvec * 16 + pl.tail == 1000);
+    EXPECT(ew_set_path(EW_PATH_V128) == EW_OK);
+    EXPECT(ew_plan_query(EW_BF16, ptrs, 3, 1000, &pl) == EW_OK);
+    EXPECT(pl.vec_bytes == 16 && pl.head == 7);
+    EXPECT(pl.head + pl.nvec * 8 + pl.tail == 1000);
     EXPECT(ew_set_path(EW_PATH_AUTO) == EW_OK);
 
     ew_launch_record rec;

@@ -127,29 +127,16 @@ def plan(dt, ptrs, n, path="auto"):
         ew.set_path("auto")
 
 
-def test_plan_aligned_f32_width_follows_size():
-    # AUTO: 16-byte accesses below 1 GiB per array, 32-byte from there
+def test_plan_aligned_f32_uses_256_bit_body():
     n = (1 << 20) + 3  # the odd-tail fp32 add size
-    ptrs = [P, P + (1 << 34), P + (2 << 34)]
-    assert plan(0, ptrs, n) == {"path": 2, "vec_bytes": 16, "head": 0, "nvec": (1 << 20) // 4, "tail": 3}
-    assert plan(0, ptrs, n, "v256") == {"path": 3, "vec_bytes": 32, "head": 0, "nvec": (1 << 20) // 8,
-                                        "tail": 3}
-    for dt, e in ((0, 4), (1, 2), (2, 2)):
-        wide = (1 << 30) // e
-        assert plan(dt, ptrs, wide - 1)["vec_bytes"] == 16
-        assert plan(dt, ptrs, wide)["vec_bytes"] == 32
-    assert plan(0, ptrs, 1 << 28)["vec_bytes"] == 32  # the fp32 add at 2^28: 1 GiB per array
-    assert plan(2, ptrs, 1 << 28)["vec_bytes"] == 16  # bf16 at 2^28: 512 MiB
+    p = plan(0, [P, P + (1 << 24), P + (2 << 24)], n)
+    assert p == {"path": 3, "vec_bytes": 32, "head": 0, "nvec": (1 << 20) // 8, "tail": 3}
 
 
 def test_plan_offset_by_one_element_bf16():
     # all three pointers one bf16 element past a 256-byte boundary
     n = 1 << 28
-    p = plan(2, [P + 2, P + 2 + (1 << 30), P + 2 + (2 << 30)], n)  # 512 MiB arrays: 16-byte body
-    assert p["vec_bytes"] == 16 and p["head"] == 7
-    assert p["head"] + p["nvec"] * 8 + p["tail"] == n
-    assert p["tail"] == (n - 7) % 8
-    p = plan(2, [P + 2, P + 2 + (1 << 30), P + 2 + (2 << 30)], n, "v256")
+    p = plan(2, [P + 2, P + 2 + (1 << 30), P + 2 + (2 << 30)], n)
     assert p["vec_bytes"] == 32 and p["head"] == 15
     assert p["head"] + p["nvec"] * 16 + p["tail"] == n
     assert p["tail"] == (n - 15) % 16

@@ -273,14 +273,17 @@ def _gather_laps(n, s):
     return 2 <= sm <= 64 and n <= 1 << 32 and n // sm >= LAP_BLOCK
 
 
-def _gather_auto_schedule(n, s, dtype):
+def _gather_auto_schedule(n, s, dtype, in_aligned16=False):
     """The schedule AUTO picks: tiled from s = 8 (4-byte elements) or s = 5
-    (2-byte elements) up to 64, lap order below it where every lap holds a
+    (2-byte elements) up to 64, and for 2-byte elements at s = 2 and 4 on an
+    input aligned to 16 bytes; lap order below that where every lap holds a
     block, else index order."""
     sm = s % n
     if n > 1 << 32:
         return 2
     if (5 if ESIZE[dtype] == 2 else 8) <= sm <= 64:
+        return 4
+    if ESIZE[dtype] == 2 and in_aligned16 and sm in (2, 4):
         return 4
     return 3 if _gather_laps(n, s) else 1
 
@@ -530,9 +533,9 @@ def test_launch_record_and_grid():
     ew.ew_add(a, b, torch.empty_like(a))
     rec = ew.last_launch()
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert rec["launches"] == 1 and rec["vec_bytes"] == 16 and rec["path"] == 2  # 16 MiB arrays
+    assert rec["launches"] == 1 and rec["vec_bytes"] == 32 and rec["path"] == 3
     assert 1 <= rec["grid"] <= sms * (2048 // rec["block"])
-    assert rec["nvec"] == n // 4 and rec["head"] == 0 and rec["tail"] == 0
+    assert rec["nvec"] == n // 8 and rec["head"] == 0 and rec["tail"] == 0
     torch.cuda.synchronize()
 
 
@@ -640,8 +643,7 @@ def test_config_saxpy_f32_32M_in_place():
 def test_config_add_16bit_2p28(dtype, offset):
     rec = _full("add", dtype, 1 << 28, inputs.seed_for("add_16"), inputs.seed_for("add_16", 1),
                 offset=offset, dist="normal")
-    assert rec["vec_bytes"] == 16  # 512 MiB arrays: 16-byte accesses
-    assert rec["head"] == (7 if offset else 0)
+    assert rec["head"] == (15 if offset else 0)
 
 
 def test_bf16_add_2p28_pointers_of_different_parity():
@@ -803,19 +805,20 @@ def test_gather_tiled(dtype):
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16", "i32"])
 def test_gather_auto_crossover(dtype):
     """AUTO's choice around its crossovers: lap order below s = 8 (4-byte
-    elements) or s = 5 (2-byte elements), the tiled kernel from there to 64
-    (wide tiles store lap by lap, narrow ones side by side; powers of two take
-    the specialised kernel), index order from 65; each against the oracle."""
+    elements) or s = 5 (2-byte elements, except s = 2 and 4 on this aligned
+    input), the tiled kernel from there to 64 (wide tiles store lap by lap,
+    narrow ones side by side; powers of two take the specialised kernel),
+    index order from 65; each against the oracle."""
     L = ew.lib()
     ew.set_schedule("auto")
     n = 300_007
     x = inputs.random_bits(n, "f32" if dtype == "i32" else dtype, 7300 + len(dtype))
-    for s in (4, 5, 6, 7, 8, 9, 16, 24, 32, 48, 64, 65):
+    for s in (2, 3, 4, 5, 6, 7, 8, 9, 16, 24, 32, 48, 64, 65):
         bi = GuardedBuffer(n, dtype, 0).fill(x)
         bo = GuardedBuffer(n, dtype, 2)
         assert L.ew_gather_stride(DT_CODE[dtype], bi.view.data_ptr(), bo.view.data_ptr(), n, s, _stream()) == 0
         rec = ew.last_launch()
-        assert rec["schedule"] == _gather_auto_schedule(n, s, dtype if dtype != "i32" else "f32"), (s, rec)
+        assert rec["schedule"] == _gather_auto_schedule(n, s, dtype if dtype != "i32" else "f32", True), (s, rec)
         torch.cuda.synchronize()
         assert_bits_equal(bo.host(), oracle.gather_stride(x, s), "f32" if dtype == "i32" else dtype, False,
                           "auto gather %s s=%d" % (dtype, s))
@@ -984,8 +987,9 @@ def test_gather_span_variant(dtype):
 
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16", "i32"])
 def test_gather_tiled_pow2(dtype):
-    """The tiled gather specialised for strides 8, 16, 32 and 64 (and strides
-    congruent to them mod n), on a 16-byte aligned input: one ragged block,
+    """The tiled gather specialised for strides 2, 4, 8, 16, 32 and 64 (and
+    strides congruent to them mod n), on a 16-byte aligned input (strides 2
+    and 4 under EW_SCHED_TILED, the others under AUTO): one ragged block,
     exactly one and several full 16 KiB spans, spans plus a ragged block, n
     divisible by the stride (every lap on one residue row) and not (laps of
     unequal length on distinct rows), output offsets that start laps on odd
@@ -996,7 +1000,8 @@ def test_gather_tiled_pow2(dtype):
     e = ESIZE[dtype]
     span = 16384 // e  # input elements a block stages (16 KiB)
     bits = "f32" if dtype == "i32" else dtype
-    for s in (8, 16, 32, 64):
+    for s in (2, 4, 8, 16, 32, 64):
+        ew.set_schedule("tiled" if s < 8 else "auto")
         sizes = (s + 1, 1000, span - 1, span, span + 1, 2 * span, 3 * span + 5, (1 << 20) + 3, 1 << 20)
         for n in sizes:
             x = inputs.random_bits(n, bits, 9900 + n + s)

@@ -14,13 +14,11 @@ pytestmark = pytest.mark.skipif(not os.path.exists(ew.LIB_PATH), reason="libew.s
 
 BASE = 0x7f0000000000  # fake, 4 KiB aligned; never dereferenced
 ESIZE = {0: 4, 1: 2, 2: 2}
-CAP = {"scalar": None, "v128": 16, "v256": 32, "tma": 32}
+CAP = {"scalar": None, "v128": 16, "v256": 32, "auto": 32, "tma": 32}
 
 
 def _cap(path, e, n):
-    """Widest access a path may use: AUTO takes 32 bytes from 1 GiB per array."""
-    if path == "auto":
-        return 32 if n * e >= 1 << 30 else 16
+    """Widest access a path may use."""
     return CAP[path] or e
 
 

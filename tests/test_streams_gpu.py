@@ -41,7 +41,7 @@ def test_many_threads_many_streams():
                 for _ in range(20):  # repeated launches interleave with the other threads
                     ew.ew_add(a, b, c, stream=s)
                     rec = ew.last_launch()  # per-thread record
-                    assert rec["launches"] == 1 and rec["nvec"] == n // 4  # 16-byte vectors (4 MiB arrays)
+                    assert rec["launches"] == 1 and rec["nvec"] == n // 8
                 s.synchronize()
                 results[t] = c.cpu().numpy()
         except Exception as e:  # pragma: no cover - reported below
