@@ -227,3 +227,55 @@ def test_sectors_lookup_is_tied_to_the_kernel_sources(tmp_path, monkeypatch):
     (prof / "traffic.json").write_text(json.dumps(ent))
     got = bench.profiled_sectors()
     assert got["gather"] is None and got["copy"] is None
+
+
+class _FakeParity:
+    """Stands in for the oracle comparison: reports a planted result."""
+
+    def __init__(self, result):
+        self.enabled = True
+        self.result = result
+        self.reruns = 0
+
+    def check(self, name, out, want, n, **kw):
+        return dict(self.result)
+
+
+def _aux_with(parity):
+    aux = bench.Aux.__new__(bench.Aux)  # only the bookkeeping of the entries is exercised
+    aux.parity = parity
+    aux.out = {}
+    return aux
+
+
+def test_parity_gate_drops_the_speed_of_a_mismatching_workload():
+    aux = _aux_with(_FakeParity({"parity": "MISMATCH", "first_bad_index": 12345}))
+    ran = []
+    aux._finish("w", {"gbps": 7000.0, "frac": 1.03, "kernel_ms": 0.45}, (object(), None, 10, lambda: ran.append(1)))
+    ent = aux.out["w"]
+    assert ent["parity"] == "MISMATCH" and ent["first_bad_index"] == 12345
+    assert "gbps" not in ent and "frac" not in ent and "kernel_ms" not in ent
+    assert ran == [1]  # the in-place reset and relaunch ran before the comparison
+
+
+def test_parity_gate_keeps_the_speed_of_a_matching_workload():
+    aux = _aux_with(_FakeParity({"parity": True, "parity_elements": 10}))
+    aux._finish("w", {"gbps": 7000.0}, (object(), None, 10))
+    assert aux.out["w"]["gbps"] == 7000.0 and aux.out["w"]["parity"] is True
+    aux._finish("lib", {"gbps": 6800.0}, None)
+    assert aux.out["lib"]["parity"] == "not applicable" and aux.out["lib"]["gbps"] == 6800.0
+
+
+def test_l2_resident_entries_carry_no_hbm_fraction():
+    aux = _aux_with(None)
+    aux.peak, aux.l2_bytes = 6796.2, 135528448
+
+    class _M:
+        @staticmethod
+        def gbps(nbytes, s):
+            return nbytes / s / 1e9
+    aux.metrics = _M
+    small = aux._speed(100663296, 8.1e-6)  # 2^23-element SAXPY: 100 MB per launch
+    assert small["l2_resident"] is True and "frac" not in small and small["gbps"] > 10000
+    big = aux._speed(402653184, 57e-6)
+    assert "l2_resident" not in big and 1.0 < big["frac"] < 1.2
