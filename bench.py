@@ -1056,7 +1056,7 @@ def run_ab_gather(args):
     L = ew.lib()
     parity = Parity(not args.no_cpu)
     n = args.n if args.n != N_HEADLINE else 1 << 26
-    strides = [args.stride] if args.stride else [2, 3, 4, 5, 8, 12, 16, 32, 64]
+    strides = [args.stride] if args.stride else [2, 3, 4, 5, 6, 7, 8, 12, 16, 24, 32, 48, 64]
     for dtype in ("f32", "bf16"):
         code = DT_CODE[dtype]
         x = inputs.as_dtype(inputs.uniform(n, inputs.seed_for("copy_f32"), 0.0, 1.0), dtype)

@@ -294,25 +294,29 @@ __global__ void __launch_bounds__(kBlock) gather_tiled_kernel(const GatherArgs g
         }
     }
     __syncthreads();
-    if (P >= 2 * kBlock) {  // lap by lap: the block walks each lap's run
-        for (uint32_t L = 0; L < s; ++L) {
-            const uint32_t len = lap_len[L] > p0 ? min(lap_len[L] - p0, P) : 0;
-            W *dst = out + lap_start[L] + p0;
-            const W *row = tile + lap_row[L];
+    // Store phase: the block's s lap runs are shared out among its warps (one
+    // warp per run, or two or four per run when s is below the warp count);
+    // lane l copies positions l, l + 32, ... of its share.  16-bit runs that
+    // start on a 4-byte boundary move as 4-byte words (rows start on whole
+    // words: the pitch is even for 2-byte elements).
+    constexpr uint32_t kWarps = kBlock / 32;
+    const uint32_t wpl = s >= kWarps ? 1u : kWarps / s >= 4 ? 4u : kWarps / s >= 2 ? 2u : 1u;
+    const uint32_t seg = P / wpl;
+    const uint32_t lane = threadIdx.x & 31u;
+    for (uint32_t item = threadIdx.x >> 5; item < s * wpl; item += kWarps) {
+        const uint32_t L = item / wpl, q0 = (item - L * wpl) * seg;
+        const uint32_t len = lap_len[L] > p0 ? min(lap_len[L] - p0, P) : 0u;
+        const uint32_t end = len > q0 ? min(len - q0, seg) : 0u;
+        const W *row = tile + lap_row[L] + q0;
+        W *dst = out + (static_cast<size_t>(lap_start[L]) + p0 + q0);
+        if (E == 2 && end == seg && (reinterpret_cast<uintptr_t>(dst) & 3u) == 0) {
+            const uint32_t *row_w = reinterpret_cast<const uint32_t *>(row);
+            uint32_t *dst_w = reinterpret_cast<uint32_t *>(dst);
 #pragma unroll 4
-            for (uint32_t q = threadIdx.x; q < len; q += kBlock) dst[q] = row[q];
-        }
-    } else {  // fewer positions than threads: kBlock / P laps side by side
-        uint32_t cur = ~0u, first = 0, len = 0, row = 0;
-        for (uint32_t k = threadIdx.x; k < span; k += kBlock) {
-            const uint32_t L = k >> g.tile_log2p, q = k & (P - 1);
-            if (L != cur) {  // warp-uniform: P >= 32
-                cur = L;
-                first = lap_start[L] + p0;
-                len = lap_len[L] > p0 ? lap_len[L] - p0 : 0;
-                row = lap_row[L];
-            }
-            if (q < len) out[static_cast<size_t>(first + q)] = tile[row + q];
+            for (uint32_t w = lane; w < seg / 2; w += 32) dst_w[w] = row_w[w];
+        } else {
+#pragma unroll 4
+            for (uint32_t q = lane; q < end; q += 32) dst[q] = row[q];
         }
     }
 }
