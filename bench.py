@@ -821,7 +821,8 @@ class Aux:
         g2 = lambda: L.ew_gather_stride(0, X.ptr, Y.ptr, n26, 2, s)  # noqa: E731
         self.record_graph("gather2_f32_2p26_graph", "gather", "f32", n26, g2, (Y, want_gather(2), n26, clear))
         variants = [("gather2_f32_2p26", 2, "auto", "auto"), ("gather4_f32_2p26", 4, "auto", "auto"),
-                    ("gather8_f32_2p26", 8, "auto", "auto"), ("gather16_f32_2p26", 16, "auto", "auto"),
+                    ("gather8_f32_2p26", 8, "auto", "auto"), ("gather12_f32_2p26", 12, "auto", "auto"),
+                    ("gather16_f32_2p26", 16, "auto", "auto"),
                     ("gather64_f32_2p26", 64, "auto", "auto"),
                     ("gather16_f32_2p26_lap_order", 16, "auto", "laps"),
                     ("gather2_f32_2p26_index_order", 2, "auto", "oneshot"),

@@ -148,7 +148,7 @@ typedef enum {
  * EW_SCHED_TILED      gather only, same range of s and n as EW_SCHED_LAPS (any
  *                     n >= 1 there): the transpose-like schedule.  A block
  *                     reads the contiguous input span that its positions of
- *                     all s laps draw from (32 KiB) once, coalesced, into
+ *                     all s laps draw from (12-20 KiB) once, coalesced, into
  *                     shared memory with one row per residue mod s, then
  *                     writes each lap's outputs as one coalesced run.  For
  *                     s = 2, 4, ..., 64 and an input aligned to 16 bytes a
@@ -156,14 +156,12 @@ typedef enum {
  *                     s as shifts, a conflict-free shared-memory layout, warps
  *                     copying whole lap runs; the launch record shows
  *                     EW_PATH_V128).
- * EW_SCHED_AUTO       for the gather: EW_SCHED_LAPS below the crossover,
- *                     EW_SCHED_TILED from it up to s = 64.  The measured
- *                     crossover is s = 8 for 4-byte elements (from s = 8 a
- *                     lap-ordered fp32 warp load spends one 32-byte sector per
- *                     lane) and s = 5 for 2-byte elements (whose lap-ordered
- *                     loads move 2 bytes each); 2-byte elements at s = 2 and
- *                     4 on an input aligned to 16 bytes also take
- *                     EW_SCHED_TILED.  For the other operators,
+ * EW_SCHED_AUTO       for the gather: EW_SCHED_LAPS for s < 5, EW_SCHED_TILED
+ *                     for 5 <= s <= 64 (the measured crossover: a
+ *                     lap-ordered warp load fetches more sectors per useful
+ *                     byte as s grows, and 16-bit lanes move 2 bytes each);
+ *                     2-byte elements at s = 2 and 4 on an input aligned to
+ *                     16 bytes also take EW_SCHED_TILED.  For the other operators,
  *                     EW_SCHED_ONESHOT.  A gather with n > 2^32 always runs
  *                     persistent. */
 typedef enum {

@@ -443,17 +443,18 @@ enum class GatherKind { SPAN, TILED, LAPS, ONESHOT, STRIDE };
 constexpr uint64_t kOneshotMaxN = uint64_t(1) << 32;  // the 32-bit index kernels
 
 // AUTO's crossover from lap order to the tiled kernels.  Lap order issues one
-// load per output: from s = 8 each fp32 lane's load is its own 32-byte sector
-// (L2-to-SM traffic bounds it), and 16-bit lanes move 2 bytes per load.  The
-// tiled kernels read 16 bytes per load at any s.  Measured on GB300 at 2^26
-// elements they win from s = 8 for 4-byte elements (within 1.5% at s = 5 to
-// 7; lap order is 4% ahead at s = 2 and 4) and from s = 5 for 2-byte ones
-// (bf16 at s = 5: 5053 against 4607 GB/s).  For 2-byte elements at s = 2 and
-// 4 on a 16-byte aligned input the kernel specialised for the stride wins too
-// (bf16: 5971 against 5472 at s = 2, 5975 against 5253 at s = 4).
+// load per output: as s grows each fp32 lane's load needs more of its own
+// 32-byte sector (from s = 8 one per lane; L2-to-SM traffic bounds it), and
+// 16-bit lanes move 2 bytes per load.  The tiled kernels read 16 bytes per
+// load at any s.  Measured on GB300 at 2^26 elements they win from s = 5 for
+// both element sizes (fp32 at s = 5, 6, 7: 6396, 6399, 6480 GB/s against
+// 6101, 5941, 5463 in lap order), and lap order stays 2-3% ahead below that.
+// For 2-byte elements at s = 2 and 4 on a 16-byte aligned input the kernel
+// specialised for the stride wins too (bf16: 5962 against 5256 at s = 2,
+// 5966 against 5249 at s = 4).
 bool auto_tiled(int e, uint64_t s_mod, bool in_aligned16) {
     if (e == 2 && in_aligned16 && (s_mod == 2 || s_mod == 4)) return true;
-    return s_mod >= (e == 2 ? 5u : 8u);
+    return s_mod >= 5u;
 }
 
 GatherArgs gather_args(const void *in, void *out, uint64_t n, uint64_t s_mod) {
@@ -516,7 +517,8 @@ GatherLaunch plan_gather_span(const void *in, void *out, uint64_t n, uint64_t s_
 }
 
 // Tiled kernel: P (a power of two) positions of every lap per block, the
-// 32 KiB input span they draw from staged in shared memory, rows padded.  A
+// input span they draw from (up to 20 KiB) staged in shared memory, rows
+// padded.  A
 // power-of-two stride from 8 to 64 on a 16-byte aligned input takes the
 // kernel specialised for that stride (16-byte loads; the launch record shows
 // EW_PATH_V128 and vec_bytes 16), any other the general one.
@@ -540,9 +542,16 @@ GatherLaunch plan_gather_tiled(int e, const void *in, void *out, uint64_t n, uin
     }
     gl.entry = e == 4 ? gather_tiled_4() : gather_tiled_2();
     gl.args = gather_args(in, out, n, s_mod);
-    const uint32_t per_block = (kTiledSpanBytes / e) / static_cast<uint32_t>(s_mod);
+    // P: the largest power of two whose span s*P*e stays within
+    // kTiledStageBytes, raised until a lap run is kTiledMinRunBytes long.
+    // Measured on GB300 at 2^26 (strides 3 to 48, both element sizes): blocks
+    // staging 24 KiB or more (8 per SM) ran 9-13% slower than ones staging
+    // 12-20 KiB, the shared memory then leaving little of the SM's L1 for
+    // loads in flight; runs below 512 bytes made the store phase the limit.
+    const uint32_t su = static_cast<uint32_t>(s_mod), eu = static_cast<uint32_t>(e);
     uint32_t log2p = 0;
-    while ((2u << log2p) <= per_block) ++log2p;  // largest power of two <= per_block
+    while ((2u << log2p) * su * eu <= kTiledStageBytes) ++log2p;
+    while ((1u << log2p) * eu < kTiledMinRunBytes) ++log2p;
     gl.args.tile_p = 1u << log2p;
     gl.args.tile_log2p = log2p;
     gl.args.tile_pitch = gl.args.tile_p + tiled_pad_words(static_cast<uint32_t>(s_mod), e) * (4 / e);

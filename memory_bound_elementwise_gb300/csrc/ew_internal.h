@@ -113,8 +113,10 @@ constexpr uint64_t kMaxLaps = 64;
 const GatherEntry *gather_laps_4();
 const GatherEntry *gather_laps_2();
 // Tiled (transposing) gather: same range as the lap kernel; a block stages
-// kTiledSpanBytes of input in shared memory.
-constexpr uint32_t kTiledSpanBytes = 32768;
+// at most kTiledStageBytes of input in shared memory (more when that would
+// leave lap runs shorter than kTiledMinRunBytes).
+constexpr uint32_t kTiledStageBytes = 20480;
+constexpr uint32_t kTiledMinRunBytes = 512;
 const GatherEntry *gather_tiled_4();
 const GatherEntry *gather_tiled_2();
 // Tiled gather specialised for a power-of-two stride (2, 4, ..., 64) and an

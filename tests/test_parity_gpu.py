@@ -274,14 +274,13 @@ def _gather_laps(n, s):
 
 
 def _gather_auto_schedule(n, s, dtype, in_aligned16=False):
-    """The schedule AUTO picks: tiled from s = 8 (4-byte elements) or s = 5
-    (2-byte elements) up to 64, and for 2-byte elements at s = 2 and 4 on an
-    input aligned to 16 bytes; lap order below that where every lap holds a
-    block, else index order."""
+    """The schedule AUTO picks: tiled from s = 5 up to 64, and for 2-byte
+    elements at s = 2 and 4 on an input aligned to 16 bytes; lap order below
+    that where every lap holds a block, else index order."""
     sm = s % n
     if n > 1 << 32:
         return 2
-    if (5 if ESIZE[dtype] == 2 else 8) <= sm <= 64:
+    if 5 <= sm <= 64:
         return 4
     if ESIZE[dtype] == 2 and in_aligned16 and sm in (2, 4):
         return 4
@@ -495,7 +494,7 @@ def test_gather_small(dtype):
 
 @pytest.mark.parametrize("dtype", ["f32", "f16"])
 def test_gather_lap_order(dtype):
-    """The lap-ordered gather (schedule 'laps'; AUTO's choice below s = 8)
+    """The lap-ordered gather (schedule 'laps'; AUTO's choice below s = 5)
     for strides 2..64 once every lap holds a block of outputs: sizes at, just below and just above the
     threshold n = 2048 s, laps of unequal length (s not dividing n), laps that
     read the same sources (s | n) and laps on distinct residues (s coprime to
@@ -804,11 +803,10 @@ def test_gather_tiled(dtype):
 
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16", "i32"])
 def test_gather_auto_crossover(dtype):
-    """AUTO's choice around its crossovers: lap order below s = 8 (4-byte
-    elements) or s = 5 (2-byte elements, except s = 2 and 4 on this aligned
-    input), the tiled kernel from there to 64 (wide tiles store lap by lap,
-    narrow ones side by side; powers of two take the specialised kernel),
-    index order from 65; each against the oracle."""
+    """AUTO's choice around its crossovers: lap order below s = 5 (for 2-byte
+    elements except s = 2 and 4 on this aligned input), the tiled kernels from
+    there to 64 (powers of two take the specialised kernel), index order from
+    65; each against the oracle."""
     L = ew.lib()
     ew.set_schedule("auto")
     n = 300_007
