@@ -553,7 +553,6 @@ GatherLaunch plan_gather_tiled(int e, const void *in, void *out, uint64_t n, uin
     while ((2u << log2p) * su * eu <= kTiledStageBytes) ++log2p;
     while ((1u << log2p) * eu < kTiledMinRunBytes) ++log2p;
     gl.args.tile_p = 1u << log2p;
-    gl.args.tile_log2p = log2p;
     gl.args.tile_pitch = gl.args.tile_p + tiled_pad_words(static_cast<uint32_t>(s_mod), e) * (4 / e);
     set_lap_geometry(&gl.args, n, s_mod);
     const uint64_t lap_len = (n + s_mod - 1) / s_mod;

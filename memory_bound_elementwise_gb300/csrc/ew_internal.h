@@ -97,7 +97,6 @@ struct GatherArgs {
     uint32_t lap_m;      // lap kernel: n mod s_mod
     uint32_t div_magic;  // lap and tiled kernels: floor(2^32 / s_mod) + 1
     uint32_t tile_p;     // tiled kernel: lap positions per block (a power of two)
-    uint32_t tile_log2p; // log2(tile_p)
     uint32_t tile_pitch; // elements per shared-memory row (tile_p plus bank padding)
 };
 using GatherLaunchFn = cudaError_t (*)(const GatherArgs &, int grid, cudaStream_t);
