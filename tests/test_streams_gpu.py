@@ -113,6 +113,37 @@ def test_cuda_graph_capture_and_replay(path):
     assert ew.device_error() == (0, 0)
 
 
+def test_graph_capture_of_gathers():
+    """Every gather kernel AUTO picks, captured into one CUDA graph: lap order
+    (fp32, s = 2), the general tiled kernel (fp32, s = 12), the specialised
+    tiled kernels (fp32, s = 16; bf16, s = 2, whose store packs 16-bit pairs)
+    and index order (s = 65); replayed on fresh inputs against the oracle."""
+    n = (1 << 21) + 9
+    x = torch.empty(n, device="cuda")
+    xh = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    outs = {s: torch.empty(n, device="cuda") for s in (2, 12, 16, 65)}
+    out_h = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    st = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        for s, o in outs.items():
+            ew.ew_gather_stride(x, o, s, stream=st)
+        ew.ew_gather_stride(xh, out_h, 2, stream=st)
+    for rep in range(2):
+        hx = _f32(n, 700 + rep)
+        hh = inputs.as_dtype(_f32(n, 800 + rep), "bf16")
+        x.copy_(torch.from_numpy(hx))
+        xh.copy_(torch.from_numpy(hh.view("int16")).view(torch.bfloat16))
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        for s, o in outs.items():
+            assert_bits_equal(o.cpu().numpy(), oracle.gather_stride(hx, s), "f32", False,
+                              "graph gather s=%d rep %d" % (s, rep))
+        got_h = out_h.view(torch.int16).cpu().numpy().view("uint16")
+        assert_bits_equal(got_h, oracle.gather_stride(hh, 2), "bf16", False, "graph bf16 gather rep %d" % rep)
+
+
 def test_graph_capture_of_mixed_parity_bf16_add():
     """A 16-bit add with pointers of different parity, captured into a graph:
     inside the capture AUTO keeps the vector kernel (no pointer queries while
