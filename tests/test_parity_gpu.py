@@ -1036,3 +1036,29 @@ def test_gather_pow2_full_size_2p26(dtype, s):
     torch.cuda.synchronize()
     assert_bits_equal(bo.host(), oracle.gather_stride(x, s), dtype, False, "gather %d 2^26 %s" % (s, dtype))
     assert bo.guards_intact() and bi.guards_intact()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16", "i32"])
+def test_gather_random_cases(dtype):
+    """Seeded random gathers across every schedule: sizes from 1 to 2^20 + 999
+    (ragged tiles and laps), strides from 1 to 200 and beyond n, input and
+    output offsets from 0 to 9 elements; each output against the oracle and
+    the guard zones intact."""
+    L = ew.lib()
+    g = inputs.rng(0x6A7E + DT_CODE[dtype])
+    bits = "f32" if dtype == "i32" else dtype
+    for case in range(60):
+        n = int(g.choice([g.integers(1, 5000), g.integers(5000, 300_000), g.integers(300_000, (1 << 20) + 1000)]))
+        s = int(g.choice([g.integers(1, 9), g.integers(9, 65), g.integers(65, 200), n + int(g.integers(0, 70))]))
+        sched = str(g.choice(["auto", "auto", "laps", "tiled", "oneshot", "persistent"]))
+        in_off, out_off = int(g.integers(0, 10)), int(g.integers(0, 10))
+        ew.set_schedule(sched)
+        x = inputs.random_bits(n, bits, 12000 + case)
+        bi = GuardedBuffer(n, dtype, in_off).fill(x)
+        bo = GuardedBuffer(n, dtype, out_off)
+        assert L.ew_gather_stride(DT_CODE[dtype], bi.view.data_ptr(), bo.view.data_ptr(), n, s, _stream()) == 0
+        torch.cuda.synchronize()
+        assert_bits_equal(bo.host(), oracle.gather_stride(x, s), bits, False,
+                          "random gather %s n=%d s=%d %s offs=%d,%d" % (dtype, n, s, sched, in_off, out_off))
+        assert bi.guards_intact() and bo.guards_intact()
+    ew.set_schedule("auto")
