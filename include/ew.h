@@ -151,17 +151,19 @@ typedef enum {
  *                     all s laps draw from (12-20 KiB) once, coalesced, into
  *                     shared memory with one row per residue mod s, then
  *                     writes each lap's outputs as one coalesced run.  For
- *                     s = 2, 4, ..., 64 and an input aligned to 16 bytes a
+ *                     s = 2, 4, ..., 64 (powers of two) and s = 3, 5, 6, 7,
+ *                     9 to 15 and 24 on an input aligned to 16 bytes a
  *                     kernel specialised for that stride runs (division by
- *                     s as shifts, a conflict-free shared-memory layout, warps
- *                     copying whole lap runs; the launch record shows
- *                     EW_PATH_V128).
+ *                     s at compile time, staging stores at fixed offsets, a
+ *                     padded shared-memory layout, warps copying whole lap
+ *                     runs; the launch record shows EW_PATH_V128 and the
+ *                     block size chosen for the stride).
  * EW_SCHED_AUTO       for the gather: EW_SCHED_LAPS for s < 5, EW_SCHED_TILED
  *                     for 5 <= s <= 64 (the measured crossover: a
  *                     lap-ordered warp load fetches more sectors per useful
  *                     byte as s grows, and 16-bit lanes move 2 bytes each);
- *                     2-byte elements at s = 2 and 4 on an input aligned to
- *                     16 bytes also take EW_SCHED_TILED.  For the other operators,
+ *                     2-byte elements at s = 2, 3 and 4 on an input aligned
+ *                     to 16 bytes also take EW_SCHED_TILED.  For the other operators,
  *                     EW_SCHED_ONESHOT.  A gather with n > 2^32 always runs
  *                     persistent. */
 typedef enum {

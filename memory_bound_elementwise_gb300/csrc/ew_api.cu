@@ -261,6 +261,46 @@ uint32_t tiled_pad_words(uint32_t s, int e) {
     return table[e == 2 ? 1 : 0][s];
 }
 
+// Row padding, in elements, of the fixed-stride tiled gather's tile: the pad
+// in [0, 32) (even for 2-byte elements, so rows start on whole words) that
+// minimises the most distinct words any bank receives when the lanes of a
+// warp store element k of their 16-byte loads, over every warp of the block
+// and every k.  Computed once per (element size, stride).
+uint32_t fixed_pad_elems(int e, uint32_t s, uint32_t p, uint32_t threads) {
+    static std::mutex mu;
+    static std::map<std::pair<int, uint32_t>, uint32_t> cache;
+    std::lock_guard<std::mutex> lk(mu);
+    const auto key = std::make_pair(e, s);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    const uint32_t v = 16 / static_cast<uint32_t>(e), step = e == 2 ? 2 : 1;
+    uint32_t best_pad = 0, best = ~0u;
+    for (uint32_t pad = 0; pad < 32; pad += step) {
+        uint32_t worst = 0;
+        for (uint32_t w = 0; w < threads / 32; ++w) {
+            for (uint32_t k = 0; k < v; ++k) {
+                uint32_t words[32], nw = 0, per_bank[32] = {};
+                for (uint32_t t = 0; t < 32; ++t) {
+                    const uint32_t j = v * (32 * w + t) + k;
+                    const uint32_t word = ((j % s) * (p + pad) + j / s) * static_cast<uint32_t>(e) / 4;
+                    bool seen = false;
+                    for (uint32_t q = 0; q < nw; ++q) seen = seen || words[q] == word;
+                    if (!seen) {
+                        words[nw++] = word;
+                        worst = std::max(worst, ++per_bank[word % 32]);
+                    }
+                }
+            }
+        }
+        if (worst < best) {
+            best = worst;
+            best_pad = pad;
+        }
+    }
+    cache.emplace(key, best_pad);
+    return best_pad;
+}
+
 int clamp_grid(int64_t blocks) {
     return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(blocks, INT_MAX)));
 }
@@ -449,11 +489,11 @@ constexpr uint64_t kOneshotMaxN = uint64_t(1) << 32;  // the 32-bit index kernel
 // load at any s.  Measured on GB300 at 2^26 elements they win from s = 5 for
 // both element sizes (fp32 at s = 5, 6, 7: 6396, 6399, 6480 GB/s against
 // 6101, 5941, 5463 in lap order), and lap order stays 2-3% ahead below that.
-// For 2-byte elements at s = 2 and 4 on a 16-byte aligned input the kernel
-// specialised for the stride wins too (bf16: 5962 against 5256 at s = 2,
-// 5966 against 5249 at s = 4).
+// For 2-byte elements at s = 2, 3 and 4 on a 16-byte aligned input the
+// kernels specialised for the stride win too (bf16: 5975, 5846, 5983 GB/s
+// against 5398, 5050, 5175 in lap order).
 bool auto_tiled(int e, uint64_t s_mod, bool in_aligned16) {
-    if (e == 2 && in_aligned16 && (s_mod == 2 || s_mod == 4)) return true;
+    if (e == 2 && in_aligned16 && s_mod >= 2 && s_mod <= 4) return true;
     return s_mod >= 5u;
 }
 
@@ -516,12 +556,13 @@ GatherLaunch plan_gather_span(const void *in, void *out, uint64_t n, uint64_t s_
     return gl;
 }
 
-// Tiled kernel: P (a power of two) positions of every lap per block, the
-// input span they draw from (up to 20 KiB) staged in shared memory, rows
-// padded.  A
-// power-of-two stride from 8 to 64 on a 16-byte aligned input takes the
-// kernel specialised for that stride (16-byte loads; the launch record shows
-// EW_PATH_V128 and vec_bytes 16), any other the general one.
+// Tiled kernels: P positions of every lap per block, the input span they
+// draw from staged in shared memory, rows padded.  On a 16-byte aligned input
+// a power-of-two stride (2 to 64) takes the kernel specialised for it, and
+// 3, 5, 6, 7, 9-15 and 24 the fixed-stride kernel (16-byte loads; the
+// launch record shows EW_PATH_V128 and vec_bytes 16); any other stride, or
+// an unaligned input, the general kernel (P a power of two, span up to
+// 20 KiB).
 GatherLaunch plan_gather_tiled(int e, const void *in, void *out, uint64_t n, uint64_t s_mod) {
     GatherLaunch gl;
     const GatherEntry *pow2 = e == 4 ? gather_tiled_pow2_4(s_mod) : gather_tiled_pow2_2(s_mod);
@@ -536,6 +577,24 @@ GatherLaunch plan_gather_tiled(int e, const void *in, void *out, uint64_t n, uin
         gl.vec_bytes = 16;
         gl.smem = pow2->smem_bytes;
         gl.block = kTiledPow2Threads;
+        gl.schedule = EW_SCHED_TILED;
+        gl.nvec = static_cast<int64_t>(n);
+        return gl;
+    }
+    const GatherEntry *fixed = gather_tiled_fixed(e, s_mod);
+    if (fixed != nullptr && reinterpret_cast<uintptr_t>(in) % 16 == 0) {
+        gl.entry = fixed;
+        gl.args = gather_args(in, out, n, s_mod);
+        gl.args.tile_p = fixed->tile_p;
+        gl.args.tile_pitch = fixed->tile_p + fixed_pad_elems(e, static_cast<uint32_t>(s_mod), fixed->tile_p,
+                                                             static_cast<uint32_t>(fixed->block));
+        set_lap_geometry(&gl.args, n, s_mod);
+        const uint64_t lap_len = (n + s_mod - 1) / s_mod;
+        gl.grid = clamp_grid(static_cast<int64_t>((lap_len + gl.args.tile_p - 1) / gl.args.tile_p));
+        gl.path = EW_PATH_V128;
+        gl.vec_bytes = 16;
+        gl.smem = static_cast<int32_t>(s_mod * gl.args.tile_pitch * e);
+        gl.block = fixed->block;
         gl.schedule = EW_SCHED_TILED;
         gl.nvec = static_cast<int64_t>(n);
         return gl;

@@ -1,0 +1,28 @@
+// ew_gather_fixed.cu -- instantiations of the fixed-stride tiled gather for
+// strides that are not powers of two (both element sizes), in a translation
+// unit of their own so that the build compiles them in parallel with the rest.
+#include "ew_kernels.cuh"
+
+namespace ew {
+
+namespace {
+#define EW_FIXED_STRIDES(X) X(3) X(5) X(6) X(7) X(9) X(10) X(11) X(12) X(13) X(14) X(15) X(24)
+#define EW_ENTRY4(S) tiled_fixed_entry<4, S>(),
+#define EW_ENTRY2(S) tiled_fixed_entry<2, S>(),
+#define EW_STRIDE(S) S,
+const GatherEntry kFixed4[] = {EW_FIXED_STRIDES(EW_ENTRY4)};
+const GatherEntry kFixed2[] = {EW_FIXED_STRIDES(EW_ENTRY2)};
+constexpr uint64_t kFixedStrides[] = {EW_FIXED_STRIDES(EW_STRIDE)};
+#undef EW_ENTRY4
+#undef EW_ENTRY2
+#undef EW_STRIDE
+#undef EW_FIXED_STRIDES
+}  // namespace
+
+const GatherEntry *gather_tiled_fixed(int e, uint64_t stride) {
+    for (size_t k = 0; k < sizeof(kFixedStrides) / sizeof(kFixedStrides[0]); ++k)
+        if (kFixedStrides[k] == stride) return e == 4 ? &kFixed4[k] : &kFixed2[k];
+    return nullptr;
+}
+
+}  // namespace ew

@@ -105,6 +105,8 @@ struct GatherEntry {
     GatherLaunchFn launch;
     int unroll;
     int smem_bytes = 0;  // static shared memory per block, for the launch record
+    int block = kBlock;  // threads per block
+    uint32_t tile_p = 0; // lap positions per block of the fixed-stride tiled kernels
 };
 // Lap-ordered gather: 2 <= s_mod <= kMaxLaps, n <= 2^32 and n >= s_mod x the
 // outputs of one block.
@@ -125,6 +127,11 @@ constexpr int kTiledPow2SpanBytes = 16384;
 constexpr int kTiledPow2Threads = 256;
 const GatherEntry *gather_tiled_pow2_4(uint64_t stride);
 const GatherEntry *gather_tiled_pow2_2(uint64_t stride);
+// Tiled gather specialised for a fixed stride that is not a power of two
+// (3, 5, 6, 7, 9 to 15, 24) and an input aligned to 16 bytes; the block
+// size is chosen per stride, the row pitch (args.tile_pitch) by the host.
+// nullptr for other strides.
+const GatherEntry *gather_tiled_fixed(int e, uint64_t stride);
 const GatherEntry *gather_oneshot_4();  // binary32, n <= 2^32
 const GatherEntry *gather_stride_4();   // binary32, any n
 const GatherEntry *gather_oneshot_2();  // 16-bit types

@@ -627,3 +627,144 @@ cudaError_t launch_gather_stride(const GatherArgs &g, int grid, cudaStream_t s) 
 }
 
 }  // namespace ew
+
+namespace ew {
+
+// ---------------------------------------------------------------- fixed-stride tiled gather
+//
+// The tiled schedule for a stride S that is not a power of two but is known
+// at compile time.  A thread's 16-byte loads stay in the same rows when the
+// block's threads T are chosen so that V*T (V elements per load) is a
+// multiple of S: load i of thread t holds span elements V*t + V*T*i + k,
+// whose row (V*t + k) mod S does not depend on i and whose column advances
+// by V*T/S per load.  So each thread works out, once, the shared-memory
+// offset of each of its V elements, and every load's elements go to those
+// offsets plus a compile-time step.  T is the smallest multiple of
+// lcm(32, S / gcd(S, V)) from 192 threads; a block stages about 16 KiB of
+// input (the span is kLoads*V*T elements, P = span / S positions per lap).
+// The row pitch comes from the host (tile_pitch), chosen for the bank spread
+// of these stores; the rows live in dynamic shared memory.  The store phase
+// is the power-of-two kernel's: warps share out the lap runs.
+
+constexpr int gcd_int(int a, int b) { return b == 0 ? a : gcd_int(b, a % b); }
+constexpr int lcm_int(int a, int b) { return a / gcd_int(a, b) * b; }
+
+template <int E, int S>
+struct TiledFixed {
+    static constexpr int kPerVec = 16 / E;
+    static constexpr int kBase = lcm_int(32, S / gcd_int(S, kPerVec));
+    static constexpr int kThreads = ((192 + kBase - 1) / kBase) * kBase;
+    static constexpr int kWarps = kThreads / 32;
+    static constexpr int kWarpsPerLap = S >= kWarps ? 1 : kWarps / S;
+    // loads per thread: about 16 KiB of span, with each warp's share of a run
+    // a whole number of warp-wide 4-byte words
+    static constexpr int kRunAlign = E == 2 ? 64 : 32;
+    static constexpr int loads_for(int l) {
+        return (l * kPerVec * kThreads / S) % (kRunAlign * kWarpsPerLap) == 0 ? l : loads_for(l + 1);
+    }
+    static constexpr int kLoadsWanted = 16384 / (16 * kThreads) > 0 ? 16384 / (16 * kThreads) : 1;
+    static constexpr int kLoads = loads_for(kLoadsWanted);
+    static constexpr int kSpan = kLoads * kPerVec * kThreads;  // elements
+    static constexpr int kP = kSpan / S;
+    static constexpr int kColStep = kPerVec * kThreads / S;
+    static constexpr int kSeg = kP / kWarpsPerLap;
+    static constexpr int kWraps = (kPerVec - 1) / S + 1;  // row wraps within one load, at most
+    static_assert(kThreads <= 512 && kThreads >= S, "block size");
+    static_assert((kPerVec * kThreads) % S == 0 && kSpan % S == 0, "rows invariant across a thread's loads");
+    static_assert(kSeg % kRunAlign == 0, "whole warp-wide words per run share");
+};
+
+template <int E, int S>
+__global__ void __launch_bounds__(TiledFixed<E, S>::kThreads) gather_tiled_fixed_kernel(const GatherArgs g) {
+    enter_grid();
+    using T = TiledFixed<E, S>;
+    using W = typename std::conditional<E == 4, uint32_t, uint16_t>::type;
+    extern __shared__ __align__(16) unsigned char fixed_raw[];
+    W *tile = reinterpret_cast<W *>(fixed_raw);
+    __shared__ uint32_t lap_start[S], lap_len[S], lap_row[S];
+    const uint32_t pitch = g.tile_pitch;
+    W *out = static_cast<W *>(g.out);
+    const uint32_t p0 = blockIdx.x * static_cast<uint32_t>(T::kP);
+    if (threadIdx.x < S) {  // lap L: first output, length, offset of its source row
+        const uint32_t L = threadIdx.x, a0 = L * g.lap_m;
+        const uint32_t c0 = (a0 + S - 1) / S;                  // ceil(L*m/S)
+        const uint32_t c1 = (a0 + g.lap_m + S - 1) / S;
+        lap_start[L] = L * g.lap_q + c0;
+        lap_len[L] = g.lap_q + (c1 - c0);
+        lap_row[L] = (c0 * S - a0) * pitch;
+    }
+    const uint64_t j0 = static_cast<uint64_t>(S) * p0;  // first source of the span
+    const W *src = static_cast<const W *>(g.in) + j0;
+    const bool full = j0 + T::kSpan <= g.n;              // block-uniform
+    if (full) {
+        const char *src_bytes = reinterpret_cast<const char *>(src);
+        Vec<16> v[T::kLoads];
+#pragma unroll
+        for (int i = 0; i < T::kLoads; ++i) v[i] = ld<16>(src_bytes + (threadIdx.x + i * T::kThreads) * 16u);
+        // offsets of this thread's V elements (rows fixed across its loads)
+        const uint32_t j = T::kPerVec * threadIdx.x;
+        const uint32_t r0 = j % S, c0 = j / S;
+        uint32_t at[T::kPerVec];
+#pragma unroll
+        for (int k = 0; k < T::kPerVec; ++k) {
+            uint32_t r = r0 + k, c = c0;
+#pragma unroll
+            for (int w = 0; w < T::kWraps; ++w) {
+                const bool wrap = r >= S;
+                r = wrap ? r - S : r;
+                c = wrap ? c + 1 : c;
+            }
+            at[k] = r * pitch + c;
+        }
+#pragma unroll
+        for (int i = 0; i < T::kLoads; ++i) {
+#pragma unroll
+            for (int k = 0; k < T::kPerVec; ++k) {
+                const uint32_t w = v[i].w[k * E / 4];
+                tile[at[k] + i * T::kColStep] = static_cast<W>(E == 4 ? w : w >> (16u * (k & 1)));
+            }
+        }
+    } else {
+        const uint32_t avail = static_cast<uint32_t>(g.n - j0);  // fewer than kSpan
+        for (uint32_t j = threadIdx.x; j < avail; j += T::kThreads) tile[(j % S) * pitch + j / S] = src[j];
+    }
+    __syncthreads();
+    const uint32_t lane = threadIdx.x & 31u;
+    for (uint32_t item = threadIdx.x >> 5; item < static_cast<uint32_t>(S * T::kWarpsPerLap);
+         item += T::kWarps) {
+        const uint32_t L = item / T::kWarpsPerLap, q0 = (item % T::kWarpsPerLap) * T::kSeg;
+        const W *row = tile + lap_row[L] + q0;
+        W *dst = out + (static_cast<size_t>(lap_start[L]) + p0 + q0);
+        if (full) {
+            if (E == 4 || (reinterpret_cast<uintptr_t>(dst) & 3u) == 0) {
+                const uint32_t *row_w = reinterpret_cast<const uint32_t *>(row);
+                uint32_t *dst_w = reinterpret_cast<uint32_t *>(dst);
+#pragma unroll 8
+                for (int i = 0; i < T::kSeg * E / 4 / 32; ++i) dst_w[lane + 32 * i] = row_w[lane + 32 * i];
+            } else {
+#pragma unroll 8
+                for (int i = 0; i < T::kSeg / 32; ++i) dst[lane + 32 * i] = row[lane + 32 * i];
+            }
+        } else {
+            const uint32_t len = lap_len[L] > p0 ? min(lap_len[L] - p0, static_cast<uint32_t>(T::kP)) : 0u;
+            const uint32_t end = len > q0 ? min(len - q0, static_cast<uint32_t>(T::kSeg)) : 0u;
+            for (uint32_t q = lane; q < end; q += 32) dst[q] = row[q];
+        }
+    }
+}
+
+template <int E, int S>
+cudaError_t launch_gather_tiled_fixed(const GatherArgs &g, int grid, cudaStream_t s) {
+    const size_t smem = static_cast<size_t>(S) * g.tile_pitch * E;
+    return launch_kernel(&gather_tiled_fixed_kernel<E, S>, grid, TiledFixed<E, S>::kThreads, smem, s, g);
+}
+
+template <int E, int S>
+constexpr GatherEntry tiled_fixed_entry() {
+    using T = TiledFixed<E, S>;
+    return GatherEntry{reinterpret_cast<const void *>(&gather_tiled_fixed_kernel<E, S>),
+                       &launch_gather_tiled_fixed<E, S>, T::kLoads, 0, T::kThreads,
+                       static_cast<uint32_t>(T::kP)};
+}
+
+}  // namespace ew

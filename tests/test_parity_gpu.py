@@ -275,14 +275,14 @@ def _gather_laps(n, s):
 
 def _gather_auto_schedule(n, s, dtype, in_aligned16=False):
     """The schedule AUTO picks: tiled from s = 5 up to 64, and for 2-byte
-    elements at s = 2 and 4 on an input aligned to 16 bytes; lap order below
+    elements at s = 2 to 4 on an input aligned to 16 bytes; lap order below
     that where every lap holds a block, else index order."""
     sm = s % n
     if n > 1 << 32:
         return 2
     if 5 <= sm <= 64:
         return 4
-    if ESIZE[dtype] == 2 and in_aligned16 and sm in (2, 4):
+    if ESIZE[dtype] == 2 and in_aligned16 and sm in (2, 3, 4):
         return 4
     return 3 if _gather_laps(n, s) else 1
 
@@ -804,7 +804,7 @@ def test_gather_tiled(dtype):
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16", "i32"])
 def test_gather_auto_crossover(dtype):
     """AUTO's choice around its crossovers: lap order below s = 5 (for 2-byte
-    elements except s = 2 and 4 on this aligned input), the tiled kernels from
+    elements except s = 2 to 4 on this aligned input), the tiled kernels from
     there to 64 (powers of two take the specialised kernel), index order from
     65; each against the oracle."""
     L = ew.lib()
@@ -1061,4 +1061,43 @@ def test_gather_random_cases(dtype):
         assert_bits_equal(bo.host(), oracle.gather_stride(x, s), bits, False,
                           "random gather %s n=%d s=%d %s offs=%d,%d" % (dtype, n, s, sched, in_off, out_off))
         assert bi.guards_intact() and bo.guards_intact()
+    ew.set_schedule("auto")
+
+
+FIXED_STRIDES = (3, 5, 6, 7, 9, 10, 11, 12, 13, 14, 15, 24)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16", "i32"])
+def test_gather_tiled_fixed_strides(dtype):
+    """The tiled gather specialised for fixed strides that are not powers of
+    two (3, 5-7, 9-15, 24, and strides congruent to them mod n) on a
+    16-byte aligned input, with the block size chosen per stride: one ragged
+    block, one and several full spans, spans plus a ragged block, n divisible
+    by the stride and not, output offsets that start laps on odd and even
+    elements.  A 2-byte input offset takes the general tiled kernel."""
+    L = ew.lib()
+    code = DT_CODE[dtype]
+    e = ESIZE[dtype]
+    bits = "f32" if dtype == "i32" else dtype
+    ew.set_schedule("tiled")
+    for s in FIXED_STRIDES:
+        for n in (s + 1, 997, 4096 * 4 // e - 1, 16384 // e + 5, 3 * 16384 // e + 11, (1 << 20) + 3, 1 << 20):
+            x = inputs.random_bits(n, bits, 15000 + n + s)
+            for stride in ((s, n + s) if n < 2000 else (s,)):
+                for in_off, out_off in ((0, 0), (0, 1), (0, 3), (4 // e if e == 2 else 1, 2)):
+                    bi = GuardedBuffer(n, dtype, in_off).fill(x)
+                    bo = GuardedBuffer(n, dtype, out_off)
+                    assert L.ew_gather_stride(code, bi.view.data_ptr(), bo.view.data_ptr(), n, stride,
+                                              _stream()) == 0
+                    rec = ew.last_launch()
+                    aligned = (in_off * e) % 16 == 0
+                    assert rec["schedule"] == 4, (n, s, rec)
+                    assert rec["path"] == (2 if aligned else 1) and rec["vec_bytes"] == (16 if aligned else e), rec
+                    assert (rec["block"] % 96 == 0 or rec["block"] % 160 == 0 or rec["block"] % 224 == 0
+                            or rec["block"] >= 288) if aligned else rec["block"] == 256, rec
+                    torch.cuda.synchronize()
+                    assert_bits_equal(bo.host(), oracle.gather_stride(x, stride), bits, False,
+                                      "fixed tiled gather %s n=%d s=%d offs=%d,%d"
+                                      % (dtype, n, stride, in_off, out_off))
+                    assert bi.guards_intact() and bo.guards_intact()
     ew.set_schedule("auto")
