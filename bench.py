@@ -840,10 +840,10 @@ class Aux:
         ew.set_schedule("auto")
         del X, Y
         gathered.clear()
-        # 16-bit gathers (the tiled kernel's 2-byte instantiation from stride 8)
+        # 16-bit gathers (the tiled kernels' 2-byte instantiations)
         xh = inputs.as_dtype(inputs.uniform(n26, inputs.seed_for("copy_f32", 3), 0.0, 1.0), "bf16")
         X, Y = self.buf(xh, "bf16"), self.buf(np.zeros_like(xh), "bf16")
-        for stride in (2, 16, 64):
+        for stride in (2, 3, 16, 64):
             want = orc.gather_stride(xh, stride)
             Y.raw.zero_()
             self.record("gather%d_bf16_2p26" % stride, "gather", "bf16", n26,
