@@ -152,7 +152,7 @@ typedef enum {
  *                     shared memory with one row per residue mod s, then
  *                     writes each lap's outputs as one coalesced run.  For
  *                     s = 2, 4, ..., 64 (powers of two) and s = 3, 5, 6, 7,
- *                     9 to 15 and 24 on an input aligned to 16 bytes a
+ *                     9 to 15, 24 and 48 on an input aligned to 16 bytes a
  *                     kernel specialised for that stride runs (division by
  *                     s at compile time, staging stores at fixed offsets, a
  *                     padded shared-memory layout, warps copying whole lap

@@ -559,7 +559,7 @@ GatherLaunch plan_gather_span(const void *in, void *out, uint64_t n, uint64_t s_
 // Tiled kernels: P positions of every lap per block, the input span they
 // draw from staged in shared memory, rows padded.  On a 16-byte aligned input
 // a power-of-two stride (2 to 64) takes the kernel specialised for it, and
-// 3, 5, 6, 7, 9-15 and 24 the fixed-stride kernel (16-byte loads; the
+// 3, 5, 6, 7, 9-15, 24 and 48 the fixed-stride kernel (16-byte loads; the
 // launch record shows EW_PATH_V128 and vec_bytes 16); any other stride, or
 // an unaligned input, the general kernel (P a power of two, span up to
 // 20 KiB).

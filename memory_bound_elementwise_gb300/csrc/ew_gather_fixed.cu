@@ -6,7 +6,7 @@
 namespace ew {
 
 namespace {
-#define EW_FIXED_STRIDES(X) X(3) X(5) X(6) X(7) X(9) X(10) X(11) X(12) X(13) X(14) X(15) X(24)
+#define EW_FIXED_STRIDES(X) X(3) X(5) X(6) X(7) X(9) X(10) X(11) X(12) X(13) X(14) X(15) X(24) X(48)
 #define EW_ENTRY4(S) tiled_fixed_entry<4, S>(),
 #define EW_ENTRY2(S) tiled_fixed_entry<2, S>(),
 #define EW_STRIDE(S) S,

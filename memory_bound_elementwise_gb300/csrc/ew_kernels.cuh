@@ -640,8 +640,9 @@ namespace ew {
 // by V*T/S per load.  So each thread works out, once, the shared-memory
 // offset of each of its V elements, and every load's elements go to those
 // offsets plus a compile-time step.  T is the smallest multiple of
-// lcm(32, S / gcd(S, V)) from 192 threads; a block stages about 16 KiB of
-// input (the span is kLoads*V*T elements, P = span / S positions per lap).
+// lcm(32, S / gcd(S, V)) from 192 threads (384 from S = 32); a block stages
+// about 16 KiB of input (32 KiB from S = 32, so that lap runs stay long; the
+// span is kLoads*V*T elements, P = span / S positions per lap).
 // The row pitch comes from the host (tile_pitch), chosen for the bank spread
 // of these stores; the rows live in dynamic shared memory.  The store phase
 // is the power-of-two kernel's: warps share out the lap runs.
@@ -653,7 +654,10 @@ template <int E, int S>
 struct TiledFixed {
     static constexpr int kPerVec = 16 / E;
     static constexpr int kBase = lcm_int(32, S / gcd_int(S, kPerVec));
-    static constexpr int kThreads = ((192 + kBase - 1) / kBase) * kBase;
+    // wide strides: bigger blocks and spans, so that lap runs stay long
+    static constexpr int kMinThreads = S >= 32 ? 384 : 192;
+    static constexpr int kTargetBytes = S >= 32 ? 32768 : 16384;
+    static constexpr int kThreads = ((kMinThreads + kBase - 1) / kBase) * kBase;
     static constexpr int kWarps = kThreads / 32;
     static constexpr int kWarpsPerLap = S >= kWarps ? 1 : kWarps / S;
     // loads per thread: about 16 KiB of span, with each warp's share of a run
@@ -662,7 +666,7 @@ struct TiledFixed {
     static constexpr int loads_for(int l) {
         return (l * kPerVec * kThreads / S) % (kRunAlign * kWarpsPerLap) == 0 ? l : loads_for(l + 1);
     }
-    static constexpr int kLoadsWanted = 16384 / (16 * kThreads) > 0 ? 16384 / (16 * kThreads) : 1;
+    static constexpr int kLoadsWanted = kTargetBytes / (16 * kThreads) > 0 ? kTargetBytes / (16 * kThreads) : 1;
     static constexpr int kLoads = loads_for(kLoadsWanted);
     static constexpr int kSpan = kLoads * kPerVec * kThreads;  // elements
     static constexpr int kP = kSpan / S;

@@ -1064,13 +1064,13 @@ def test_gather_random_cases(dtype):
     ew.set_schedule("auto")
 
 
-FIXED_STRIDES = (3, 5, 6, 7, 9, 10, 11, 12, 13, 14, 15, 24)
+FIXED_STRIDES = (3, 5, 6, 7, 9, 10, 11, 12, 13, 14, 15, 24, 48)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16", "i32"])
 def test_gather_tiled_fixed_strides(dtype):
     """The tiled gather specialised for fixed strides that are not powers of
-    two (3, 5-7, 9-15, 24, and strides congruent to them mod n) on a
+    two (3, 5-7, 9-15, 24, 48, and strides congruent to them mod n) on a
     16-byte aligned input, with the block size chosen per stride: one ragged
     block, one and several full spans, spans plus a ragged block, n divisible
     by the stride and not, output offsets that start laps on odd and even
