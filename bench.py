@@ -120,6 +120,7 @@ PROFILE_CASES = {
     "gather2_span_f32": ("gather_span", "f32", 0),
     "add_bf16_mixed": ("add", "bf16", (1, 0, 3)),
     "gather16_f32": ("gather16", "f32", 0),
+    "gather16_f32_off1": ("gather16", "f32", 1),  # input one element past 16 bytes: the general tiled kernel
     "gather16_bf16": ("gather16", "bf16", 0),
     "gather2_bf16": ("gather", "bf16", 0),
     "saxpy_relu_f32": ("saxpy_relu", "f32", 0),
