@@ -30,8 +30,10 @@ the whole array (dispatch, vector body, scalar head/tail).
               element and with pointers of different parity; bf16/fp16 SAXPY,
               ReLU and both fused chains at 2^28; SAXPY 32M, 2^26 and 2^28;
               ReLU 2^28 out of place and in place; fused add+ReLU and
-              SAXPY+ReLU against the unfused pairs; copy and gathers at strides
-              2, 4 and 16 at 2^26 in each block order; the even/odd select;
+              SAXPY+ReLU against the unfused pairs; copy and gathers at 2^26
+              (fp32 strides 2 to 64 in each block order, bf16 strides 2, 3, 16
+              and 64), each gather also against the contiguous copy of its
+              dtype and n (frac_of_copy_same_n); the even/odd select;
               fp32 add at 2^20+3; the headline through the persistent schedule
               and the bulk-copy path; chains of short SAXPY calls; the library
               device-to-device copy).  Every entry's output is compared with
@@ -56,6 +58,7 @@ import ctypes
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -100,6 +103,8 @@ def parse(argv=None):
     p.add_argument("--profile-case", default=None, choices=sorted(PROFILE_CASES),
                    help="run only warmup+steps launches of one workload at --n (for ncu captures)")
     p.add_argument("--stride", type=int, default=None, help="gather stride for the gather profile cases")
+    p.add_argument("--ab-strides", default=None,
+                   help="gather A/B: comma-separated strides, each on an aligned input and one element past it")
     p.add_argument("--ab", default=None, choices=["widths", "gather"],
                    help="A/B timing instead of the benchmark: access widths, or gather schedules by stride")
     return p.parse_args(argv)
@@ -457,6 +462,16 @@ class Timer:
         e = self.torch.cuda.Event(enable_timing=True)
         e.record(self.stream)
         return e
+
+
+def add_copy_fractions(out):
+    """Each 2^26 gather entry gets its rate over that of the contiguous copy of
+    the same dtype and n measured in the same run (copy_<dtype>_2p26)."""
+    for name, ent in out.items():
+        m = re.match(r"gather\d+_(f32|bf16)_2p26", name)
+        copy = out.get("copy_%s_2p26" % m.group(1), {}) if m else {}
+        if "gbps" in ent and "gbps" in copy:
+            ent["frac_of_copy_same_n"] = ent["gbps"] / copy["gbps"]
 
 
 def time_launches(torch, stream, fn, steps, warmup, poll=None):
@@ -844,6 +859,8 @@ class Aux:
         # 16-bit gathers (the tiled kernels' 2-byte instantiations)
         xh = inputs.as_dtype(inputs.uniform(n26, inputs.seed_for("copy_f32", 3), 0.0, 1.0), "bf16")
         X, Y = self.buf(xh, "bf16"), self.buf(np.zeros_like(xh), "bf16")
+        self.record("copy_bf16_2p26", "copy", "bf16", n26, lambda: L.ew_copy(2, X.ptr, Y.ptr, n26, s),
+                    (Y, lambda lo, hi: xh[lo:hi], n26), steps=200)
         for stride in (2, 3, 16, 64):
             want = orc.gather_stride(xh, stride)
             Y.raw.zero_()
@@ -963,6 +980,7 @@ class Aux:
         for ent in self.out.values():  # against the copy ceiling measured in this run
             if "frac" in ent:
                 ent["frac_of_d2d"] = ent["gbps"] / g
+        add_copy_fractions(self.out)
         if "gather2_f32_2p26" in self.out:
             self.out["gather2_f32_2p26"]["sectors_per_request"] = profiled_sectors()
         return self.out
@@ -1046,8 +1064,9 @@ def run_ab_widths(args):
 
 
 def run_ab_gather(args):
-    """Gather schedules (lap order, tiled, index order) at strides 2 to 64, on
-    2^26 fp32 and bf16 elements: median per launch and parity for each."""
+    """Gather schedules (lap order, tiled) at strides 2 to 64, on 2^26 fp32 and
+    bf16 elements, on a 16-byte aligned input and on one a single element past
+    it: median and mean per launch and parity for each."""
     import torch
 
     import memory_bound_elementwise_gb300 as ew
@@ -1058,14 +1077,19 @@ def run_ab_gather(args):
     L = ew.lib()
     parity = Parity(not args.no_cpu)
     n = args.n if args.n != N_HEADLINE else 1 << 26
-    strides = [args.stride] if args.stride else [2, 3, 4, 5, 6, 7, 8, 12, 16, 24, 32, 48, 64]
-    for dtype in ("f32", "bf16"):
+    # aligned: the specialised strides and three that only the general tiled
+    # kernel serves; one element past 16 bytes: the general kernel throughout
+    plan = [(0, [2, 3, 4, 5, 6, 7, 8, 12, 16, 17, 24, 32, 40, 48, 63, 64]), (1, [2, 3, 4, 5, 12, 16, 40])]
+    if args.ab_strides or args.stride:
+        chosen = [int(v) for v in args.ab_strides.split(",")] if args.ab_strides else [args.stride]
+        plan = [(0, chosen), (1, chosen)]
+    for dtype, (offset, strides) in ((d, p) for d in ("f32", "bf16") for p in plan):
         code = DT_CODE[dtype]
         x = inputs.as_dtype(inputs.uniform(n, inputs.seed_for("copy_f32"), 0.0, 1.0), dtype)
-        X, Y = DevBuf(torch, dev, x, dtype), DevBuf(torch, dev, np.zeros_like(x), dtype)
+        X, Y = DevBuf(torch, dev, x, dtype, offset), DevBuf(torch, dev, np.zeros_like(x), dtype)
         for stride in strides:
             want = parity.oracle.gather_stride(x, stride) if parity.enabled else None
-            row = {"ab": "gather", "dtype": dtype, "n": n, "stride": stride}
+            row = {"ab": "gather", "dtype": dtype, "n": n, "stride": stride, "input_offset_elems": offset}
             for sched in ("auto", "laps", "tiled"):
                 ew.set_schedule(sched)
                 call = lambda: L.ew_gather_stride(code, X.ptr, Y.ptr, n, stride, s)  # noqa: E731
@@ -1073,9 +1097,10 @@ def run_ab_gather(args):
                 total, kern = time_launches(torch, stream, call, 50, 3)
                 t = sorted(time_launches.last_per_launch)
                 rec = ew.last_launch()
-                row[sched] = {"median_us": t[len(t) // 2] * 1e6,
-                              "gbps_median": metrics.gbps(metrics.algorithmic_bytes("gather", dtype, n),
-                                                          t[len(t) // 2]),
+                nbytes = metrics.algorithmic_bytes("gather", dtype, n)
+                row[sched] = {"median_us": t[len(t) // 2] * 1e6, "mean_us": kern * 1e6,
+                              "gbps_median": metrics.gbps(nbytes, t[len(t) // 2]),
+                              "gbps_mean": metrics.gbps(nbytes, kern),
                               "schedule_ran": ew.SCHED_NAMES.get(rec["schedule"], rec["schedule"])}
                 if want is not None:
                     row[sched].update(parity.check("g%d%s%s" % (stride, dtype, sched), Y,

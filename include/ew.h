@@ -152,7 +152,8 @@ typedef enum {
  *                     shared memory with one row per residue mod s, then
  *                     writes each lap's outputs as one coalesced run.  For
  *                     s = 2, 4, ..., 64 (powers of two) and s = 3, 5, 6, 7,
- *                     9 to 15, 24 and 48 on an input aligned to 16 bytes a
+ *                     9 to 15, the even strides 18 to 30, 40, 48, 52, 56
+ *                     and 60 on an input aligned to 16 bytes a
  *                     kernel specialised for that stride runs (division by
  *                     s at compile time, staging stores at fixed offsets, a
  *                     padded shared-memory layout, warps copying whole lap
@@ -162,8 +163,8 @@ typedef enum {
  *                     for 5 <= s <= 64 (the measured crossover: a
  *                     lap-ordered warp load fetches more sectors per useful
  *                     byte as s grows, and 16-bit lanes move 2 bytes each);
- *                     2-byte elements at s = 2, 3 and 4 on an input aligned
- *                     to 16 bytes also take EW_SCHED_TILED.  For the other operators,
+ *                     2-byte elements take EW_SCHED_TILED from s = 2.
+ *                     For the other operators,
  *                     EW_SCHED_ONESHOT.  A gather with n > 2^32 always runs
  *                     persistent. */
 typedef enum {

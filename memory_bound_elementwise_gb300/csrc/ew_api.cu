@@ -221,44 +221,51 @@ bool all_device_memory(const void *const *p, int np) {
     return true;
 }
 
-// Row padding, in 4-byte words, of the tiled gather's shared-memory tile.  A
-// warp writes 32 consecutive input elements j to row j mod s, column j / s;
-// with rows a multiple of 32 words plus w apart, element j lands in bank
-// ((j mod s) * w + word of j / s) mod 32.  Chosen once per (s, element size):
-// the w in [1, 32) that puts the fewest distinct words in any bank (one for
-// every s except even s below 32 that are not powers of two, which get two).
-uint32_t tiled_pad_words(uint32_t s, int e) {
-    static const std::array<std::array<uint8_t, kMaxLaps + 1>, 2> table = [] {
-        std::array<std::array<uint8_t, kMaxLaps + 1>, 2> t{};
-        for (int k = 0; k < 2; ++k) {
-            const uint32_t elems_per_word = k == 0 ? 1 : 2;  // 4-byte, 2-byte elements
-            for (uint32_t sv = 2; sv <= kMaxLaps; ++sv) {
-                uint32_t best_w = 1, best = 33;
-                for (uint32_t w = 1; w < 32; ++w) {
-                    // distinct words per bank; rows are 64 * 32 words (a multiple of 32) plus w apart
-                    uint32_t words[32], nw = 0, per_bank[32] = {};
-                    for (uint32_t j = 0; j < 32; ++j) {
-                        const uint32_t word = (j % sv) * (2048 + w) + (j / sv) / elems_per_word;
-                        bool seen = false;
-                        for (uint32_t q = 0; q < nw; ++q) seen = seen || words[q] == word;
-                        if (!seen) {
-                            words[nw++] = word;
-                            ++per_bank[word % 32];
-                        }
-                    }
-                    uint32_t worst = 0;
-                    for (uint32_t b = 0; b < 32; ++b) worst = std::max(worst, per_bank[b]);
-                    if (worst < best) {
-                        best = worst;
-                        best_w = w;
+// Row padding, in 4-byte words, of the general tiled gather's tile.  Lane t
+// of warp w stores element k of its 16-byte load, span element
+// j = V*(32*w + t) + k (V elements per load), to row j mod s, column j / s.
+// Rows are p elements (a multiple of 32 words) plus w_pad words apart, so the
+// element lands in bank ((j mod s) * w_pad + word of j / s) mod 32.  Chosen
+// once per (s, element size, p): the w_pad in [1, 32) with the fewest
+// wavefronts (the most distinct words in one bank) summed over the stores of
+// a whole span.  An input past a 16-byte boundary shifts j by the same few
+// elements in every load, which moves no store into another bank count.
+uint32_t tiled_pad_words(uint32_t s, int e, uint32_t p) {
+    static std::mutex mu;
+    static std::map<std::pair<int, uint32_t>, uint32_t> cache;
+    std::lock_guard<std::mutex> lk(mu);
+    const auto key = std::make_pair(e, s);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    const uint32_t v = 16 / static_cast<uint32_t>(e), ew = static_cast<uint32_t>(e);
+    const uint32_t nv = s * p / v;  // loads in a full span
+    uint32_t best_w = 1;
+    uint64_t best = ~uint64_t(0);
+    for (uint32_t w_pad = 1; w_pad < 32; ++w_pad) {
+        uint64_t total = 0;
+        for (uint32_t w = 0; w * 32 < nv; ++w) {
+            for (uint32_t k = 0; k < v; ++k) {
+                uint32_t words[32], nw = 0, per_bank[32] = {}, worst = 0;
+                for (uint32_t t = 0; t < 32 && 32 * w + t < nv; ++t) {
+                    const uint32_t j = v * (32 * w + t) + k;
+                    const uint32_t word = (j % s) * (2048 + w_pad) + (j / s) * ew / 4;
+                    bool seen = false;
+                    for (uint32_t q = 0; q < nw; ++q) seen = seen || words[q] == word;
+                    if (!seen) {
+                        words[nw++] = word;
+                        worst = std::max(worst, ++per_bank[word % 32]);
                     }
                 }
-                t[k][sv] = static_cast<uint8_t>(best_w);
+                total += worst;
             }
         }
-        return t;
-    }();
-    return table[e == 2 ? 1 : 0][s];
+        if (total < best) {
+            best = total;
+            best_w = w_pad;
+        }
+    }
+    cache.emplace(key, best_w);
+    return best_w;
 }
 
 // Row padding, in elements, of the fixed-stride tiled gather's tile: the pad
@@ -489,13 +496,12 @@ constexpr uint64_t kOneshotMaxN = uint64_t(1) << 32;  // the 32-bit index kernel
 // load at any s.  Measured on GB300 at 2^26 elements they win from s = 5 for
 // both element sizes (fp32 at s = 5, 6, 7: 6396, 6399, 6480 GB/s against
 // 6101, 5941, 5463 in lap order), and lap order stays 2-3% ahead below that.
-// For 2-byte elements at s = 2, 3 and 4 on a 16-byte aligned input the
-// kernels specialised for the stride win too (bf16: 5975, 5846, 5983 GB/s
-// against 5398, 5050, 5175 in lap order).
-bool auto_tiled(int e, uint64_t s_mod, bool in_aligned16) {
-    if (e == 2 && in_aligned16 && s_mod >= 2 && s_mod <= 4) return true;
-    return s_mod >= 5u;
-}
+// For 2-byte elements the tiled kernels win from s = 2: at s = 2, 3 and 4
+// the kernels specialised for the stride on a 16-byte aligned input (bf16:
+// 5974, 5866, 5996 GB/s against 5358, 4998, 5239 in lap order), and the
+// general one on an input past a 16-byte boundary (5689, 5266, 5684 against
+// 5418, 4987, 5246).
+bool auto_tiled(int e, uint64_t s_mod) { return s_mod >= (e == 2 ? 2u : 5u); }
 
 GatherArgs gather_args(const void *in, void *out, uint64_t n, uint64_t s_mod) {
     GatherArgs a{};
@@ -520,14 +526,14 @@ void set_lap_geometry(GatherArgs *a, uint64_t n, uint64_t s_mod) {
 //   laps     AUTO below that, or EW_SCHED_LAPS, once every lap holds a block;
 //   oneshot  index order, one block per chunk (n <= 2^32);
 //   stride   index order, grid-stride (EW_SCHED_PERSISTENT, or n > 2^32).
-GatherKind choose_gather(int e, uint64_t n, uint64_t s_mod, bool in_aligned16) {
+GatherKind choose_gather(int e, uint64_t n, uint64_t s_mod) {
     const int path = g_path.load(std::memory_order_relaxed);
     const int sched = g_schedule.load(std::memory_order_relaxed);
     const bool small_n = n <= kOneshotMaxN;
     if (path == EW_PATH_V256 && e == 4 && (s_mod == 2 || s_mod == 4) && small_n) return GatherKind::SPAN;
     if (sched == EW_SCHED_PERSISTENT || !small_n) return GatherKind::STRIDE;
     const bool small_stride = s_mod >= 2 && s_mod <= kMaxLaps;
-    const bool tiled = sched == EW_SCHED_TILED || (sched == EW_SCHED_AUTO && auto_tiled(e, s_mod, in_aligned16));
+    const bool tiled = sched == EW_SCHED_TILED || (sched == EW_SCHED_AUTO && auto_tiled(e, s_mod));
     if (small_stride && tiled) return GatherKind::TILED;
     const GatherEntry *laps = e == 4 ? gather_laps_4() : gather_laps_2();
     const uint64_t lap_block = static_cast<uint64_t>(kBlock) * laps->unroll;
@@ -559,10 +565,11 @@ GatherLaunch plan_gather_span(const void *in, void *out, uint64_t n, uint64_t s_
 // Tiled kernels: P positions of every lap per block, the input span they
 // draw from staged in shared memory, rows padded.  On a 16-byte aligned input
 // a power-of-two stride (2 to 64) takes the kernel specialised for it, and
-// 3, 5, 6, 7, 9-15, 24 and 48 the fixed-stride kernel (16-byte loads; the
-// launch record shows EW_PATH_V128 and vec_bytes 16); any other stride, or
-// an unaligned input, the general kernel (P a power of two, span up to
-// 20 KiB).
+// the strides of the fixed-stride set (3, 5-7, 9-15, the even strides 18-30,
+// 40, 48, 52, 56, 60) the fixed-stride kernel; any other stride, or an
+// unaligned input, the general kernel (P a power of two, span up to 20 KiB
+// unless that leaves lap runs under 512 bytes).  All stage with 16-byte loads
+// (the launch record shows EW_PATH_V128 and vec_bytes 16).
 GatherLaunch plan_gather_tiled(int e, const void *in, void *out, uint64_t n, uint64_t s_mod) {
     GatherLaunch gl;
     const GatherEntry *pow2 = e == 4 ? gather_tiled_pow2_4(s_mod) : gather_tiled_pow2_2(s_mod);
@@ -612,11 +619,12 @@ GatherLaunch plan_gather_tiled(int e, const void *in, void *out, uint64_t n, uin
     while ((2u << log2p) * su * eu <= kTiledStageBytes) ++log2p;
     while ((1u << log2p) * eu < kTiledMinRunBytes) ++log2p;
     gl.args.tile_p = 1u << log2p;
-    gl.args.tile_pitch = gl.args.tile_p + tiled_pad_words(static_cast<uint32_t>(s_mod), e) * (4 / e);
+    gl.args.tile_pitch = gl.args.tile_p + tiled_pad_words(su, e, gl.args.tile_p) * (4 / e);
     set_lap_geometry(&gl.args, n, s_mod);
     const uint64_t lap_len = (n + s_mod - 1) / s_mod;
     gl.grid = clamp_grid(static_cast<int64_t>((lap_len + gl.args.tile_p - 1) / gl.args.tile_p));
-    gl.vec_bytes = e;
+    gl.path = EW_PATH_V128;  // 16-byte staging loads from each span's first 16-byte boundary
+    gl.vec_bytes = 16;
     gl.smem = static_cast<int32_t>(s_mod * gl.args.tile_pitch * e);
     gl.schedule = EW_SCHED_TILED;
     gl.nvec = static_cast<int64_t>(n);
@@ -775,7 +783,7 @@ ew_status ew_gather_stride(ew_dtype dt, const void *in, void *out, int64_t n, in
     const uint64_t un = static_cast<uint64_t>(n);
     const uint64_t s_mod = static_cast<uint64_t>(stride) % un;
     GatherLaunch gl;
-    switch (choose_gather(e, un, s_mod, reinterpret_cast<uintptr_t>(in) % 16 == 0)) {
+    switch (choose_gather(e, un, s_mod)) {
         case GatherKind::SPAN: gl = plan_gather_span(in, out, un, s_mod); break;
         case GatherKind::TILED: gl = plan_gather_tiled(e, in, out, un, s_mod); break;
         case GatherKind::LAPS: gl = plan_gather_laps(e, in, out, un, s_mod); break;

@@ -6,7 +6,11 @@
 namespace ew {
 
 namespace {
-#define EW_FIXED_STRIDES(X) X(3) X(5) X(6) X(7) X(9) X(10) X(11) X(12) X(13) X(14) X(15) X(24) X(48)
+// Every stride up to 64 that is not a power of two and whose block fits the
+// kernel's rule (at most 512 threads with V*T a multiple of the stride).
+#define EW_FIXED_STRIDES(X)                                                                       \
+    X(3) X(5) X(6) X(7) X(9) X(10) X(11) X(12) X(13) X(14) X(15) X(18) X(20) X(22) X(24) X(26) \
+    X(28) X(30) X(40) X(48) X(52) X(56) X(60)
 #define EW_ENTRY4(S) tiled_fixed_entry<4, S>(),
 #define EW_ENTRY2(S) tiled_fixed_entry<2, S>(),
 #define EW_STRIDE(S) S,

@@ -128,7 +128,8 @@ constexpr int kTiledPow2Threads = 256;
 const GatherEntry *gather_tiled_pow2_4(uint64_t stride);
 const GatherEntry *gather_tiled_pow2_2(uint64_t stride);
 // Tiled gather specialised for a fixed stride that is not a power of two
-// (3, 5, 6, 7, 9 to 15, 24, 48) and an input aligned to 16 bytes; the block
+// (3, 5, 6, 7, 9 to 15, the even strides 18 to 30, 40, 48, 52, 56, 60) and
+// an input aligned to 16 bytes; the block
 // size is chosen per stride, the row pitch (args.tile_pitch) by the host.
 // nullptr for other strides.
 const GatherEntry *gather_tiled_fixed(int e, uint64_t stride);

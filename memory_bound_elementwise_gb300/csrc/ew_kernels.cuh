@@ -210,8 +210,9 @@ __global__ void __launch_bounds__(kBlock) gather_laps_kernel(const GatherArgs g)
 // Tiled gather for a small stride (2 <= s <= kMaxLaps, n <= 2^32): the
 // transpose-like schedule.  Block b owns positions [b*P, (b+1)*P) of every
 // lap.  Their sources r_L + s*p fill the input span [s*b*P, s*(b+1)*P),
-// clipped at n, which the block reads once, coalesced (16-byte loads when the
-// span is 16-byte aligned).  It writes the span to shared memory transposed:
+// clipped at n, which the block reads once, coalesced: 16-byte loads from the
+// span's first 16-byte boundary on, single elements before it and after the
+// last whole vector.  It writes the span to shared memory transposed:
 // element j goes to row j mod s, column j / s.  Row r then holds, in position
 // order, the sources of every lap with r_L = r, so each lap's outputs leave as
 // one coalesced run.  Rows are padded so that a warp's 32 consecutive
@@ -242,10 +243,14 @@ __global__ void __launch_bounds__(kBlock) gather_tiled_kernel(const GatherArgs g
     const uint32_t span = s * P;
     const uint32_t avail = g.n - j0 < span ? static_cast<uint32_t>(g.n - j0) : span;
     const W *src = static_cast<const W *>(g.in) + j0;
-    uint32_t done = 0;  // leading span elements staged by vector loads
-    if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
-        const uint4 *src4 = reinterpret_cast<const uint4 *>(src);
-        const uint32_t nv = avail / kPerVec;
+    // Elements before the span's first 16-byte boundary (the input pointer is
+    // element-aligned, so this is a whole number of elements).
+    const uint32_t to16 = ((16u - (static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src)) & 15u)) & 15u) / E;
+    const uint32_t h = to16 < avail ? to16 : avail;
+    const uint32_t nv = (avail - h) / kPerVec;
+    const uint32_t done = h + nv * kPerVec;  // [h, done) is staged by vector loads
+    {
+        const uint4 *src4 = reinterpret_cast<const uint4 *>(src + h);
         for (uint32_t base = 0; base < nv; base += U * kBlock) {
             uint4 v[U];
 #pragma unroll
@@ -257,7 +262,7 @@ __global__ void __launch_bounds__(kBlock) gather_tiled_kernel(const GatherArgs g
             for (int u = 0; u < U; ++u) {
                 const uint32_t vi = base + u * kBlock + threadIdx.x;
                 if (vi >= nv) continue;
-                const uint32_t j = vi * kPerVec;
+                const uint32_t j = h + vi * kPerVec;
                 const uint32_t c = div_by_s(j, s, g.div_magic);
                 uint32_t r = j - c * s;
                 uint32_t at = r * pitch + c;  // tile slot of element j
@@ -275,23 +280,14 @@ __global__ void __launch_bounds__(kBlock) gather_tiled_kernel(const GatherArgs g
                 }
             }
         }
-        done = nv * kPerVec;
     }
-    for (uint32_t base = done; base < avail; base += 8 * kBlock) {  // unaligned span, ragged end
-        W v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const uint32_t j = base + u * kBlock + threadIdx.x;
-            if (j < avail) v[u] = src[j];
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const uint32_t j = base + u * kBlock + threadIdx.x;
-            if (j < avail) {
-                const uint32_t c = div_by_s(j, s, g.div_magic);
-                tile[(j - c * s) * pitch + c] = v[u];
-            }
-        }
+    // Single elements: the head [0, h) and the ragged end [done, avail), fewer
+    // than 2 * kPerVec in all.
+    const uint32_t rest = h + (avail - done);
+    if (threadIdx.x < rest) {
+        const uint32_t j = threadIdx.x < h ? threadIdx.x : done + (threadIdx.x - h);
+        const uint32_t c = div_by_s(j, s, g.div_magic);
+        tile[(j - c * s) * pitch + c] = src[j];
     }
     __syncthreads();
     // Store phase: the block's s lap runs are shared out among its warps (one
@@ -641,8 +637,9 @@ namespace ew {
 // offset of each of its V elements, and every load's elements go to those
 // offsets plus a compile-time step.  T is the smallest multiple of
 // lcm(32, S / gcd(S, V)) from 192 threads (384 from S = 32); a block stages
-// about 16 KiB of input (32 KiB from S = 32, so that lap runs stay long; the
-// span is kLoads*V*T elements, P = span / S positions per lap).
+// about 16 KiB of input (20 KiB for blocks of 352 threads or more, 32 KiB
+// from S = 32 so that lap runs stay long; the span is kLoads*V*T elements,
+// P = span / S positions per lap).
 // The row pitch comes from the host (tile_pitch), chosen for the bank spread
 // of these stores; the rows live in dynamic shared memory.  The store phase
 // is the power-of-two kernel's: warps share out the lap runs.
@@ -656,12 +653,19 @@ struct TiledFixed {
     static constexpr int kBase = lcm_int(32, S / gcd_int(S, kPerVec));
     // wide strides: bigger blocks and spans, so that lap runs stay long
     static constexpr int kMinThreads = S >= 32 ? 384 : 192;
-    static constexpr int kTargetBytes = S >= 32 ? 32768 : 16384;
     static constexpr int kThreads = ((kMinThreads + kBase - 1) / kBase) * kBase;
+    // Span per block: 16 KiB for blocks of up to 320 threads (6 to 10 per
+    // SM), 20 KiB for the larger ones (4 or 5 per SM), 32 KiB for the wide
+    // strides.  Measured on GB300 at 2^26: 224- and 288-thread blocks
+    // staging 17.5-18 KiB instead of 14-13.5 lost 3-8% on 16-bit elements
+    // (the shared memory then crowds out the L1 the loads in flight use),
+    // while 352- and 416-thread blocks staging 16.5-19.5 KiB instead of
+    // 11-13 gained 4-7% (s = 11, 13, 22, 26) on both element sizes.
+    static constexpr int kTargetBytes = S >= 32 ? 32768 : kThreads >= 352 ? 20480 : 16384;
     static constexpr int kWarps = kThreads / 32;
     static constexpr int kWarpsPerLap = S >= kWarps ? 1 : kWarps / S;
-    // loads per thread: about 16 KiB of span, with each warp's share of a run
-    // a whole number of warp-wide 4-byte words
+    // loads per thread: about kTargetBytes of span, with each warp's share of
+    // a run a whole number of warp-wide 4-byte words
     static constexpr int kRunAlign = E == 2 ? 64 : 32;
     static constexpr int loads_for(int l) {
         return (l * kPerVec * kThreads / S) % (kRunAlign * kWarpsPerLap) == 0 ? l : loads_for(l + 1);

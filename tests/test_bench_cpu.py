@@ -279,3 +279,19 @@ def test_l2_resident_entries_carry_no_hbm_fraction():
     assert small["l2_resident"] is True and "frac" not in small and small["gbps"] > 10000
     big = aux._speed(402653184, 57e-6)
     assert "l2_resident" not in big and 1.0 < big["frac"] < 1.2
+
+
+def test_gathers_are_compared_with_the_copy_of_their_own_dtype():
+    out = {"copy_f32_2p26": {"gbps": 6500.0}, "copy_bf16_2p26": {"gbps": 6000.0},
+           "gather12_f32_2p26": {"gbps": 6337.0},
+           "gather2_bf16_2p26": {"gbps": 5980.0},
+           "gather2_f32_2p26_index_order": {"gbps": 4680.0},
+           "gather3_bf16_2p26": {"parity": "MISMATCH"},  # no speed: no fraction
+           "add_f32_2p28": {"gbps": 7160.0}}
+    bench.add_copy_fractions(out)
+    assert out["gather12_f32_2p26"]["frac_of_copy_same_n"] == 6337.0 / 6500.0
+    assert out["gather2_bf16_2p26"]["frac_of_copy_same_n"] == 5980.0 / 6000.0
+    assert out["gather2_f32_2p26_index_order"]["frac_of_copy_same_n"] == 4680.0 / 6500.0
+    assert "frac_of_copy_same_n" not in out["gather3_bf16_2p26"]
+    assert "frac_of_copy_same_n" not in out["add_f32_2p28"]
+    assert "frac_of_copy_same_n" not in out["copy_f32_2p26"]

@@ -11,6 +11,8 @@ stride-2 gather at 2^26; and the bench's further workloads: bf16 add at
 stride-16 gather at 2^26.
 The bar is bit-exact; NaN results of arithmetic compare as "both NaN".
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -273,16 +275,14 @@ def _gather_laps(n, s):
     return 2 <= sm <= 64 and n <= 1 << 32 and n // sm >= LAP_BLOCK
 
 
-def _gather_auto_schedule(n, s, dtype, in_aligned16=False):
-    """The schedule AUTO picks: tiled from s = 5 up to 64, and for 2-byte
-    elements at s = 2 to 4 on an input aligned to 16 bytes; lap order below
-    that where every lap holds a block, else index order."""
+def _gather_auto_schedule(n, s, dtype):
+    """The schedule AUTO picks: tiled up to s = 64, from s = 5 for 4-byte
+    elements and from s = 2 for 2-byte ones; lap order below that where
+    every lap holds a block, else index order."""
     sm = s % n
     if n > 1 << 32:
         return 2
-    if 5 <= sm <= 64:
-        return 4
-    if ESIZE[dtype] == 2 and in_aligned16 and sm in (2, 3, 4):
+    if (5 if ESIZE[dtype] == 4 else 2) <= sm <= 64:
         return 4
     return 3 if _gather_laps(n, s) else 1
 
@@ -801,12 +801,41 @@ def test_gather_tiled(dtype):
             assert bi.guards_intact() and bo.guards_intact()
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_gather_tiled_general_every_input_offset(dtype):
+    """The general tiled kernel stages each span with 16-byte loads from its
+    first 16-byte boundary and single elements around them: every input offset
+    within 16 bytes (offset 0 takes the specialised kernels where the stride
+    has one), strides with and without a specialised kernel, spans shorter
+    than the peeled head, spans clipped at n and ragged last blocks."""
+    L = ew.lib()
+    e = ESIZE[dtype]
+    ew.set_schedule("tiled")
+    try:
+        for s in (2, 3, 5, 12, 16, 17, 40, 63, 64):
+            for n in (s + 1, s + 2, s + 5, 4097, 70001, (1 << 18) + 3):
+                x = inputs.random_bits(n, dtype, 7300 + n + s)
+                want = oracle.gather_stride(x, s)
+                for in_off in range(16 // e):
+                    bi = GuardedBuffer(n, dtype, in_off).fill(x)
+                    bo = GuardedBuffer(n, dtype, 1)
+                    assert L.ew_gather_stride(DT_CODE[dtype], bi.view.data_ptr(), bo.view.data_ptr(),
+                                              n, s, _stream()) == 0
+                    rec = ew.last_launch()
+                    assert rec["schedule"] == 4 and rec["vec_bytes"] == 16, (n, s, in_off, rec)
+                    torch.cuda.synchronize()
+                    assert_bits_equal(bo.host(), want, dtype, False,
+                                      "tiled gather n=%d s=%d input offset %d" % (n, s, in_off))
+                    assert bi.guards_intact() and bo.guards_intact()
+    finally:
+        ew.set_schedule("auto")
+
+
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16", "i32"])
 def test_gather_auto_crossover(dtype):
-    """AUTO's choice around its crossovers: lap order below s = 5 (for 2-byte
-    elements except s = 2 to 4 on this aligned input), the tiled kernels from
-    there to 64 (powers of two take the specialised kernel), index order from
-    65; each against the oracle."""
+    """AUTO's choice around its crossovers: lap order below s = 5 for 4-byte
+    elements, the tiled kernels from there (from s = 2 for 2-byte elements)
+    to 64, index order from 65; each against the oracle."""
     L = ew.lib()
     ew.set_schedule("auto")
     n = 300_007
@@ -816,7 +845,7 @@ def test_gather_auto_crossover(dtype):
         bo = GuardedBuffer(n, dtype, 2)
         assert L.ew_gather_stride(DT_CODE[dtype], bi.view.data_ptr(), bo.view.data_ptr(), n, s, _stream()) == 0
         rec = ew.last_launch()
-        assert rec["schedule"] == _gather_auto_schedule(n, s, dtype if dtype != "i32" else "f32", True), (s, rec)
+        assert rec["schedule"] == _gather_auto_schedule(n, s, dtype if dtype != "i32" else "f32"), (s, rec)
         torch.cuda.synchronize()
         assert_bits_equal(bo.host(), oracle.gather_stride(x, s), "f32" if dtype == "i32" else dtype, False,
                           "auto gather %s s=%d" % (dtype, s))
@@ -1012,7 +1041,7 @@ def test_gather_tiled_pow2(dtype):
                     rec = ew.last_launch()
                     aligned = (in_off * e) % 16 == 0
                     assert rec["schedule"] == 4, (n, s, rec)
-                    assert rec["path"] == (2 if aligned else 1) and rec["vec_bytes"] == (16 if aligned else e), rec
+                    assert rec["path"] == 2 and rec["vec_bytes"] == 16, rec  # general kernel too: 16-byte staging
                     if aligned:
                         assert rec["grid"] == -(-(-(-n // s)) // (span // s)), (n, s, rec)
                     torch.cuda.synchronize()
@@ -1064,13 +1093,22 @@ def test_gather_random_cases(dtype):
     ew.set_schedule("auto")
 
 
-FIXED_STRIDES = (3, 5, 6, 7, 9, 10, 11, 12, 13, 14, 15, 24, 48)
+FIXED_STRIDES = (3, 5, 6, 7, 9, 10, 11, 12, 13, 14, 15, 18, 20, 22, 24, 26, 28, 30, 40, 48, 52, 56, 60)
+
+
+def _fixed_block(s, e):
+    """Threads per block of the fixed-stride kernel: the smallest multiple of
+    lcm(32, s / gcd(s, V)) from 192 (384 from s = 32), V = 16 / e."""
+    base = math.lcm(32, s // math.gcd(s, 16 // e))
+    least = 384 if s >= 32 else 192
+    return -(-least // base) * base
 
 
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16", "i32"])
 def test_gather_tiled_fixed_strides(dtype):
     """The tiled gather specialised for fixed strides that are not powers of
-    two (3, 5-7, 9-15, 24, 48, and strides congruent to them mod n) on a
+    two (3, 5-7, 9-15, 18-30 even, 40, 48, 52, 56, 60, and strides congruent
+    to them mod n) on a
     16-byte aligned input, with the block size chosen per stride: one ragged
     block, one and several full spans, spans plus a ragged block, n divisible
     by the stride and not, output offsets that start laps on odd and even
@@ -1092,9 +1130,8 @@ def test_gather_tiled_fixed_strides(dtype):
                     rec = ew.last_launch()
                     aligned = (in_off * e) % 16 == 0
                     assert rec["schedule"] == 4, (n, s, rec)
-                    assert rec["path"] == (2 if aligned else 1) and rec["vec_bytes"] == (16 if aligned else e), rec
-                    assert (rec["block"] % 96 == 0 or rec["block"] % 160 == 0 or rec["block"] % 224 == 0
-                            or rec["block"] >= 288) if aligned else rec["block"] == 256, rec
+                    assert rec["path"] == 2 and rec["vec_bytes"] == 16, rec  # general kernel too: 16-byte staging
+                    assert rec["block"] == (_fixed_block(s, e) if aligned else 256), rec
                     torch.cuda.synchronize()
                     assert_bits_equal(bo.host(), oracle.gather_stride(x, stride), bits, False,
                                       "fixed tiled gather %s n=%d s=%d offs=%d,%d"
