@@ -151,9 +151,7 @@ typedef enum {
  *                     all s laps draw from (12-20 KiB) once, coalesced, into
  *                     shared memory with one row per residue mod s, then
  *                     writes each lap's outputs as one coalesced run.  For
- *                     s = 2, 4, ..., 64 (powers of two) and s = 3, 5, 6, 7,
- *                     9 to 15, the even strides 18 to 30, 40, 48, 52, 56
- *                     and 60 on an input aligned to 16 bytes a
+ *                     every s from 2 to 64 on an input aligned to 16 bytes a
  *                     kernel specialised for that stride runs (division by
  *                     s at compile time, staging stores at fixed offsets, a
  *                     padded shared-memory layout, warps copying whole lap

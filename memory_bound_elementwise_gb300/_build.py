@@ -22,7 +22,7 @@ LIB = os.path.join(OUT_DIR, "libew.so")
 OBJ_DIR = os.path.join(OUT_DIR, "obj")
 
 SOURCES = ["ew_api.cu", "ew_kernels_f32.cu", "ew_kernels_f16.cu", "ew_kernels_bf16.cu", "ew_tma.cu",
-           "ew_gather_fixed.cu"]
+           "ew_gather_fixed.cu", "ew_gather_fixed_wide.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
               "-ftz=false", "-prec-div=true", "-prec-sqrt=true", "-fmad=false",

@@ -284,10 +284,10 @@ uint32_t fixed_pad_elems(int e, uint32_t s, uint32_t p, uint32_t threads) {
     uint32_t best_pad = 0, best = ~0u;
     for (uint32_t pad = 0; pad < 32; pad += step) {
         uint32_t worst = 0;
-        for (uint32_t w = 0; w < threads / 32; ++w) {
+        for (uint32_t w = 0; 32 * w < threads; ++w) {  // a partial last warp too
             for (uint32_t k = 0; k < v; ++k) {
                 uint32_t words[32], nw = 0, per_bank[32] = {};
-                for (uint32_t t = 0; t < 32; ++t) {
+                for (uint32_t t = 0; t < 32 && 32 * w + t < threads; ++t) {
                     const uint32_t j = v * (32 * w + t) + k;
                     const uint32_t word = ((j % s) * (p + pad) + j / s) * static_cast<uint32_t>(e) / 4;
                     bool seen = false;
@@ -565,11 +565,10 @@ GatherLaunch plan_gather_span(const void *in, void *out, uint64_t n, uint64_t s_
 // Tiled kernels: P positions of every lap per block, the input span they
 // draw from staged in shared memory, rows padded.  On a 16-byte aligned input
 // a power-of-two stride (2 to 64) takes the kernel specialised for it, and
-// the strides of the fixed-stride set (3, 5-7, 9-15, the even strides 18-30,
-// 40, 48, 52, 56, 60) the fixed-stride kernel; any other stride, or an
-// unaligned input, the general kernel (P a power of two, span up to 20 KiB
-// unless that leaves lap runs under 512 bytes).  All stage with 16-byte loads
-// (the launch record shows EW_PATH_V128 and vec_bytes 16).
+// every other stride (3 to 63) the fixed-stride kernel; an unaligned input
+// the general kernel (P a power of two, span up to 20 KiB unless that leaves
+// lap runs under 512 bytes).  All stage with 16-byte loads (the launch record
+// shows EW_PATH_V128 and vec_bytes 16).
 GatherLaunch plan_gather_tiled(int e, const void *in, void *out, uint64_t n, uint64_t s_mod) {
     GatherLaunch gl;
     const GatherEntry *pow2 = e == 4 ? gather_tiled_pow2_4(s_mod) : gather_tiled_pow2_2(s_mod);

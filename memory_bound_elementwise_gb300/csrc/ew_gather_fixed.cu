@@ -1,16 +1,15 @@
 // ew_gather_fixed.cu -- instantiations of the fixed-stride tiled gather for
-// strides that are not powers of two (both element sizes), in a translation
-// unit of their own so that the build compiles them in parallel with the rest.
+// strides below 32 that are not powers of two (both element sizes), in a
+// translation unit of their own so that the build compiles them in parallel
+// with the rest; ew_gather_fixed_wide.cu holds the strides from 33.
 #include "ew_kernels.cuh"
 
 namespace ew {
 
 namespace {
-// Every stride up to 64 that is not a power of two and whose block fits the
-// kernel's rule (at most 512 threads with V*T a multiple of the stride).
-#define EW_FIXED_STRIDES(X)                                                                       \
-    X(3) X(5) X(6) X(7) X(9) X(10) X(11) X(12) X(13) X(14) X(15) X(18) X(20) X(22) X(24) X(26) \
-    X(28) X(30) X(40) X(48) X(52) X(56) X(60)
+#define EW_FIXED_STRIDES(X)                                                                        \
+    X(3) X(5) X(6) X(7) X(9) X(10) X(11) X(12) X(13) X(14) X(15) X(17) X(18) X(19) X(20) X(21) \
+    X(22) X(23) X(24) X(25) X(26) X(27) X(28) X(29) X(30) X(31)
 #define EW_ENTRY4(S) tiled_fixed_entry<4, S>(),
 #define EW_ENTRY2(S) tiled_fixed_entry<2, S>(),
 #define EW_STRIDE(S) S,
@@ -23,7 +22,9 @@ constexpr uint64_t kFixedStrides[] = {EW_FIXED_STRIDES(EW_STRIDE)};
 #undef EW_FIXED_STRIDES
 }  // namespace
 
+// Every stride from 3 to 63 that is not a power of two.
 const GatherEntry *gather_tiled_fixed(int e, uint64_t stride) {
+    if (stride > 32) return gather_tiled_fixed_wide(e, stride);
     for (size_t k = 0; k < sizeof(kFixedStrides) / sizeof(kFixedStrides[0]); ++k)
         if (kFixedStrides[k] == stride) return e == 4 ? &kFixed4[k] : &kFixed2[k];
     return nullptr;

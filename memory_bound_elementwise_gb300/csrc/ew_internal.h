@@ -128,11 +128,12 @@ constexpr int kTiledPow2Threads = 256;
 const GatherEntry *gather_tiled_pow2_4(uint64_t stride);
 const GatherEntry *gather_tiled_pow2_2(uint64_t stride);
 // Tiled gather specialised for a fixed stride that is not a power of two
-// (3, 5, 6, 7, 9 to 15, the even strides 18 to 30, 40, 48, 52, 56, 60) and
-// an input aligned to 16 bytes; the block
+// (every stride from 3 to 63 but 4, 8, 16, 32) and an input aligned to 16
+// bytes; the block
 // size is chosen per stride, the row pitch (args.tile_pitch) by the host.
 // nullptr for other strides.
 const GatherEntry *gather_tiled_fixed(int e, uint64_t stride);
+const GatherEntry *gather_tiled_fixed_wide(int e, uint64_t stride);  // strides 33 to 63
 const GatherEntry *gather_oneshot_4();  // binary32, n <= 2^32
 const GatherEntry *gather_stride_4();   // binary32, any n
 const GatherEntry *gather_oneshot_2();  // 16-bit types

@@ -636,10 +636,11 @@ namespace ew {
 // by V*T/S per load.  So each thread works out, once, the shared-memory
 // offset of each of its V elements, and every load's elements go to those
 // offsets plus a compile-time step.  T is the smallest multiple of
-// lcm(32, S / gcd(S, V)) from 192 threads (384 from S = 32); a block stages
-// about 16 KiB of input (20 KiB for blocks of 352 threads or more, 32 KiB
-// from S = 32 so that lap runs stay long; the span is kLoads*V*T elements,
-// P = span / S positions per lap).
+// lcm(32, S / gcd(S, V)) from 192 threads (384 from S = 32) when that is at
+// most 512; otherwise a multiple of S / gcd(S, V) with a partial last warp.
+// A block stages about 16 KiB of input (20 KiB for blocks of 352 threads or
+// more, 32 KiB from S = 32 so that lap runs stay long; the span is
+// kLoads*V*T elements, P = span / S positions per lap).
 // The row pitch comes from the host (tile_pitch), chosen for the bank spread
 // of these stores; the rows live in dynamic shared memory.  The store phase
 // is the power-of-two kernel's: warps share out the lap runs.
@@ -650,10 +651,12 @@ constexpr int lcm_int(int a, int b) { return a / gcd_int(a, b) * b; }
 template <int E, int S>
 struct TiledFixed {
     static constexpr int kPerVec = 16 / E;
-    static constexpr int kBase = lcm_int(32, S / gcd_int(S, kPerVec));
+    // A thread's rows stay fixed across its loads when V*T is a multiple of
+    // S, i.e. when T is a multiple of kRowPeriod.
+    static constexpr int kRowPeriod = S / gcd_int(S, kPerVec);
     // wide strides: bigger blocks and spans, so that lap runs stay long
     static constexpr int kMinThreads = S >= 32 ? 384 : 192;
-    static constexpr int kThreads = ((kMinThreads + kBase - 1) / kBase) * kBase;
+    static constexpr int kRunAlign = E == 2 ? 64 : 32;
     // Span per block: 16 KiB for blocks of up to 320 threads (6 to 10 per
     // SM), 20 KiB for the larger ones (4 or 5 per SM), 32 KiB for the wide
     // strides.  Measured on GB300 at 2^26: 224- and 288-thread blocks
@@ -661,23 +664,51 @@ struct TiledFixed {
     // (the shared memory then crowds out the L1 the loads in flight use),
     // while 352- and 416-thread blocks staging 16.5-19.5 KiB instead of
     // 11-13 gained 4-7% (s = 11, 13, 22, 26) on both element sizes.
-    static constexpr int kTargetBytes = S >= 32 ? 32768 : kThreads >= 352 ? 20480 : 16384;
-    static constexpr int kWarps = kThreads / 32;
-    static constexpr int kWarpsPerLap = S >= kWarps ? 1 : kWarps / S;
-    // loads per thread: about kTargetBytes of span, with each warp's share of
-    // a run a whole number of warp-wide 4-byte words
-    static constexpr int kRunAlign = E == 2 ? 64 : 32;
-    static constexpr int loads_for(int l) {
-        return (l * kPerVec * kThreads / S) % (kRunAlign * kWarpsPerLap) == 0 ? l : loads_for(l + 1);
+    static constexpr int target_bytes(int t) { return S >= 32 ? 32768 : t >= 352 ? 20480 : 16384; }
+    static constexpr int warps_per_lap(int t) { return S >= t / 32 ? 1 : (t / 32) / S; }
+    // loads per thread: from about target_bytes of span up, the first count
+    // that gives each warp's share of a run a whole number of warp-wide
+    // 4-byte words (-1 if none up to 64)
+    static constexpr int loads_from(int t, int l) {
+        return l > 64 ? -1
+                      : (l * kPerVec * t / S) % (kRunAlign * warps_per_lap(t)) == 0 ? l : loads_from(t, l + 1);
     }
-    static constexpr int kLoadsWanted = kTargetBytes / (16 * kThreads) > 0 ? kTargetBytes / (16 * kThreads) : 1;
-    static constexpr int kLoads = loads_for(kLoadsWanted);
+    static constexpr int loads_for(int t) {
+        return loads_from(t, target_bytes(t) / (16 * t) > 0 ? target_bytes(t) / (16 * t) : 1);
+    }
+    // Threads: the smallest multiple of lcm(32, kRowPeriod) from kMinThreads
+    // (whole warps), if that is at most 512.  Otherwise (odd strides from 17,
+    // and 34-62 where 4 or 8 does not divide them) a multiple of kRowPeriod
+    // up to 512 whose span comes nearest its target, whole warps breaking
+    // ties; the last warp is then partial and takes part in the staging only.
+    static constexpr int kWholeWarps = (kMinThreads + lcm_int(32, kRowPeriod) - 1) / lcm_int(32, kRowPeriod) *
+                                       lcm_int(32, kRowPeriod);
+    static constexpr int deviation(int t) {
+        return loads_for(t) < 0 ? 1 << 30
+                                : (loads_for(t) * 16 * t > target_bytes(t) ? loads_for(t) * 16 * t - target_bytes(t)
+                                                                            : target_bytes(t) - loads_for(t) * 16 * t);
+    }
+    static constexpr int pick_threads() {
+        if (kWholeWarps <= 512) return kWholeWarps;
+        int best = 0;
+        for (int t = (kMinThreads + kRowPeriod - 1) / kRowPeriod * kRowPeriod; t <= 512; t += kRowPeriod) {
+            if (best == 0 || deviation(t) < deviation(best) ||
+                (deviation(t) == deviation(best) && t % 32 == 0 && best % 32 != 0))
+                best = t;
+        }
+        return best;
+    }
+    static constexpr int kThreads = pick_threads();
+    static constexpr int kWarps = kThreads / 32;  // whole warps: the store phase
+    static constexpr int kWarpsPerLap = warps_per_lap(kThreads);
+    static constexpr int kLoads = loads_for(kThreads);
     static constexpr int kSpan = kLoads * kPerVec * kThreads;  // elements
     static constexpr int kP = kSpan / S;
     static constexpr int kColStep = kPerVec * kThreads / S;
     static constexpr int kSeg = kP / kWarpsPerLap;
     static constexpr int kWraps = (kPerVec - 1) / S + 1;  // row wraps within one load, at most
-    static_assert(kThreads <= 512 && kThreads >= S, "block size");
+    static_assert(kThreads <= 512 && kThreads >= S && kWarps >= 1, "block size");
+    static_assert(kLoads >= 1 && deviation(kThreads) < (1 << 30), "span");
     static_assert((kPerVec * kThreads) % S == 0 && kSpan % S == 0, "rows invariant across a thread's loads");
     static_assert(kSeg % kRunAlign == 0, "whole warp-wide words per run share");
 };
@@ -738,8 +769,11 @@ __global__ void __launch_bounds__(TiledFixed<E, S>::kThreads) gather_tiled_fixed
     }
     __syncthreads();
     const uint32_t lane = threadIdx.x & 31u;
-    for (uint32_t item = threadIdx.x >> 5; item < static_cast<uint32_t>(S * T::kWarpsPerLap);
-         item += T::kWarps) {
+    // whole warps only: a partial last warp (T not a multiple of 32) has
+    // done its share in the staging
+    const uint32_t warp = threadIdx.x >> 5;
+    const uint32_t items = static_cast<uint32_t>(S * T::kWarpsPerLap);
+    for (uint32_t item = warp; warp < T::kWarps && item < items; item += T::kWarps) {
         const uint32_t L = item / T::kWarpsPerLap, q0 = (item % T::kWarpsPerLap) * T::kSeg;
         const W *row = tile + lap_row[L] + q0;
         W *dst = out + (static_cast<size_t>(lap_start[L]) + p0 + q0);

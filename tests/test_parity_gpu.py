@@ -1093,22 +1093,45 @@ def test_gather_random_cases(dtype):
     ew.set_schedule("auto")
 
 
-FIXED_STRIDES = (3, 5, 6, 7, 9, 10, 11, 12, 13, 14, 15, 18, 20, 22, 24, 26, 28, 30, 40, 48, 52, 56, 60)
+FIXED_STRIDES = tuple(s for s in range(3, 64) if s & (s - 1))  # every stride up to 63 but the powers of two
 
 
 def _fixed_block(s, e):
-    """Threads per block of the fixed-stride kernel: the smallest multiple of
-    lcm(32, s / gcd(s, V)) from 192 (384 from s = 32), V = 16 / e."""
-    base = math.lcm(32, s // math.gcd(s, 16 // e))
+    """Threads per block of the fixed-stride kernel.  T must be a multiple of
+    the row period s / gcd(s, V) (V = 16 / e elements per load).  Whole warps:
+    the smallest multiple of lcm(32, period) from 192 (384 from s = 32) if at
+    most 512; else the multiple of the period up to 512 whose span (loads per
+    thread x 16 x T, from the target up until each warp's run share is whole
+    4-byte words) comes nearest the target, whole warps breaking ties."""
+    v = 16 // e
+    period = s // math.gcd(s, v)
     least = 384 if s >= 32 else 192
-    return -(-least // base) * base
+    lcm = math.lcm(32, period)
+    whole = -(-least // lcm) * lcm
+    if whole <= 512:
+        return whole
+
+    def deviation(t):
+        target = 32768 if s >= 32 else 20480 if t >= 352 else 16384
+        wpl = 1 if s >= t // 32 else (t // 32) // s
+        align = 64 if e == 2 else 32
+        for loads in range(max(target // (16 * t), 1), 65):
+            if (loads * v * t // s) % (align * wpl) == 0:
+                return abs(loads * 16 * t - target)
+        return 1 << 30
+    best = None
+    for t in range(-(-least // period) * period, 513, period):
+        if best is None or deviation(t) < deviation(best) or (
+                deviation(t) == deviation(best) and t % 32 == 0 and best % 32 != 0):
+            best = t
+    return best
 
 
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16", "i32"])
 def test_gather_tiled_fixed_strides(dtype):
     """The tiled gather specialised for fixed strides that are not powers of
-    two (3, 5-7, 9-15, 18-30 even, 40, 48, 52, 56, 60, and strides congruent
-    to them mod n) on a
+    two (every stride from 3 to 63 but 4, 8, 16, 32, and strides congruent to
+    them mod n) on a
     16-byte aligned input, with the block size chosen per stride: one ragged
     block, one and several full spans, spans plus a ragged block, n divisible
     by the stride and not, output offsets that start laps on odd and even
