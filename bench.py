@@ -1311,10 +1311,31 @@ def run_ours(args):
         e2e_total, e2e_serial_total, e2e_piped_total = float(t[0]), float(t[1]), float(t[2])
     e2e_value = metrics.gbps(step_bytes * e2e_steps * world, e2e_total)
     e2e_ok = bool(torch.equal(c_pin, c.cpu())) and piped_ok
+
+    # the CPU-GPU link's own ceiling in this run: copy-engine transfers of the
+    # same pinned buffers host to device, device to host, and both at once
+    def link_step(up, down):
+        start = torch.cuda.Event()
+        start.record(stream)
+        for side, go, dst, src in ((h2d, up, a_d, a_pin), (d2h, down, c_pin, c_d)):
+            if go:
+                side.wait_event(start)
+                with torch.cuda.stream(side):
+                    dst.copy_(src, non_blocking=True)
+                joined = torch.cuda.Event()
+                joined.record(side)
+                stream.wait_event(joined)
+    link = {}
+    for name, up, down, per in (("h2d", True, False, 4 * n), ("d2h", False, True, 4 * n), ("both", True, True, 8 * n)):
+        tot, _ = time_launches(torch, stream, lambda up=up, down=down: link_step(up, down), 5, 1)
+        link[name + "_gbps"] = metrics.gbps(per * 5, tot)
     e2e = {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": 8 * n, "d2h_bytes_per_step": 4 * n,
            "steps": e2e_steps, "result_matches_device": e2e_ok,
            "how": "ew_add on pinned host A, B, C: the kernel reads 8N bytes from and writes 4N bytes "
-                  "to host memory over the CPU-GPU link every step"}
+                  "to host memory over the CPU-GPU link every step",
+           "link": dict(link, how="cudaMemcpyAsync of the same pinned 1 GiB buffers, one direction and "
+                                  "both at once on two streams, in this run"),
+           "frac_of_link_both": e2e_value / link["both_gbps"]}
     e2e_staged = {"staged_pipelined_gbps": metrics.gbps(step_bytes * e2e_steps * world, e2e_piped_total),
                   "staged_pipelined_how": "cudaMemcpyAsync H2D of A, B, ew_add on device copies, D2H of C, "
                                           "in %d chunks overlapped on three streams" % len(spans),

@@ -35,4 +35,7 @@ def test_bench_headline_is_the_last_line_and_checked():
     e2e = head["e2e"]
     assert e2e["h2d_bytes_per_step"] == 8 * n and e2e["d2h_bytes_per_step"] == 4 * n
     assert e2e["value"] > 0 and e2e["result_matches_device"] is True
+    link = e2e["link"]
+    assert 0 < link["h2d_gbps"] and 0 < link["d2h_gbps"] and 0 < link["both_gbps"]
+    assert e2e["frac_of_link_both"] == pytest.approx(e2e["value"] / link["both_gbps"])
     assert head["clocks"]["sm_mhz"] is None or head["clocks"]["sm_mhz"] > 0
