@@ -105,6 +105,8 @@ def parse(argv=None):
     p.add_argument("--stride", type=int, default=None, help="gather stride for the gather profile cases")
     p.add_argument("--ab-strides", default=None,
                    help="gather A/B: comma-separated strides, each on an aligned input and one element past it")
+    p.add_argument("--ab-offsets", default="0,1",
+                   help="gather A/B: comma-separated input offsets in elements (default 0,1)")
     p.add_argument("--ab", default=None, choices=["widths", "gather"],
                    help="A/B timing instead of the benchmark: access widths, or gather schedules by stride")
     return p.parse_args(argv)
@@ -1082,7 +1084,7 @@ def run_ab_gather(args):
     plan = [(0, [2, 3, 4, 5, 6, 7, 8, 12, 16, 17, 24, 32, 40, 48, 63, 64]), (1, [2, 3, 4, 5, 12, 16, 40])]
     if args.ab_strides or args.stride:
         chosen = [int(v) for v in args.ab_strides.split(",")] if args.ab_strides else [args.stride]
-        plan = [(0, chosen), (1, chosen)]
+        plan = [(int(o), chosen) for o in args.ab_offsets.split(",")]
     for dtype, (offset, strides) in ((d, p) for d in ("f32", "bf16") for p in plan):
         code = DT_CODE[dtype]
         x = inputs.as_dtype(inputs.uniform(n, inputs.seed_for("copy_f32"), 0.0, 1.0), dtype)
