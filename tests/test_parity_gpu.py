@@ -1067,6 +1067,28 @@ def test_gather_pow2_full_size_2p26(dtype, s):
     assert bo.guards_intact() and bi.guards_intact()
 
 
+@pytest.mark.parametrize("dtype,s,in_off", [("f32", 63, 0), ("bf16", 33, 0), ("bf16", 6, 0), ("f32", 12, 0),
+                                           ("f32", 40, 1), ("bf16", 17, 3)])
+def test_gather_fixed_and_general_full_size_2p26(dtype, s, in_off):
+    """The fixed-stride kernel at n = 2^26 (s = 63 and 33 with a partial last
+    warp, s = 6 and 12 with the larger register allowance) and the general
+    kernel on inputs 1 and 3 elements past 16 bytes: every output against the
+    oracle, with the block size the launch record reports."""
+    n = 1 << 26
+    e = ESIZE[dtype]
+    x = inputs.as_dtype(inputs.uniform(n, inputs.seed_for("copy_f32", 5), 0.0, 1.0), dtype)
+    bi, bo = GuardedBuffer(n, dtype, in_off).fill(x), GuardedBuffer(n, dtype)
+    assert ew.lib().ew_gather_stride(DT_CODE[dtype], bi.view.data_ptr(), bo.view.data_ptr(), n, s,
+                                     _stream()) == 0
+    rec = ew.last_launch()
+    assert rec["schedule"] == 4 and rec["path"] == 2, rec
+    assert rec["block"] == (_fixed_block(s, e) if (in_off * e) % 16 == 0 else 256), rec
+    torch.cuda.synchronize()
+    assert_bits_equal(bo.host(), oracle.gather_stride(x, s), dtype, False,
+                      "gather %d 2^26 %s offset %d" % (s, dtype, in_off))
+    assert bo.guards_intact() and bi.guards_intact()
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16", "i32"])
 def test_gather_random_cases(dtype):
     """Seeded random gathers across every schedule: sizes from 1 to 2^20 + 999
