@@ -148,15 +148,17 @@ typedef enum {
  * EW_SCHED_TILED      gather only, same range of s and n as EW_SCHED_LAPS (any
  *                     n >= 1 there): the transpose-like schedule.  A block
  *                     reads the contiguous input span that its positions of
- *                     all s laps draw from (12-20 KiB) once, coalesced, into
+ *                     all s laps draw from (12-32 KiB) once, coalesced, into
  *                     shared memory with one row per residue mod s, then
  *                     writes each lap's outputs as one coalesced run.  For
- *                     every s from 2 to 64 on an input aligned to 16 bytes a
- *                     kernel specialised for that stride runs (division by
- *                     s at compile time, staging stores at fixed offsets, a
- *                     padded shared-memory layout, warps copying whole lap
- *                     runs; the launch record shows EW_PATH_V128 and the
- *                     block size chosen for the stride).
+ *                     every s from 2 to 64 on an input aligned to 16 bytes,
+ *                     and for the s that are not powers of two on any
+ *                     input, a kernel specialised for that stride runs
+ *                     (division by s at compile time, staging stores at
+ *                     fixed offsets, a padded shared-memory layout, warps
+ *                     copying whole lap runs; the launch record shows
+ *                     EW_PATH_V128 and the block size chosen for the
+ *                     stride).
  * EW_SCHED_AUTO       for the gather: EW_SCHED_LAPS for s < 5, EW_SCHED_TILED
  *                     for 5 <= s <= 64 (the measured crossover: a
  *                     lap-ordered warp load fetches more sectors per useful

@@ -564,11 +564,12 @@ GatherLaunch plan_gather_span(const void *in, void *out, uint64_t n, uint64_t s_
 
 // Tiled kernels: P positions of every lap per block, the input span they
 // draw from staged in shared memory, rows padded.  On a 16-byte aligned input
-// a power-of-two stride (2 to 64) takes the kernel specialised for it, and
-// every other stride (3 to 63) the fixed-stride kernel; an unaligned input
-// the general kernel (P a power of two, span up to 20 KiB unless that leaves
-// lap runs under 512 bytes).  All stage with 16-byte loads (the launch record
-// shows EW_PATH_V128 and vec_bytes 16).
+// a power-of-two stride (2 to 64) takes the kernel specialised for it; every
+// other stride (3 to 63) takes the fixed-stride kernel on any input (its
+// shifted instance past a 16-byte boundary); a power-of-two stride on an
+// unaligned input the general kernel (P a power of two, span up to 20 KiB
+// unless that leaves lap runs under 512 bytes).  All stage with 16-byte
+// loads (the launch record shows EW_PATH_V128 and vec_bytes 16).
 GatherLaunch plan_gather_tiled(int e, const void *in, void *out, uint64_t n, uint64_t s_mod) {
     GatherLaunch gl;
     const GatherEntry *pow2 = e == 4 ? gather_tiled_pow2_4(s_mod) : gather_tiled_pow2_2(s_mod);
@@ -587,8 +588,10 @@ GatherLaunch plan_gather_tiled(int e, const void *in, void *out, uint64_t n, uin
         gl.nvec = static_cast<int64_t>(n);
         return gl;
     }
-    const GatherEntry *fixed = gather_tiled_fixed(e, s_mod);
-    if (fixed != nullptr && reinterpret_cast<uintptr_t>(in) % 16 == 0) {
+    // any element-aligned input: past a 16-byte boundary the shifted instance
+    // moves its loads to the boundaries
+    const GatherEntry *fixed = gather_tiled_fixed(e, s_mod, reinterpret_cast<uintptr_t>(in) % 16 != 0);
+    if (fixed != nullptr) {
         gl.entry = fixed;
         gl.args = gather_args(in, out, n, s_mod);
         gl.args.tile_p = fixed->tile_p;

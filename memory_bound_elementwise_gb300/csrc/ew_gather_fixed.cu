@@ -10,23 +10,30 @@ namespace {
 #define EW_FIXED_STRIDES(X)                                                                        \
     X(3) X(5) X(6) X(7) X(9) X(10) X(11) X(12) X(13) X(14) X(15) X(17) X(18) X(19) X(20) X(21) \
     X(22) X(23) X(24) X(25) X(26) X(27) X(28) X(29) X(30) X(31)
-#define EW_ENTRY4(S) tiled_fixed_entry<4, S>(),
-#define EW_ENTRY2(S) tiled_fixed_entry<2, S>(),
+#define EW_ENTRY4(S) tiled_fixed_entry<4, S, false>(),
+#define EW_ENTRY2(S) tiled_fixed_entry<2, S, false>(),
+#define EW_SHIFTED4(S) tiled_fixed_entry<4, S, true>(),
+#define EW_SHIFTED2(S) tiled_fixed_entry<2, S, true>(),
 #define EW_STRIDE(S) S,
 const GatherEntry kFixed4[] = {EW_FIXED_STRIDES(EW_ENTRY4)};
 const GatherEntry kFixed2[] = {EW_FIXED_STRIDES(EW_ENTRY2)};
+const GatherEntry kShifted4[] = {EW_FIXED_STRIDES(EW_SHIFTED4)};  // input past a 16-byte boundary
+const GatherEntry kShifted2[] = {EW_FIXED_STRIDES(EW_SHIFTED2)};
 constexpr uint64_t kFixedStrides[] = {EW_FIXED_STRIDES(EW_STRIDE)};
 #undef EW_ENTRY4
 #undef EW_ENTRY2
+#undef EW_SHIFTED4
+#undef EW_SHIFTED2
 #undef EW_STRIDE
 #undef EW_FIXED_STRIDES
 }  // namespace
 
 // Every stride from 3 to 63 that is not a power of two.
-const GatherEntry *gather_tiled_fixed(int e, uint64_t stride) {
-    if (stride > 32) return gather_tiled_fixed_wide(e, stride);
+const GatherEntry *gather_tiled_fixed(int e, uint64_t stride, bool shifted) {
+    if (stride > 32) return gather_tiled_fixed_wide(e, stride, shifted);
     for (size_t k = 0; k < sizeof(kFixedStrides) / sizeof(kFixedStrides[0]); ++k)
-        if (kFixedStrides[k] == stride) return e == 4 ? &kFixed4[k] : &kFixed2[k];
+        if (kFixedStrides[k] == stride)
+            return shifted ? (e == 4 ? &kShifted4[k] : &kShifted2[k]) : (e == 4 ? &kFixed4[k] : &kFixed2[k]);
     return nullptr;
 }
 

@@ -132,8 +132,9 @@ const GatherEntry *gather_tiled_pow2_2(uint64_t stride);
 // bytes; the block
 // size is chosen per stride, the row pitch (args.tile_pitch) by the host.
 // nullptr for other strides.
-const GatherEntry *gather_tiled_fixed(int e, uint64_t stride);
-const GatherEntry *gather_tiled_fixed_wide(int e, uint64_t stride);  // strides 33 to 63
+// shifted: the instance for an input that is not 16-byte aligned.
+const GatherEntry *gather_tiled_fixed(int e, uint64_t stride, bool shifted);
+const GatherEntry *gather_tiled_fixed_wide(int e, uint64_t stride, bool shifted);  // strides 33 to 63
 const GatherEntry *gather_oneshot_4();  // binary32, n <= 2^32
 const GatherEntry *gather_stride_4();   // binary32, any n
 const GatherEntry *gather_oneshot_2();  // 16-bit types

@@ -658,13 +658,17 @@ struct TiledFixed {
     static constexpr int kMinThreads = S >= 32 ? 384 : 192;
     static constexpr int kRunAlign = E == 2 ? 64 : 32;
     // Span per block: 16 KiB for blocks of up to 320 threads (6 to 10 per
-    // SM), 20 KiB for the larger ones (4 or 5 per SM), 32 KiB for the wide
-    // strides.  Measured on GB300 at 2^26: 224- and 288-thread blocks
-    // staging 17.5-18 KiB instead of 14-13.5 lost 3-8% on 16-bit elements
-    // (the shared memory then crowds out the L1 the loads in flight use),
-    // while 352- and 416-thread blocks staging 16.5-19.5 KiB instead of
-    // 11-13 gained 4-7% (s = 11, 13, 22, 26) on both element sizes.
-    static constexpr int target_bytes(int t) { return S >= 32 ? 32768 : t >= 352 ? 20480 : 16384; }
+    // SM), 20 KiB for 352 to 448 threads (4 or 5 per SM), 24 KiB for 480,
+    // 32 KiB for the wide strides.  Measured on GB300 at 2^26: 224- and
+    // 288-thread blocks staging 17.5-18 KiB instead of 14-13.5 lost 3-8% on
+    // 16-bit elements (the shared memory then crowds out the L1 the loads in
+    // flight use), while 352- and 416-thread blocks staging 16.5-19.5 KiB
+    // instead of 11-13 gained 4-7% (s = 11, 13, 22, 26) on both element
+    // sizes, and 480-thread blocks (s = 15, 30) 22.5 KiB instead of 15 gained
+    // 3-5% (7% on an input past a 16-byte boundary).
+    static constexpr int target_bytes(int t) {
+        return S >= 32 ? 32768 : t >= 480 ? 24576 : t >= 352 ? 20480 : 16384;
+    }
     static constexpr int warps_per_lap(int t) { return S >= t / 32 ? 1 : (t / 32) / S; }
     // loads per thread: from about target_bytes of span up, the first count
     // that gives each warp's share of a run a whole number of warp-wide
@@ -721,7 +725,7 @@ struct TiledFixed {
     static_assert(kSeg % kRunAlign == 0, "whole warp-wide words per run share");
 };
 
-template <int E, int S>
+template <int E, int S, bool kShifted>
 __global__ void __launch_bounds__(TiledFixed<E, S>::kThreads, TiledFixed<E, S>::kMinBlocks)
 gather_tiled_fixed_kernel(const GatherArgs g) {
     enter_grid();
@@ -744,33 +748,62 @@ gather_tiled_fixed_kernel(const GatherArgs g) {
     const uint64_t j0 = static_cast<uint64_t>(S) * p0;  // first source of the span
     const W *src = static_cast<const W *>(g.in) + j0;
     const bool full = j0 + T::kSpan <= g.n;              // block-uniform
+    // An input d elements past a 16-byte boundary (the kShifted instances):
+    // every span starts d elements past one too (a span is a whole number of
+    // 16-byte loads), so the loads are shifted back by d.  Load i of thread t
+    // then holds span elements V*(t + T*i) + k - d, still in rows fixed
+    // across i.  Thread 0's first load would start before the span and is
+    // skipped; the V elements not covered (the valid part of that load and
+    // the span's last d) are staged singly.  The aligned instances compile
+    // with d = 0, without that work.
+    const uint32_t d = kShifted ? (static_cast<uint32_t>(reinterpret_cast<uintptr_t>(g.in)) & 15u) / E : 0u;
     if (full) {
-        const char *src_bytes = reinterpret_cast<const char *>(src);
+        const char *src_bytes = reinterpret_cast<const char *>(src) - d * E;
         Vec<16> v[T::kLoads];
 #pragma unroll
-        for (int i = 0; i < T::kLoads; ++i) v[i] = ld<16>(src_bytes + (threadIdx.x + i * T::kThreads) * 16u);
-        // offsets of this thread's V elements (rows fixed across its loads)
-        const uint32_t j = T::kPerVec * threadIdx.x;
-        const uint32_t r0 = j % S, c0 = j / S;
+        for (int i = 0; i < T::kLoads; ++i)
+            if (!kShifted || i > 0 || d == 0 || threadIdx.x > 0)
+                v[i] = ld<16>(src_bytes + (threadIdx.x + i * T::kThreads) * 16u);
+        // offsets of this thread's V elements in its first load (rows fixed
+        // across its loads)
         uint32_t at[T::kPerVec];
+        if constexpr (kShifted) {
+            // from span index V*t + k - d, made non-negative by adding V*S.
+            // For thread 0 with d > 0 the first columns are -1 or less: the
+            // offset wraps modulo 2^32, and only that thread's later loads
+            // use it, whose columns (+ i*kColStep) are back at 0 or more
 #pragma unroll
-        for (int k = 0; k < T::kPerVec; ++k) {
-            uint32_t r = r0 + k, c = c0;
-#pragma unroll
-            for (int w = 0; w < T::kWraps; ++w) {
-                const bool wrap = r >= S;
-                r = wrap ? r - S : r;
-                c = wrap ? c + 1 : c;
+            for (int k = 0; k < T::kPerVec; ++k) {
+                const uint32_t jp = T::kPerVec * threadIdx.x + k - d + T::kPerVec * S;
+                at[k] = (jp % S) * pitch + jp / S - T::kPerVec;
             }
-            at[k] = r * pitch + c;
+        } else {
+            const uint32_t j = T::kPerVec * threadIdx.x;
+            const uint32_t r0 = j % S, c0 = j / S;
+#pragma unroll
+            for (int k = 0; k < T::kPerVec; ++k) {
+                uint32_t r = r0 + k, c = c0;
+#pragma unroll
+                for (int w = 0; w < T::kWraps; ++w) {
+                    const bool wrap = r >= S;
+                    r = wrap ? r - S : r;
+                    c = wrap ? c + 1 : c;
+                }
+                at[k] = r * pitch + c;
+            }
         }
 #pragma unroll
         for (int i = 0; i < T::kLoads; ++i) {
+            if (kShifted && i == 0 && d != 0 && threadIdx.x == 0) continue;
 #pragma unroll
             for (int k = 0; k < T::kPerVec; ++k) {
                 const uint32_t w = v[i].w[k * E / 4];
                 tile[at[k] + i * T::kColStep] = static_cast<W>(E == 4 ? w : w >> (16u * (k & 1)));
             }
+        }
+        if (kShifted && d != 0 && threadIdx.x < T::kPerVec) {  // span elements [0, V - d) and [span - d, span)
+            const uint32_t j = threadIdx.x < T::kPerVec - d ? threadIdx.x : T::kSpan - T::kPerVec + threadIdx.x;
+            tile[(j % S) * pitch + j / S] = src[j];
         }
     } else {
         const uint32_t avail = static_cast<uint32_t>(g.n - j0);  // fewer than kSpan
@@ -804,17 +837,17 @@ gather_tiled_fixed_kernel(const GatherArgs g) {
     }
 }
 
-template <int E, int S>
+template <int E, int S, bool kShifted>
 cudaError_t launch_gather_tiled_fixed(const GatherArgs &g, int grid, cudaStream_t s) {
     const size_t smem = static_cast<size_t>(S) * g.tile_pitch * E;
-    return launch_kernel(&gather_tiled_fixed_kernel<E, S>, grid, TiledFixed<E, S>::kThreads, smem, s, g);
+    return launch_kernel(&gather_tiled_fixed_kernel<E, S, kShifted>, grid, TiledFixed<E, S>::kThreads, smem, s, g);
 }
 
-template <int E, int S>
+template <int E, int S, bool kShifted>
 constexpr GatherEntry tiled_fixed_entry() {
     using T = TiledFixed<E, S>;
-    return GatherEntry{reinterpret_cast<const void *>(&gather_tiled_fixed_kernel<E, S>),
-                       &launch_gather_tiled_fixed<E, S>, T::kLoads, 0, T::kThreads,
+    return GatherEntry{reinterpret_cast<const void *>(&gather_tiled_fixed_kernel<E, S, kShifted>),
+                       &launch_gather_tiled_fixed<E, S, kShifted>, T::kLoads, 0, T::kThreads,
                        static_cast<uint32_t>(T::kP)};
 }
 

@@ -803,11 +803,12 @@ def test_gather_tiled(dtype):
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_gather_tiled_general_every_input_offset(dtype):
-    """The general tiled kernel stages each span with 16-byte loads from its
-    first 16-byte boundary and single elements around them: every input offset
-    within 16 bytes (offset 0 takes the specialised kernels where the stride
-    has one), strides with and without a specialised kernel, spans shorter
-    than the peeled head, spans clipped at n and ragged last blocks."""
+    """Tiled gathers on every input offset within 16 bytes: the general
+    kernel (power-of-two strides past a 16-byte boundary) stages each span
+    with 16-byte loads from its first 16-byte boundary and single elements
+    around them; the fixed-stride kernel (the other strides) shifts its loads
+    to the boundaries.  Spans shorter than the peeled head, spans clipped at n
+    and ragged last blocks."""
     L = ew.lib()
     e = ESIZE[dtype]
     ew.set_schedule("tiled")
@@ -1068,12 +1069,14 @@ def test_gather_pow2_full_size_2p26(dtype, s):
 
 
 @pytest.mark.parametrize("dtype,s,in_off", [("f32", 63, 0), ("bf16", 33, 0), ("bf16", 6, 0), ("f32", 12, 0),
-                                           ("f32", 40, 1), ("bf16", 17, 3)])
+                                           ("f32", 40, 1), ("bf16", 17, 3), ("bf16", 6, 7), ("f32", 16, 1),
+                                           ("bf16", 64, 5)])
 def test_gather_fixed_and_general_full_size_2p26(dtype, s, in_off):
     """The fixed-stride kernel at n = 2^26 (s = 63 and 33 with a partial last
-    warp, s = 6 and 12 with the larger register allowance) and the general
-    kernel on inputs 1 and 3 elements past 16 bytes: every output against the
-    oracle, with the block size the launch record reports."""
+    warp, s = 6 and 12 with the larger register allowance, s = 40, 17 and 6 on
+    inputs 1, 3 and 7 elements past 16 bytes) and the general kernel (power-of-
+    two strides on inputs past 16 bytes): every output against the oracle, with
+    the block size the launch record reports."""
     n = 1 << 26
     e = ESIZE[dtype]
     x = inputs.as_dtype(inputs.uniform(n, inputs.seed_for("copy_f32", 5), 0.0, 1.0), dtype)
@@ -1082,7 +1085,8 @@ def test_gather_fixed_and_general_full_size_2p26(dtype, s, in_off):
                                      _stream()) == 0
     rec = ew.last_launch()
     assert rec["schedule"] == 4 and rec["path"] == 2, rec
-    assert rec["block"] == (_fixed_block(s, e) if (in_off * e) % 16 == 0 else 256), rec
+    pow2 = s & (s - 1) == 0  # the power-of-two and the general kernels both run 256 threads
+    assert rec["block"] == (256 if pow2 else _fixed_block(s, e)), rec
     torch.cuda.synchronize()
     assert_bits_equal(bo.host(), oracle.gather_stride(x, s), dtype, False,
                       "gather %d 2^26 %s offset %d" % (s, dtype, in_off))
@@ -1134,7 +1138,7 @@ def _fixed_block(s, e):
         return whole
 
     def deviation(t):
-        target = 32768 if s >= 32 else 20480 if t >= 352 else 16384
+        target = 32768 if s >= 32 else 24576 if t >= 480 else 20480 if t >= 352 else 16384
         wpl = 1 if s >= t // 32 else (t // 32) // s
         align = 64 if e == 2 else 32
         for loads in range(max(target // (16 * t), 1), 65):
@@ -1157,7 +1161,8 @@ def test_gather_tiled_fixed_strides(dtype):
     16-byte aligned input, with the block size chosen per stride: one ragged
     block, one and several full spans, spans plus a ragged block, n divisible
     by the stride and not, output offsets that start laps on odd and even
-    elements.  A 2-byte input offset takes the general tiled kernel."""
+    elements.  An input offset of 2 or 4 bytes runs the same kernel with its
+    loads shifted to the 16-byte boundaries."""
     L = ew.lib()
     code = DT_CODE[dtype]
     e = ESIZE[dtype]
@@ -1176,7 +1181,7 @@ def test_gather_tiled_fixed_strides(dtype):
                     aligned = (in_off * e) % 16 == 0
                     assert rec["schedule"] == 4, (n, s, rec)
                     assert rec["path"] == 2 and rec["vec_bytes"] == 16, rec  # general kernel too: 16-byte staging
-                    assert rec["block"] == (_fixed_block(s, e) if aligned else 256), rec
+                    assert rec["block"] == _fixed_block(s, e), rec  # any offset: shifted loads
                     torch.cuda.synchronize()
                     assert_bits_equal(bo.host(), oracle.gather_stride(x, stride), bits, False,
                                       "fixed tiled gather %s n=%d s=%d offs=%d,%d"
