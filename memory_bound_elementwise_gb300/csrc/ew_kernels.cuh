@@ -282,7 +282,8 @@ __global__ void __launch_bounds__(kBlock) gather_tiled_kernel(const GatherArgs g
         }
     }
     // Single elements: the head [0, h) and the ragged end [done, avail), fewer
-    // than 2 * kPerVec in all.
+    // than 2 * kPerVec in all.  (Loading them ahead of the vector loads made
+    // this kernel 1-3% slower.)
     const uint32_t rest = h + (avail - done);
     if (threadIdx.x < rest) {
         const uint32_t j = threadIdx.x < h ? threadIdx.x : done + (threadIdx.x - h);
@@ -764,6 +765,13 @@ gather_tiled_fixed_kernel(const GatherArgs g) {
         for (int i = 0; i < T::kLoads; ++i)
             if (!kShifted || i > 0 || d == 0 || threadIdx.x > 0)
                 v[i] = ld<16>(src_bytes + (threadIdx.x + i * T::kThreads) * 16u);
+        // span elements [0, V - d) and [span - d, span), staged singly: loaded
+        // here, with the vector loads, so that their latency overlaps
+        const bool single = kShifted && d != 0 && threadIdx.x < T::kPerVec;
+        const uint32_t single_j =
+            threadIdx.x < T::kPerVec - d ? threadIdx.x : T::kSpan - T::kPerVec + threadIdx.x;
+        W single_v = 0;
+        if (single) single_v = src[single_j];
         // offsets of this thread's V elements in its first load (rows fixed
         // across its loads)
         uint32_t at[T::kPerVec];
@@ -801,10 +809,7 @@ gather_tiled_fixed_kernel(const GatherArgs g) {
                 tile[at[k] + i * T::kColStep] = static_cast<W>(E == 4 ? w : w >> (16u * (k & 1)));
             }
         }
-        if (kShifted && d != 0 && threadIdx.x < T::kPerVec) {  // span elements [0, V - d) and [span - d, span)
-            const uint32_t j = threadIdx.x < T::kPerVec - d ? threadIdx.x : T::kSpan - T::kPerVec + threadIdx.x;
-            tile[(j % S) * pitch + j / S] = src[j];
-        }
+        if (single) tile[(single_j % S) * pitch + single_j / S] = single_v;
     } else {
         const uint32_t avail = static_cast<uint32_t>(g.n - j0);  // fewer than kSpan
         for (uint32_t j = threadIdx.x; j < avail; j += T::kThreads) tile[(j % S) * pitch + j / S] = src[j];
