@@ -498,9 +498,10 @@ constexpr uint64_t kOneshotMaxN = uint64_t(1) << 32;  // the 32-bit index kernel
 // 6101, 5941, 5463 in lap order), and lap order stays 2-3% ahead below that.
 // For 2-byte elements the tiled kernels win from s = 2: at s = 2, 3 and 4
 // the kernels specialised for the stride on a 16-byte aligned input (bf16:
-// 5974, 5866, 5996 GB/s against 5358, 4998, 5239 in lap order), and the
-// general one on an input past a 16-byte boundary (5689, 5266, 5684 against
-// 5418, 4987, 5246).
+// 5974, 5866, 5996 GB/s against 5358, 4998, 5239 in lap order), and on an
+// input past a 16-byte boundary the general kernel at s = 2 and 4 (5686,
+// 5701 against 5375, 5235) and the fixed-stride kernel's shifted instance at
+// s = 3 (5906 against 4973).
 bool auto_tiled(int e, uint64_t s_mod) { return s_mod >= (e == 2 ? 2u : 5u); }
 
 GatherArgs gather_args(const void *in, void *out, uint64_t n, uint64_t s_mod) {

@@ -215,9 +215,9 @@ __global__ void __launch_bounds__(kBlock) gather_laps_kernel(const GatherArgs g)
 // last whole vector.  It writes the span to shared memory transposed:
 // element j goes to row j mod s, column j / s.  Row r then holds, in position
 // order, the sources of every lap with r_L = r, so each lap's outputs leave as
-// one coalesced run.  Rows are padded so that a warp's 32 consecutive
-// elements spread over the banks.  Unlike the lap kernel, every input element
-// is loaded once per block, whether one lap, several or none use it.
+// one coalesced run.  Rows are padded (the pad searched on the host for the
+// bank spread of these staging stores).  Unlike the lap kernel, every input
+// element is loaded once per block, whether one lap, several or none use it.
 template <int E, int U>
 __global__ void __launch_bounds__(kBlock) gather_tiled_kernel(const GatherArgs g) {
     enter_grid();
