@@ -499,9 +499,8 @@ constexpr uint64_t kOneshotMaxN = uint64_t(1) << 32;  // the 32-bit index kernel
 // For 2-byte elements the tiled kernels win from s = 2: at s = 2, 3 and 4
 // the kernels specialised for the stride on a 16-byte aligned input (bf16:
 // 5974, 5866, 5996 GB/s against 5358, 4998, 5239 in lap order), and on an
-// input past a 16-byte boundary the general kernel at s = 2 and 4 (5686,
-// 5701 against 5375, 5235) and the fixed-stride kernel's shifted instance at
-// s = 3 (5906 against 4973).
+// input past a 16-byte boundary the fixed-stride kernel's shifted instances
+// (5948, 5906, 6045 against 5375, 4973, 5235).
 bool auto_tiled(int e, uint64_t s_mod) { return s_mod >= (e == 2 ? 2u : 5u); }
 
 GatherArgs gather_args(const void *in, void *out, uint64_t n, uint64_t s_mod) {
@@ -567,10 +566,11 @@ GatherLaunch plan_gather_span(const void *in, void *out, uint64_t n, uint64_t s_
 // draw from staged in shared memory, rows padded.  On a 16-byte aligned input
 // a power-of-two stride (2 to 64) takes the kernel specialised for it; every
 // other stride (3 to 63) takes the fixed-stride kernel on any input (its
-// shifted instance past a 16-byte boundary); a power-of-two stride on an
-// unaligned input the general kernel (P a power of two, span up to 20 KiB
-// unless that leaves lap runs under 512 bytes).  All stage with 16-byte
-// loads (the launch record shows EW_PATH_V128 and vec_bytes 16).
+// shifted instance past a 16-byte boundary), and so do 2-byte elements at
+// s = 2, 4 and 8 past a 16-byte boundary; the other powers of two there take
+// the general kernel (P a power of two, span up to 20 KiB unless that leaves
+// lap runs under 512 bytes).  All stage with 16-byte loads (the launch record
+// shows EW_PATH_V128 and vec_bytes 16).
 GatherLaunch plan_gather_tiled(int e, const void *in, void *out, uint64_t n, uint64_t s_mod) {
     GatherLaunch gl;
     const GatherEntry *pow2 = e == 4 ? gather_tiled_pow2_4(s_mod) : gather_tiled_pow2_2(s_mod);

@@ -130,8 +130,9 @@ const GatherEntry *gather_tiled_pow2_2(uint64_t stride);
 // Tiled gather specialised for a fixed stride that is not a power of two
 // (every stride from 3 to 63 but 4, 8, 16, 32), on any element-aligned
 // input; shifted selects the instance for an input that is not 16-byte
-// aligned.  The block size is chosen per stride, the row pitch
-// (args.tile_pitch) by the host.  nullptr for other strides.
+// aligned, which also exists for 2-byte elements at s = 2, 4 and 8.  The block
+// size is chosen per stride, the row pitch (args.tile_pitch) by the host.
+// nullptr for other strides.
 const GatherEntry *gather_tiled_fixed(int e, uint64_t stride, bool shifted);
 const GatherEntry *gather_tiled_fixed_wide(int e, uint64_t stride, bool shifted);  // strides 33 to 63
 const GatherEntry *gather_oneshot_4();  // binary32, n <= 2^32

@@ -1070,13 +1070,14 @@ def test_gather_pow2_full_size_2p26(dtype, s):
 
 @pytest.mark.parametrize("dtype,s,in_off", [("f32", 63, 0), ("bf16", 33, 0), ("bf16", 6, 0), ("f32", 12, 0),
                                            ("f32", 40, 1), ("bf16", 17, 3), ("bf16", 6, 7), ("f32", 16, 1),
-                                           ("bf16", 64, 5)])
+                                           ("bf16", 64, 5), ("bf16", 4, 3)])
 def test_gather_fixed_and_general_full_size_2p26(dtype, s, in_off):
     """The fixed-stride kernel at n = 2^26 (s = 63 and 33 with a partial last
     warp, s = 6 and 12 with the larger register allowance, s = 40, 17 and 6 on
     inputs 1, 3 and 7 elements past 16 bytes) and the general kernel (power-of-
-    two strides on inputs past 16 bytes): every output against the oracle, with
-    the block size the launch record reports."""
+    two strides on inputs past 16 bytes, but 2-byte elements at s = 4, which
+    take the fixed-stride kernel's shifted instance): every output against the
+    oracle, with the block size the launch record reports."""
     n = 1 << 26
     e = ESIZE[dtype]
     x = inputs.as_dtype(inputs.uniform(n, inputs.seed_for("copy_f32", 5), 0.0, 1.0), dtype)
@@ -1085,8 +1086,12 @@ def test_gather_fixed_and_general_full_size_2p26(dtype, s, in_off):
                                      _stream()) == 0
     rec = ew.last_launch()
     assert rec["schedule"] == 4 and rec["path"] == 2, rec
-    pow2 = s & (s - 1) == 0  # the power-of-two and the general kernels both run 256 threads
-    assert rec["block"] == (256 if pow2 else _fixed_block(s, e)), rec
+    # aligned powers of two: the power-of-two kernel; past 16 bytes the general
+    # kernel (both 256 threads), but for 2-byte elements at s = 2, 4, 8; every
+    # other case the fixed-stride one
+    pow2, aligned = s & (s - 1) == 0, (in_off * e) % 16 == 0
+    shifted_pow2 = pow2 and not aligned and e == 2 and s <= 8
+    assert rec["block"] == (256 if pow2 and not shifted_pow2 else _fixed_block(s, e)), rec
     torch.cuda.synchronize()
     assert_bits_equal(bo.host(), oracle.gather_stride(x, s), dtype, False,
                       "gather %d 2^26 %s offset %d" % (s, dtype, in_off))
