@@ -152,8 +152,9 @@ typedef enum {
  *                     shared memory with one row per residue mod s, then
  *                     writes each lap's outputs as one coalesced run.  For
  *                     every s from 2 to 64 on an input aligned to 16 bytes,
- *                     and for the s that are not powers of two on any
- *                     input, a kernel specialised for that stride runs
+ *                     and for the s that are not powers of two (and, for
+ *                     2-byte elements, s = 2, 4, 8) on any input, a kernel
+ *                     specialised for that stride runs
  *                     (division by s at compile time, staging stores at
  *                     fixed offsets, a padded shared-memory layout, warps
  *                     copying whole lap runs; the launch record shows
