@@ -296,6 +296,18 @@ typedef struct {
 } ew_launch_record;
 EW_API ew_status ew_last_launch(ew_launch_record *out);
 
+/* The launch record an ew_gather_stride call with these arguments would leave,
+ * under the current ew_set_path / ew_set_schedule selections (host arithmetic
+ * only; needs no GPU and reads neither buffer): which kernel schedule, its
+ * grid, block, dynamic shared memory and access width.  One exception: the
+ * grid of the grid-stride kernel (EW_SCHED_PERSISTENT, or n > 2^32), which
+ * depends on the device's SM count and occupancy, is reported as 0.  Returns
+ * what ew_gather_stride returns for the same arguments, without its optional
+ * pointer-kind check; n == 0 gives a record with launches = 0.  out_record:
+ * caller-owned; EW_ERR_NULL_POINTER when null. */
+EW_API ew_status ew_gather_plan_query(ew_dtype dtype, const void *in, const void *out, int64_t n,
+                                      int64_t stride, ew_launch_record *out_record);
+
 /* ---- errors ----------------------------------------------------------- */
 
 EW_API const char *ew_status_string(ew_status status);

@@ -48,7 +48,7 @@ EXPORTS = ("ew_add", "ew_saxpy", "ew_relu", "ew_add_relu", "ew_saxpy_relu", "ew_
            "ew_gather_stride", "ew_set_path", "ew_set_programmatic_launch",
            "ew_get_programmatic_launch",
            "ew_get_path", "ew_set_schedule", "ew_get_schedule", "ew_set_pointer_check",
-           "ew_plan_query", "ew_last_launch", "ew_status_string", "ew_last_cuda_error",
+           "ew_plan_query", "ew_last_launch", "ew_gather_plan_query", "ew_status_string", "ew_last_cuda_error",
            "ew_device_error", "ew_selftest_bounded_wait", "ew_version")
 
 
@@ -101,7 +101,7 @@ def lib():
     for name in ("ew_add", "ew_saxpy", "ew_relu", "ew_add_relu", "ew_saxpy_relu", "ew_select_even_odd", "ew_copy",
                  "ew_gather_stride",
                  "ew_set_path", "ew_set_schedule", "ew_set_pointer_check", "ew_plan_query",
-                 "ew_last_launch", "ew_device_error", "ew_selftest_bounded_wait"):
+                 "ew_last_launch", "ew_gather_plan_query", "ew_device_error", "ew_selftest_bounded_wait"):
         getattr(L, name).restype = ctypes.c_int
     L.ew_set_path.argtypes = [ctypes.c_int]
     L.ew_get_path.argtypes = []
@@ -117,6 +117,7 @@ def lib():
     L.ew_get_programmatic_launch.restype = ctypes.c_int
     L.ew_plan_query.argtypes = [ctypes.c_int, ctypes.POINTER(vp), i32, i64, ctypes.POINTER(Plan)]
     L.ew_last_launch.argtypes = [ctypes.POINTER(LaunchRecord)]
+    L.ew_gather_plan_query.argtypes = [ctypes.c_int, vp, vp, i64, i64, ctypes.POINTER(LaunchRecord)]
     L.ew_status_string.argtypes = [ctypes.c_int]
     L.ew_status_string.restype = ctypes.c_char_p
     L.ew_last_cuda_error.argtypes = []
@@ -285,6 +286,15 @@ def plan_query(dtype_code, ptrs, n):
     out = Plan()
     check(lib().ew_plan_query(dtype_code, arr, len(ptrs), int(n), ctypes.byref(out)), "ew_plan_query")
     return {k: getattr(out, k) for k, _ in Plan._fields_}
+
+
+def gather_plan_query(dtype_code, in_ptr, out_ptr, n, stride):
+    """The launch record an ew_gather_stride call would leave (host only; the
+    grid-stride kernel's grid is 0), as last_launch() returns it."""
+    rec = LaunchRecord()
+    check(lib().ew_gather_plan_query(dtype_code, in_ptr, out_ptr, int(n), int(stride), ctypes.byref(rec)),
+          "ew_gather_plan_query")
+    return rec.as_dict()
 
 
 def last_launch():

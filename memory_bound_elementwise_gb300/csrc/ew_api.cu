@@ -684,6 +684,55 @@ cudaError_t plan_gather_stride(int e, int dev, int sms, const void *in, void *ou
     return cudaSuccess;
 }
 
+// Argument checks of a gather call (the pointer-kind check aside).
+ew_status check_gather(ew_dtype dt, const void *in, const void *out, int64_t n, int64_t stride) {
+    const void *p[2] = {in, out};
+    const ew_status st = check_common(dt, n, p, 2);
+    if (st != EW_OK) return st;
+    if (stride <= 0) return EW_ERR_INVALID_VALUE;
+    if (n > 0 && overlaps(in, out, n * elem_size(dt))) return EW_ERR_OVERLAP;
+    return EW_OK;
+}
+
+// The launch a gather call makes (n > 0, arguments checked).  dev < 0: no
+// device to ask; the grid-stride kernel's grid, which depends on the SM count
+// and occupancy, is then left 0.
+cudaError_t plan_gather(int e, const void *in, const void *out, int64_t n, int64_t stride, int dev, int sms,
+                        GatherLaunch *gl) {
+    const uint64_t un = static_cast<uint64_t>(n);
+    const uint64_t s_mod = static_cast<uint64_t>(stride) % un;
+    void *o = const_cast<void *>(out);
+    switch (choose_gather(e, un, s_mod)) {
+        case GatherKind::SPAN: *gl = plan_gather_span(in, o, un, s_mod); break;
+        case GatherKind::TILED: *gl = plan_gather_tiled(e, in, o, un, s_mod); break;
+        case GatherKind::LAPS: *gl = plan_gather_laps(e, in, o, un, s_mod); break;
+        case GatherKind::ONESHOT: *gl = plan_gather_oneshot(e, in, o, un, s_mod); break;
+        case GatherKind::STRIDE:
+            if (dev >= 0) return plan_gather_stride(e, dev, sms, in, o, un, s_mod, gl);
+            gl->entry = e == 4 ? gather_stride_4() : gather_stride_2();
+            gl->vec_bytes = e;
+            gl->schedule = EW_SCHED_PERSISTENT;
+            gl->nvec = n;
+            break;
+    }
+    return cudaSuccess;
+}
+
+ew_launch_record record_of(const GatherLaunch &gl) {
+    ew_launch_record r{};
+    r.launches = 1;
+    r.path = gl.path;
+    r.vec_bytes = gl.vec_bytes;
+    r.grid = gl.grid;
+    r.block = gl.block;
+    r.smem = gl.smem;
+    r.schedule = gl.schedule;
+    r.head = gl.head;
+    r.nvec = gl.nvec;
+    r.tail = gl.tail;
+    return r;
+}
+
 }  // namespace
 
 bool ew::programmatic_launch() { return g_programmatic.load(std::memory_order_relaxed) != 0; }
@@ -771,42 +820,32 @@ ew_status ew_gather_stride(ew_dtype dt, const void *in, void *out, int64_t n, in
                            ew_stream_t s) {
     t_last = ew_launch_record{};
     const void *p[2] = {in, out};
-    ew_status st = check_common(dt, n, p, 2);
-    if (st != EW_OK) return st;
-    if (stride <= 0) return EW_ERR_INVALID_VALUE;
-    if (n == 0) return EW_OK;
-    if (overlaps(in, out, n * elem_size(dt))) return EW_ERR_OVERLAP;
+    ew_status st = check_gather(dt, in, out, n, stride);
+    if (st != EW_OK || n == 0) return st;
     if (pointer_check_enabled()) {
         if ((st = check_device_pointers(p, 2)) != EW_OK) return st;
     }
     int dev = 0, sms = 0;
     cudaError_t ce = device_info(&dev, &sms);
     if (ce != cudaSuccess) return cuda_fail(ce);
-    const int e = elem_size(dt);
-    const uint64_t un = static_cast<uint64_t>(n);
-    const uint64_t s_mod = static_cast<uint64_t>(stride) % un;
     GatherLaunch gl;
-    switch (choose_gather(e, un, s_mod)) {
-        case GatherKind::SPAN: gl = plan_gather_span(in, out, un, s_mod); break;
-        case GatherKind::TILED: gl = plan_gather_tiled(e, in, out, un, s_mod); break;
-        case GatherKind::LAPS: gl = plan_gather_laps(e, in, out, un, s_mod); break;
-        case GatherKind::ONESHOT: gl = plan_gather_oneshot(e, in, out, un, s_mod); break;
-        case GatherKind::STRIDE:
-            if ((ce = plan_gather_stride(e, dev, sms, in, out, un, s_mod, &gl)) != cudaSuccess) return cuda_fail(ce);
-            break;
-    }
+    if ((ce = plan_gather(elem_size(dt), in, out, n, stride, dev, sms, &gl)) != cudaSuccess) return cuda_fail(ce);
     ce = gl.entry->launch(gl.args, gl.grid, reinterpret_cast<cudaStream_t>(s));
     if (ce != cudaSuccess) return cuda_fail(ce);
-    t_last.launches = 1;
-    t_last.path = gl.path;
-    t_last.vec_bytes = gl.vec_bytes;
-    t_last.grid = gl.grid;
-    t_last.block = gl.block;
-    t_last.smem = gl.smem;
-    t_last.schedule = gl.schedule;
-    t_last.head = gl.head;
-    t_last.nvec = gl.nvec;
-    t_last.tail = gl.tail;
+    t_last = record_of(gl);
+    return EW_OK;
+}
+
+ew_status ew_gather_plan_query(ew_dtype dt, const void *in, const void *out, int64_t n, int64_t stride,
+                               ew_launch_record *out_record) {
+    if (out_record == nullptr) return EW_ERR_NULL_POINTER;
+    const ew_status st = check_gather(dt, in, out, n, stride);
+    if (st != EW_OK) return st;
+    *out_record = ew_launch_record{};
+    if (n == 0) return EW_OK;
+    GatherLaunch gl;
+    plan_gather(elem_size(dt), in, out, n, stride, -1, 0, &gl);  // no device: grid-stride grid left 0
+    *out_record = record_of(gl);
     return EW_OK;
 }
 

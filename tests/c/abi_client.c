@@ -46,6 +46,12 @@ static int host_mode(void) {
 
     ew_launch_record rec;
     EXPECT(ew_last_launch(&rec) == EW_OK && rec.launches == 0);
+    /* a gather plan, host only: stride 12 on 2^20 fp32 elements runs the
+       fixed-stride tiled kernel, 192 threads, 320 lap positions per block */
+    EXPECT(ew_gather_plan_query(EW_F32, q, q + (1 << 22), 1 << 20, 12, &rec) == EW_OK);
+    EXPECT(rec.launches == 1 && rec.schedule == EW_SCHED_TILED && rec.block == 192);
+    EXPECT(rec.grid == ((1 << 20) / 12 + 1 + 319) / 320 && rec.vec_bytes == 16);
+    EXPECT(ew_gather_plan_query(EW_F32, q, q + (1 << 22), 1 << 20, 12, NULL) == EW_ERR_NULL_POINTER);
     printf("host ok\n");
     return 0;
 }

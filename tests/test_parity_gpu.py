@@ -11,7 +11,6 @@ stride-2 gather at 2^26; and the bench's further workloads: bf16 add at
 stride-16 gather at 2^26.
 The bar is bit-exact; NaN results of arithmetic compare as "both NaN".
 """
-import math
 
 import numpy as np
 import pytest
@@ -20,6 +19,7 @@ import torch
 import memory_bound_elementwise_gb300 as ew
 import oracle
 from memory_bound_elementwise_gb300 import inputs
+from tests.gather_geometry import fixed_block
 from tests.gpu_util import GuardedBuffer, assert_bits_equal, ESIZE
 
 pytestmark = pytest.mark.gpu
@@ -1091,7 +1091,7 @@ def test_gather_fixed_and_general_full_size_2p26(dtype, s, in_off):
     # other case the fixed-stride one
     pow2, aligned = s & (s - 1) == 0, (in_off * e) % 16 == 0
     shifted_pow2 = pow2 and not aligned and e == 2 and s <= 8
-    assert rec["block"] == (256 if pow2 and not shifted_pow2 else _fixed_block(s, e)), rec
+    assert rec["block"] == (256 if pow2 and not shifted_pow2 else fixed_block(s, e)), rec
     torch.cuda.synchronize()
     assert_bits_equal(bo.host(), oracle.gather_stride(x, s), dtype, False,
                       "gather %d 2^26 %s offset %d" % (s, dtype, in_off))
@@ -1127,37 +1127,6 @@ def test_gather_random_cases(dtype):
 FIXED_STRIDES = tuple(s for s in range(3, 64) if s & (s - 1))  # every stride up to 63 but the powers of two
 
 
-def _fixed_block(s, e):
-    """Threads per block of the fixed-stride kernel.  T must be a multiple of
-    the row period s / gcd(s, V) (V = 16 / e elements per load).  Whole warps:
-    the smallest multiple of lcm(32, period) from 192 (384 from s = 32) if at
-    most 512; else the multiple of the period up to 512 whose span (loads per
-    thread x 16 x T, from the target up until each warp's run share is whole
-    4-byte words) comes nearest the target, whole warps breaking ties."""
-    v = 16 // e
-    period = s // math.gcd(s, v)
-    least = 384 if s >= 32 else 192
-    lcm = math.lcm(32, period)
-    whole = -(-least // lcm) * lcm
-    if whole <= 512:
-        return whole
-
-    def deviation(t):
-        target = 32768 if s >= 32 else 24576 if t >= 480 else 20480 if t >= 352 else 16384
-        wpl = 1 if s >= t // 32 else (t // 32) // s
-        align = 64 if e == 2 else 32
-        for loads in range(max(target // (16 * t), 1), 65):
-            if (loads * v * t // s) % (align * wpl) == 0:
-                return abs(loads * 16 * t - target)
-        return 1 << 30
-    best = None
-    for t in range(-(-least // period) * period, 513, period):
-        if best is None or deviation(t) < deviation(best) or (
-                deviation(t) == deviation(best) and t % 32 == 0 and best % 32 != 0):
-            best = t
-    return best
-
-
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16", "i32"])
 def test_gather_tiled_fixed_strides(dtype):
     """The tiled gather specialised for fixed strides that are not powers of
@@ -1186,7 +1155,7 @@ def test_gather_tiled_fixed_strides(dtype):
                     aligned = (in_off * e) % 16 == 0
                     assert rec["schedule"] == 4, (n, s, rec)
                     assert rec["path"] == 2 and rec["vec_bytes"] == 16, rec  # general kernel too: 16-byte staging
-                    assert rec["block"] == _fixed_block(s, e), rec  # any offset: shifted loads
+                    assert rec["block"] == fixed_block(s, e), rec  # any offset: shifted loads
                     torch.cuda.synchronize()
                     assert_bits_equal(bo.host(), oracle.gather_stride(x, stride), bits, False,
                                       "fixed tiled gather %s n=%d s=%d offs=%d,%d"
