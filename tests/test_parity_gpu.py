@@ -1162,3 +1162,33 @@ def test_gather_tiled_fixed_strides(dtype):
                                       % (dtype, n, stride, in_off, out_off))
                     assert bi.guards_intact() and bo.guards_intact()
     ew.set_schedule("auto")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_gather_plan_query_matches_the_launch(dtype):
+    """ew_gather_plan_query reports the launch record a real ew_gather_stride
+    call leaves, for each schedule, aligned and offset inputs and strides
+    taking each kernel (the grid-stride kernel's grid aside: the query leaves
+    it to the device)."""
+    L = ew.lib()
+    code = DT_CODE[dtype]
+    n = 300_007
+    x = inputs.random_bits(n, dtype, 7800)
+    try:
+        for sched in ("auto", "tiled", "laps", "oneshot", "persistent"):
+            ew.set_schedule(sched)
+            for s in (2, 3, 4, 8, 12, 16, 33, 64, 65):
+                for in_off in (0, 1, 3):
+                    bi = GuardedBuffer(n, dtype, in_off).fill(x)
+                    bo = GuardedBuffer(n, dtype, 0)
+                    want = ew.gather_plan_query(code, bi.view.data_ptr(), bo.view.data_ptr(), n, s)
+                    assert L.ew_gather_stride(code, bi.view.data_ptr(), bo.view.data_ptr(), n, s,
+                                              _stream()) == 0
+                    got = ew.last_launch()
+                    if got["schedule"] == 2:
+                        assert want["grid"] == 0 and got["grid"] > 0
+                        want["grid"] = got["grid"]
+                    assert got == want, (sched, s, in_off, got, want)
+            torch.cuda.synchronize()
+    finally:
+        ew.set_schedule("auto")
