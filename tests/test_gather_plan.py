@@ -42,8 +42,8 @@ def _expected(e, n, stride, in_off, sched):
     return 1, "oneshot", None
 
 
-def _check(dt, e, n, stride, in_off, sched):
-    rec = ew.gather_plan_query(dt, BASE + in_off * e, OUT, n, stride)
+def _check(dt, e, n, stride, in_off, sched, out=OUT):
+    rec = ew.gather_plan_query(dt, BASE + in_off * e, out, n, stride)
     schedule, kernel, p = _expected(e, n, stride, in_off, sched)
     where = (dt, n, stride, in_off, sched, rec)
     assert rec["launches"] == 1 and rec["schedule"] == schedule, where
@@ -106,3 +106,36 @@ def test_gather_plan_query_arguments():
     assert L.ew_gather_plan_query(0, BASE, OUT, 100, 3, None) == 2           # null record
     assert L.ew_gather_plan_query(9, BASE, OUT, 100, 3, rec) == 3            # dtype
     assert L.ew_gather_plan_query(0, BASE, BASE + 40, 100, 3, rec) == 4      # overlap
+
+
+try:  # the property test needs hypothesis; without it that test alone is skipped
+    from hypothesis import given, settings, strategies as st
+except ImportError:
+    given = None
+
+
+def _property(test):
+    if given is None:
+        @pytest.mark.skip(reason="hypothesis is not installed")
+        def skipped():
+            pass
+        return skipped
+    return settings(max_examples=600, deadline=None)(given(
+        dt=st.sampled_from([0, 1, 2, 3]),
+        n=st.one_of(st.integers(1, 5000), st.integers(1, 1 << 33), st.integers(1, 1 << 40)),
+        stride=st.one_of(st.integers(1, 80), st.integers(1, 1 << 41)),
+        in_off=st.integers(0, 7),
+        sched=st.sampled_from(["auto", "tiled", "laps", "oneshot", "persistent"]))(test))
+
+
+@_property
+def test_gather_plan_properties(dt, n, stride, in_off, sched):
+    """Random sizes up to 2^40, strides up to 2^41 (taken mod n), input offsets
+    and schedules: the plan follows the same rules."""
+    e = 4 if dt in (0, 3) else 2
+    in_off %= 16 // e
+    ew.set_schedule(sched)
+    try:
+        _check(dt, e, n, stride, in_off, sched, out=BASE + (1 << 43))  # clear of n * e <= 2^42 bytes
+    finally:
+        ew.set_schedule("auto")
